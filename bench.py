@@ -1,0 +1,405 @@
+"""Benchmark of one Medusa decode step (heads + top-s, tree build, tree attention through the
+synthetic layer, verification, acceptance, KV compaction) on the Vicuna-7B-shaped workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+Prints one JSON line.  `value` is whole-job decode steps per second with inputs resident in
+HBM; `e2e` is the same metric through the C ABI with the step's input copied from pinned
+host memory and its result read back every step.  Each step streams ~2.1 GB of weights,
+far more than the 129 MB L2, so no L2 flush is needed between steps.  Under torchrun every
+rank runs an independent replica of the workload (sequences are independent: no
+collective on the data path); timing is the max over ranks.  `--impl reference` times the
+fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic as S  # noqa: E402
+
+METRIC = "Medusa verify steps/s and tree-nodes/s on 1 GB300; HBM GB/s vs ~8 TB/s peak"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def config_of(w: S.Workload, n1: int):
+    return {"workload": w.name, "B": w.B, "d": w.d, "V": w.V, "K": w.K,
+            "heads": f"{w.Hq}q/{w.Hkv}kv x {w.dh}", "prefix": list(sorted(set(w.lengths))),
+            "tree_nodes": n1, "tree": f"{w.tree} top-{max(w.s)}", "mode": w.mode,
+            "temperature": w.temperature, "paged": bool(w.page_size),
+            "l2": "no flush: each step streams the weights (> 2 GB) through the 129 MB L2"}
+
+
+# ----------------------------------------------------------------------- byte model
+def kernel_bytes(w: S.Workload, n1: int, tc_heads: bool):
+    """Algorithmic HBM bytes per launch of each kernel (weights and caches read once,
+    activations and outputs at their stored widths)."""
+    es = 4 if w.dtype == "f32" else 2
+    B, d, V, K = w.B, w.d, w.V, w.K
+    M = B * n1
+    qd, kd = w.Hq * w.dh, w.Hkv * w.dh
+    act = 4 if tc_heads else 0          # bf16 hi + lo copies written next to fp32
+    kv_prefix = sum(w.lengths) * 2 * kd * es
+    return {
+        "heads_w1": K * d * d * es + B * d * 4 + B * K * d * (4 + act),
+        "heads_vocab": (K + 1) * V * d * es + B * (K + 1) * d * 4 + B * (K + 1) * V * 4,
+        "layer_qkv": (qd + 2 * kd) * d * es + M * d * 2 + M * (qd + 2 * kd) * 4,
+        "tree_attention": kv_prefix + M * (qd * 4 + 2 * kd * es),
+        "layer_out": d * qd * es + M * qd * 4 + M * d * (2 + 4 + 4),
+        "verify_logits": V * d * es + M * d * 4 + M * V * 4,
+    }
+
+
+def step_bytes(w: S.Workload, n1: int):
+    """Bytes the method itself must move per step: head weights, LM head (for the root and
+    for verification), the KV prefix, the tree nodes' K/V written and read, and the
+    synthetic layer's weights."""
+    es = 4 if w.dtype == "f32" else 2
+    d, V, K = w.d, w.V, w.K
+    qd, kd = w.Hq * w.dh, w.Hkv * w.dh
+    heads = K * d * d * es + K * V * d * es
+    lm = 2 * V * d * es
+    kv = sum(w.lengths) * 2 * kd * es + w.B * n1 * 2 * kd * es * 2
+    layer = (qd + 2 * kd + qd) * d * es + w.B * n1 * d * es
+    return heads + lm + kv + layer
+
+
+# ----------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            self.sel = vis.split(",")[device_index] if vis else str(device_index)
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.sel, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------- setup
+def setup(w: S.Workload, device):
+    from medusa_head_speculative_gb300 import binding as Bnd
+    if not os.path.exists(Bnd.LIB_PATH):
+        from medusa_head_speculative_gb300 import build
+        build.build()
+    if w.tree == "cartesian":
+        parent, rank = Bnd.tree_cartesian(w.s)
+    else:
+        parent, rank = Bnd.tree_greedy(w.s, S.score_table(w.K, max(w.s)), w.N)
+    dtype = Bnd.F32 if w.dtype == "f32" else Bnd.BF16
+    plan = Bnd.Plan(w.B, w.d, w.V, w.K, w.Hq, w.Hkv, w.dh, dtype, w.capacity, w.s, parent, rank,
+                    rope_base=w.rope_base, page_size=w.page_size,
+                    num_pages=w.B * w.pages_per_seq if w.page_size else 0)
+    wts_cpu = S.weights(w)
+    wts = {k: v.to(device) for k, v in wts_cpu.items()}
+    h_cpu = S.hidden(w)
+    kc, vc, pt = S.kv_cache(w)
+    st = dict(plan=plan, wts=wts, wts_cpu=wts_cpu, h_cpu=h_cpu, h=h_cpu.to(device),
+              kc=kc.to(device), vc=vc.to(device), pt=None if pt is None else pt.to(device),
+              length=torch.tensor(w.lengths, dtype=torch.int32, device=device),
+              len_out=torch.empty(w.B, dtype=torch.int32, device=device),
+              ws=torch.empty(plan.workspace_size, dtype=torch.uint8, device=device),
+              parent=parent, rank=rank)
+    i32 = dict(dtype=torch.int32, device=device)
+    st["out"] = dict(out_tok=torch.empty(w.B, w.K + 1, **i32), n_acc=torch.empty(w.B, **i32),
+                     path=torch.empty(w.B, w.K + 1, **i32),
+                     h_next=torch.empty(w.B, w.d, dtype=torch.float32, device=device),
+                     root_next=torch.empty(w.B, **i32))
+    o = st["out"]
+    st["wstruct"] = Bnd.weights_struct(wts)
+    st["kv"] = Bnd.kv_struct(st["kc"], st["vc"], st["length"], st["len_out"], st["pt"])
+    st["acc"] = Bnd.accept_struct(w.mode, w.temperature, w.eps, w.delta)
+    st["outs"] = Bnd.outputs_struct(o["out_tok"], o["n_acc"], o["path"], o["h_next"], o["root_next"])
+    return st
+
+
+def run_ours(args, w: S.Workload):
+    from medusa_head_speculative_gb300 import binding as Bnd
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    st = setup(w, device)
+    plan = st["plan"]
+    stream = torch.cuda.current_stream(device)
+
+    def one_step():
+        Bnd.step(plan, st["h"], None, st["wstruct"], st["kv"], st["acc"], st["outs"], st["ws"],
+                 stream)
+
+    def barrier():
+        torch.cuda.synchronize(device)
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        one_step()
+    torch.cuda.synchronize(device)
+    assert plan.status() == 0, "device status word set during warm-up"
+
+    # launches per step, from one profiled step
+    plan.profile_start(256)
+    one_step()
+    _, per_step = plan.profile_stop()
+
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier()
+    clocks.start()
+    time.sleep(0.3)                      # let the sampler attach before the region starts
+    plan.profile_start(K * per_step + 16)
+    e0.record(stream)
+    for _ in range(K):
+        one_step()
+    e1.record(stream)
+    barrier()
+    kernels, launches = plan.profile_stop()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    assert plan.status() == 0, "device status word set during the timed region"
+    n_acc_mean = float(st["out"]["n_acc"].float().mean())
+
+    # end to end: h_t from pinned host memory, result (tokens, counts) back, every step
+    ke = min(K, 500)
+    h_host = st["h_cpu"].pin_memory()
+    tok_host = torch.empty(w.B, w.K + 1, dtype=torch.int32).pin_memory()
+    nacc_host = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    h_dev = st["h"]
+    barrier()
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(ke):
+        h_dev.copy_(h_host, non_blocking=True)
+        one_step()
+        tok_host.copy_(st["out"]["out_tok"], non_blocking=True)
+        nacc_host.copy_(st["out"]["n_acc"], non_blocking=True)
+        stream.synchronize()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    wall = time.perf_counter() - t0
+    te = torch.tensor([max(e2e_ms, wall * 1e3)], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_ms = float(te.item())
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    n1 = plan.n1
+    hbm, hbm_kind = peaks()
+    kb = kernel_bytes(w, n1, plan_tc_heads(w))
+    ktab = {}
+    for name, (cnt, tot) in kernels.items():
+        us = tot * 1e3 / cnt
+        row = {"launches": cnt, "us_per_launch": round(us, 3),
+               "share": round(tot / sum(v[1] for v in kernels.values()), 4)}
+        if name in kb:
+            row["gbs"] = round(kb[name] / (us * 1e-6) / 1e9, 1)
+        ktab[name] = row
+    dom = max((n for n in kernels if n in kb), key=lambda n: kernels[n][1])
+    dom_us = kernels[dom][1] * 1e3 / kernels[dom][0]
+    achieved = kb[dom] / (dom_us * 1e-6) / 1e9
+    traffic = load_traffic(w.name, dom)
+    steps_per_s = world * K / (ms_max / 1e3)
+    sb = step_bytes(w, n1)
+    res = {
+        "metric": METRIC, "value": round(steps_per_s, 2), "unit": "steps/s", "n_gpus": world,
+        "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_max / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic: seeded N(0,1/d) weights, N(0,1) h_t and KV prefix (no trained weights)",
+        "config": config_of(w, n1),
+        "tree_nodes_per_s": round(steps_per_s * w.B * n1, 1),
+        "step_hbm_gbs": round(sb / (ms_max / K * 1e-3) / 1e9, 1),
+        "step_hbm_frac": round(sb / (ms_max / K * 1e-3) / 1e9 / hbm, 4),
+        "step_bytes": sb,
+        "mean_tokens_per_step": round(n_acc_mean, 3),
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": traffic, "algorithmic_bytes": kb[dom],
+                     "peak_source": f"{hbm_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if hbm_kind == "measured" else "fallback 6.8 TB/s"},
+        "kernels": ktab,
+        "e2e": {"value": round(world * ke / (e2e_ms / 1e3), 2), "unit": "steps/s",
+                "h2d_bytes_per_step": int(h_host.numel() * 4),
+                "d2h_bytes_per_step": int(tok_host.numel() * 4 + nacc_host.numel() * 4)},
+        "clocks": clk,
+        "gpu_launches": int(launches),
+    }
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, st, plan_spec=(st["parent"], st["rank"]))
+    if dist is not None:
+        dist.destroy_process_group()
+    return res
+
+
+def plan_tc_heads(w: S.Workload):
+    return w.dtype == "bf16" and w.B > 4
+
+
+def load_traffic(workload: str, kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if one exists for
+    this workload and kernel (profiles/<kernel>__<workload>.json); else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get("traffic_bytes_per_launch")
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------- oracle (CPU)
+def _oracle_sample_step(w, wts64, h_cpu, spec):
+    import oracle as O
+    k, v = S.kv_prefix(w, 0)
+    dims = {"Hq": w.Hq, "Hkv": w.Hkv, "dh": w.dh, "rope_base": w.rope_base}
+    acc = {"mode": w.mode, "temperature": w.temperature, "eps": w.eps, "delta": w.delta}
+    t0 = time.perf_counter()
+    O.medusa_step(wts64, h_cpu[0], k, v, spec, dims, acc, s=list(w.s))
+    return time.perf_counter() - t0
+
+
+def _oracle_spec(w):
+    import oracle as O
+    if w.tree == "cartesian":
+        return O.cartesian_tree(w.s)
+    return O.greedy_tree(S.score_table(w.K, max(w.s)), w.s, w.N)
+
+
+def cpu_baseline(w, st, plan_spec=None):
+    import oracle as O
+    wts64 = O.oracle_weights(st["wts_cpu"])
+    spec = _oracle_spec(w)
+    secs = _oracle_sample_step(w, wts64, st["h_cpu"], spec)
+    per_step = secs * w.B               # sequences are independent: one is 1/B of a step
+    return {"value": round(1.0 / per_step, 5), "unit": "steps/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"one full oracle step of sequence 0 ({secs:.1f} s), scaled by B={w.B}"}
+
+
+def run_reference(args, w: S.Workload):
+    """The fp64 oracle on the host cores, on the same workload, metric and unit."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle as O
+    wts_cpu = S.weights(w)
+    wts64 = O.oracle_weights(wts_cpu)
+    h_cpu = S.hidden(w)
+    spec = _oracle_spec(w)
+    _oracle_sample_step(w, wts64, h_cpu, spec)          # one untimed warm-up step
+    budget_s = 120.0
+    times = []
+    for _ in range(args.steps):
+        times.append(_oracle_sample_step(w, wts64, h_cpu, spec))
+        if sum(times) > budget_s:
+            break
+    per_step = sum(times) / len(times) * w.B
+    v = 1.0 / per_step
+    return {"metric": METRIC, "value": round(v, 5), "unit": "steps/s", "impl": "reference",
+            "n_gpus": 0, "steps": len(times), "steps_requested": args.steps, "warmup": 1,
+            "ms_per_step": round(per_step * 1e3, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic: seeded N(0,1/d) weights, N(0,1) h_t and KV prefix",
+            "config": config_of(w, spec.N + 1),
+            "cpu_baseline": {"value": round(v, 5), "unit": "steps/s", "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": f"{len(times)} full oracle steps of sequence 0, scaled "
+                                       f"by B={w.B}; timed steps capped at ~{budget_s:.0f} s"},
+            "e2e": {"value": round(v, 5), "unit": "steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="vicuna7b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = S.workload(args.workload)
+    res = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

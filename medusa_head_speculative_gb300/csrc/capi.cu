@@ -1,0 +1,770 @@
+// C ABI of the Medusa decode step: validation, plan, workspace layout and the launch
+// sequences of the stages and of the whole step.  Every stage runs in this library's
+// kernels on the caller's stream; nothing here computes on the host.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <set>
+#include <utility>
+#include <vector>
+
+#include "../../include/medusa.h"
+#include "kernels.h"
+
+using namespace medusa;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+// Tracing: CUDA events around every kernel launch (enabled by medusa_profile_start).
+enum KernelName {
+  KN_H_SPLIT, KN_H_W1, KN_H_VOCAB, KN_TOPK_PARTIAL, KN_TOPK_MERGE, KN_TREE_BUILD, KN_GATHER,
+  KN_QKV, KN_ROPE, KN_ATTN, KN_COMBINE, KN_O_SPLIT, KN_OUT, KN_HP_SPLIT, KN_VLOGITS, KN_VSTATS,
+  KN_ACCEPT, KN_COMPACT, KN_COUNT
+};
+static const char* const kKernelNames[KN_COUNT] = {
+  "split_h", "heads_w1", "heads_vocab", "topk_partial", "topk_merge", "tree_build",
+  "embed_gather", "layer_qkv", "rope_split", "tree_attention", "attn_combine", "split_o",
+  "layer_out", "split_hprime", "verify_logits", "verify_stats", "verify_accept", "kv_compact"};
+
+struct Profiler {
+  bool on = false;
+  int used = 0;
+  std::vector<cudaEvent_t> ev;      // two per timed launch
+  std::vector<int> name;
+  void release() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    ev.clear();
+    name.clear();
+    used = 0;
+    on = false;
+  }
+};
+
+struct medusa_plan {
+  mutable Profiler prof;
+  medusa_dims d;
+  int K, N, n1, P, smax;
+  int s[MEDUSA_MAX_HEADS];
+  std::vector<int32_t> parent, rank, depth;
+  int32_t* d_spec = nullptr;        // device [3][n1]: parent, depth, rank
+  uint32_t* d_status = nullptr;
+  int device = 0, num_sms = 148;
+  bool tc_heads = false, tc_nodes = false;   // tensor-core projections
+  int M;                                     // node rows B * n1
+  int topk_splits, topk_chunk;
+  int nsplit, chunk, rpw, rows_per_block, nrb;
+  // workspace layout (byte offsets)
+  size_t o_logits, o_u, o_uhi, o_ulo, o_hhi, o_hlo, o_cv, o_ci, o_ttok, o_tval, o_root;
+  size_t o_tok, o_pos, o_mask, o_retr, o_x, o_qkv, o_q, o_tk, o_tv, o_po, o_pml;
+  size_t o_o, o_ohi, o_olo, o_hp, o_hphi, o_hplo, o_vlog, o_am, o_stats, o_path, o_nacc;
+  size_t o_otok, o_hnext, o_rnext;
+  size_t ws_bytes;
+
+  const int32_t* dparent() const { return d_spec; }
+  const int32_t* ddepth() const { return d_spec + n1; }
+  const int32_t* drank() const { return d_spec + 2 * n1; }
+  size_t esize() const { return d.dtype == MEDUSA_F32 ? 4 : 2; }
+};
+
+namespace {
+
+template <typename T> T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+medusa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MEDUSA_OK : MEDUSA_ERR_CUDA; }
+#define MEDUSA_TRY(x)                                  \
+  do {                                                 \
+    cudaError_t e_ = (x);                              \
+    if (e_ != cudaSuccess) return MEDUSA_ERR_CUDA;     \
+  } while (0)
+
+template <typename F>
+cudaError_t timed(const medusa_plan* p, int name, cudaStream_t st, F&& launch) {
+  Profiler& pr = p->prof;
+  if (!pr.on || pr.used >= (int)pr.name.size()) return launch();
+  const int i = pr.used++;
+  cudaEventRecord(pr.ev[2 * i], st);
+  cudaError_t e = launch();
+  cudaEventRecord(pr.ev[2 * i + 1], st);
+  pr.name[i] = name;
+  return e;
+}
+#define LAUNCH(p, kn, st, expr) MEDUSA_TRY(timed(p, kn, st, [&]() { return (expr); }))
+
+medusa_status check_dims(const medusa_dims* d) {
+  if (!d) return MEDUSA_ERR_INVALID;
+  if (d->B < 1 || d->d < 1 || d->V < 1 || d->K < 1 || d->Hq < 1 || d->Hkv < 1 || d->dh < 1)
+    return MEDUSA_ERR_INVALID;
+  if (d->Hq % d->Hkv != 0) return MEDUSA_ERR_INVALID;
+  if (d->dtype != MEDUSA_F32 && d->dtype != MEDUSA_BF16) return MEDUSA_ERR_INVALID;
+  if (d->capacity < 1 || d->page_size < 0 || !(d->rope_base > 0.f)) return MEDUSA_ERR_INVALID;
+  if (d->page_size > 0 && (d->capacity % d->page_size != 0 || d->num_pages < 1))
+    return MEDUSA_ERR_INVALID;
+  if (d->K > MEDUSA_MAX_HEADS) return MEDUSA_ERR_UNSUPPORTED;
+  if (d->dh != 32 && d->dh != 64 && d->dh != 128) return MEDUSA_ERR_UNSUPPORTED;
+  const int vec = d->dtype == MEDUSA_F32 ? 4 : 8;        // elements per 16-byte load
+  if (d->d % vec != 0) return MEDUSA_ERR_UNSUPPORTED;
+  return MEDUSA_OK;
+}
+
+medusa_status check_tree(const medusa_dims* d, const medusa_tree_spec* t, std::vector<int32_t>& depth) {
+  if (!t || !t->parent || !t->rank) return MEDUSA_ERR_INVALID;
+  if (t->K != d->K) return MEDUSA_ERR_INVALID;
+  if (t->N < 0) return MEDUSA_ERR_INVALID;
+  if (t->N + 1 > MEDUSA_MAX_NODES) return MEDUSA_ERR_UNSUPPORTED;
+  for (int k = 0; k < t->K; ++k) {
+    if (t->s[k] < 1 || t->s[k] > d->V) return MEDUSA_ERR_INVALID;
+    if (t->s[k] > MEDUSA_MAX_TOPS) return MEDUSA_ERR_UNSUPPORTED;
+  }
+  const int n1 = t->N + 1;
+  if (t->parent[0] != -1 || t->rank[0] != 0) return MEDUSA_ERR_INVALID;
+  depth.assign(n1, 0);
+  std::set<std::pair<int, int>> seen;
+  for (int n = 1; n < n1; ++n) {
+    const int p = t->parent[n];
+    if (p < 0 || p >= n) return MEDUSA_ERR_INVALID;
+    depth[n] = depth[p] + 1;
+    if (depth[n] > t->K) return MEDUSA_ERR_INVALID;
+    if (t->rank[n] < 0 || t->rank[n] >= t->s[depth[n] - 1]) return MEDUSA_ERR_INVALID;
+    if (!seen.insert({p, t->rank[n]}).second) return MEDUSA_ERR_INVALID;   // duplicate child
+  }
+  return MEDUSA_OK;
+}
+
+void layout(medusa_plan* p) {
+  const medusa_dims& d = p->d;
+  const size_t B = d.B, K = p->K, V = d.V, D = d.d, n1 = p->n1, M = p->M;
+  const size_t qd = (size_t)d.Hq * d.dh, kd = (size_t)d.Hkv * d.dh;
+  const size_t R = n1 * (d.Hq / d.Hkv);
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + std::max<size_t>(bytes, 1)); return o; };
+  p->o_logits = take(B * (K + 1) * V * 4);
+  p->o_u = take(B * K * D * 4);
+  p->o_uhi = take(p->tc_heads ? B * K * D * 2 : 0);
+  p->o_ulo = take(p->tc_heads ? B * K * D * 2 : 0);
+  p->o_hhi = take(p->tc_heads ? B * D * 2 : 0);
+  p->o_hlo = take(p->tc_heads ? B * D * 2 : 0);
+  p->o_cv = take(B * (K + 1) * p->topk_splits * kTops * 4);
+  p->o_ci = take(B * (K + 1) * p->topk_splits * kTops * 4);
+  p->o_ttok = take(B * K * kTops * 4);
+  p->o_tval = take(B * K * kTops * 4);
+  p->o_root = take(B * 4);
+  p->o_tok = take(B * n1 * 4);
+  p->o_pos = take(B * n1 * 4);
+  p->o_mask = take(n1 * kMaskWords * 4);
+  p->o_retr = take(n1 * (K + 1) * 4);
+  p->o_x = take(M * D * 4);
+  p->o_qkv = take(M * (qd + 2 * kd) * 4);
+  p->o_q = take(M * qd * 4);
+  p->o_tk = take(M * kd * p->esize());
+  p->o_tv = take(M * kd * p->esize());
+  p->o_po = take(B * d.Hkv * (p->nsplit + 1) * R * d.dh * 4);
+  p->o_pml = take(B * d.Hkv * (p->nsplit + 1) * R * 2 * 4);
+  p->o_o = take(M * qd * 4);
+  p->o_ohi = take(p->tc_nodes ? M * qd * 2 : 0);
+  p->o_olo = take(p->tc_nodes ? M * qd * 2 : 0);
+  p->o_hp = take(M * D * 4);
+  p->o_hphi = take(p->tc_nodes ? M * D * 2 : 0);
+  p->o_hplo = take(p->tc_nodes ? M * D * 2 : 0);
+  p->o_vlog = take(M * V * 4);
+  p->o_am = take(M * 4);
+  p->o_stats = take(M * 4 * 4);
+  p->o_path = take(B * (K + 1) * 4);
+  p->o_nacc = take(B * 4);
+  p->o_otok = take(B * (K + 1) * 4);
+  p->o_hnext = take(B * D * 4);
+  p->o_rnext = take(B * 4);
+  p->ws_bytes = off;
+}
+
+medusa_status check_ws(const medusa_plan* p, void* ws, size_t bytes) {
+  if (!ws || bytes < p->ws_bytes || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0)
+    return MEDUSA_ERR_WORKSPACE;
+  return MEDUSA_OK;
+}
+
+inline cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// ------------------------------------------------------------------ stage bodies
+medusa_status heads_impl(const medusa_plan* p, const float* h, const int32_t* root_in,
+                         const medusa_weights* w, float* logits, int32_t* ttok, float* tval,
+                         int32_t* root, void* ws, cudaStream_t st) {
+  const medusa_dims& d = p->d;
+  const int B = d.B, K = p->K, D = d.d, V = d.V;
+  const size_t es = p->esize();
+  float* u = at<float>(ws, p->o_u);
+  MatArgs a{};
+  // u_k = SiLU(W1_k h) + h, k = 1..K
+  a.nseg = K;
+  a.M = B;
+  a.k = D;
+  a.out = u;
+  a.ldo = (long)K * D;
+  a.epi = EPI_SILU_RES;
+  a.res_f32 = h;
+  a.ldr = D;
+  bf16* hhi = nullptr; bf16* hlo = nullptr;
+  if (p->tc_heads) {
+    hhi = at<bf16>(ws, p->o_hhi);
+    hlo = at<bf16>(ws, p->o_hlo);
+    LAUNCH(p, KN_H_SPLIT, st, launch_split(h, hhi, hlo, (long)B * D, st));
+    a.out_hi = at<bf16>(ws, p->o_uhi);
+    a.out_lo = at<bf16>(ws, p->o_ulo);
+  }
+  for (int k = 0; k < K; ++k) {
+    MatSeg& s = a.seg[k];
+    s.w = static_cast<const char*>(w->w1) + (size_t)k * D * D * es;
+    s.x = h; s.a_hi = hhi; s.a_lo = hlo; s.ldx = D;
+    s.rows = D;
+    s.out_off = k * D;
+  }
+  LAUNCH(p, KN_H_W1, st, p->tc_heads ? launch_mma_gemm(a, st) : launch_rowdot(a, d.dtype, st));
+  // z_0 = LM h, z_k = W2_k u_k
+  MatArgs b{};
+  b.nseg = K + 1;
+  b.M = B;
+  b.k = D;
+  b.out = logits;
+  b.ldo = (long)(K + 1) * V;
+  b.epi = EPI_STORE;
+  b.seg[0].w = w->lm;
+  b.seg[0].x = h; b.seg[0].a_hi = hhi; b.seg[0].a_lo = hlo; b.seg[0].ldx = D;
+  b.seg[0].rows = V;
+  b.seg[0].out_off = 0;
+  for (int k = 1; k <= K; ++k) {
+    MatSeg& s = b.seg[k];
+    s.w = static_cast<const char*>(w->w2) + (size_t)(k - 1) * V * D * es;
+    s.x = u + (size_t)(k - 1) * D;
+    s.a_hi = p->tc_heads ? at<bf16>(ws, p->o_uhi) + (size_t)(k - 1) * D : nullptr;
+    s.a_lo = p->tc_heads ? at<bf16>(ws, p->o_ulo) + (size_t)(k - 1) * D : nullptr;
+    s.ldx = (long)K * D;
+    s.rows = V;
+    s.out_off = k * V;
+  }
+  LAUNCH(p, KN_H_VOCAB, st, p->tc_heads ? launch_mma_gemm(b, st) : launch_rowdot(b, d.dtype, st));
+  TopkArgs t{logits, B, K + 1, V, p->topk_splits, p->topk_chunk, at<float>(ws, p->o_cv),
+             at<int32_t>(ws, p->o_ci)};
+  LAUNCH(p, KN_TOPK_PARTIAL, st, launch_topk_partial(t, st));
+  MergeArgs mg{at<float>(ws, p->o_cv), at<int32_t>(ws, p->o_ci), B, K, V, p->topk_splits,
+               root_in, ttok, tval, root, p->d_status};
+  LAUNCH(p, KN_TOPK_MERGE, st, launch_topk_merge(mg, st));
+  return MEDUSA_OK;
+}
+
+medusa_status tree_impl(const medusa_plan* p, const int32_t* ttok, const int32_t* root,
+                        const int32_t* len, int32_t* tok, int32_t* pos, uint32_t* mask,
+                        int32_t* retr, cudaStream_t st) {
+  TreeArgs a{ttok, root, len, p->d.B, p->K, p->d.V, p->n1, p->dparent(), p->ddepth(), p->drank(),
+             tok, pos, mask, retr, p->d_status};
+  LAUNCH(p, KN_TREE_BUILD, st, launch_tree_build(a, st));
+  return MEDUSA_OK;
+}
+
+// x = E[tok] into the workspace (fp32 for the CUDA-core path, bf16 for tensor cores)
+medusa_status gather_impl(const medusa_plan* p, const medusa_weights* w, const int32_t* tok,
+                          void* ws, cudaStream_t st) {
+  const medusa_dims& d = p->d;
+  float* xf = p->tc_nodes ? nullptr : at<float>(ws, p->o_x);
+  bf16* xb = p->tc_nodes ? at<bf16>(ws, p->o_x) : nullptr;
+  LAUNCH(p, KN_GATHER, st, launch_gather(w->emb, d.dtype, tok, p->M, d.d, d.V, xf, xb, st));
+  return MEDUSA_OK;
+}
+
+medusa_status qkv_impl(const medusa_plan* p, const medusa_weights* w, const int32_t* pos, float* q,
+                       void* tk, void* tv, void* ws, cudaStream_t st) {
+  const medusa_dims& d = p->d;
+  const int qd = d.Hq * d.dh, kd = d.Hkv * d.dh;
+  float* qkv = at<float>(ws, p->o_qkv);
+  MatArgs a{};
+  a.nseg = 3;
+  a.M = p->M;
+  a.k = d.d;
+  a.out = qkv;
+  a.ldo = qd + 2 * kd;
+  a.epi = EPI_STORE;
+  const void* ws_[3] = {w->wq, w->wk, w->wv};
+  const int rows[3] = {qd, kd, kd}, offs[3] = {0, qd, qd + kd};
+  for (int i = 0; i < 3; ++i) {
+    MatSeg& s = a.seg[i];
+    s.w = ws_[i];
+    s.x = p->tc_nodes ? nullptr : at<float>(ws, p->o_x);
+    s.a_hi = p->tc_nodes ? at<bf16>(ws, p->o_x) : nullptr;
+    s.a_lo = nullptr;                         // embedding rows are exact in bf16
+    s.ldx = d.d;
+    s.rows = rows[i];
+    s.out_off = offs[i];
+  }
+  LAUNCH(p, KN_QKV, st, p->tc_nodes ? launch_mma_gemm(a, st) : launch_rowdot(a, d.dtype, st));
+  LAUNCH(p, KN_ROPE, st, launch_rope_split(qkv, pos, p->M, d.Hq, d.Hkv, d.dh, d.rope_base, d.dtype, q, tk, tv, st));
+  return MEDUSA_OK;
+}
+
+medusa_status attn_impl(const medusa_plan* p, const float* q, const medusa_kv* kv, const void* tk,
+                        const void* tv, const uint32_t* mask, float* o, bool split_out, void* ws,
+                        cudaStream_t st) {
+  const medusa_dims& d = p->d;
+  AttnArgs a{};
+  a.q = q;
+  a.kc = kv->k;
+  a.vc = kv->v;
+  a.page_table = d.page_size > 0 ? kv->page_table : nullptr;
+  a.page_size = d.page_size > 0 ? d.page_size : 1;
+  a.pages_per_seq = d.page_size > 0 ? d.capacity / d.page_size : 0;
+  a.num_pages = d.num_pages;
+  a.len = kv->len;
+  a.capacity = d.capacity;
+  a.tk = tk;
+  a.tv = tv;
+  a.mask = mask;
+  a.B = d.B;
+  a.n1 = p->n1;
+  a.Hq = d.Hq;
+  a.Hkv = d.Hkv;
+  a.G = d.Hq / d.Hkv;
+  a.dh = d.dh;
+  a.nsplit = p->nsplit;
+  a.chunk = p->chunk;
+  a.rows_per_block = p->rows_per_block;
+  a.nrb = p->nrb;
+  a.rpw = p->rpw;
+  a.part_o = at<float>(ws, p->o_po);
+  a.part_ml = at<float>(ws, p->o_pml);
+  a.o = o;
+  a.o_hi = split_out && p->tc_nodes ? at<bf16>(ws, p->o_ohi) : nullptr;
+  a.o_lo = split_out && p->tc_nodes ? at<bf16>(ws, p->o_olo) : nullptr;
+  a.status = p->d_status;
+  a.scale = 1.0f / std::sqrt((float)d.dh);
+  LAUNCH(p, KN_ATTN, st, launch_tree_attention(a, d.dtype, st));
+  LAUNCH(p, KN_COMBINE, st, launch_attn_combine(a, st));
+  return MEDUSA_OK;
+}
+
+// h' = x + Wo o ; x gathered by gather_impl, o split to bf16 hi/lo when split_ready
+medusa_status out_impl(const medusa_plan* p, const medusa_weights* w, const float* o, bool split_ready,
+                       float* hp, bool want_split, void* ws, cudaStream_t st) {
+  const medusa_dims& d = p->d;
+  const int qd = d.Hq * d.dh;
+  MatArgs a{};
+  a.nseg = 1;
+  a.M = p->M;
+  a.k = qd;
+  a.out = hp;
+  a.ldo = d.d;
+  a.epi = EPI_RES_ADD;
+  a.ldr = d.d;
+  if (p->tc_nodes) {
+    if (!split_ready)
+      LAUNCH(p, KN_O_SPLIT, st, launch_split(o, at<bf16>(ws, p->o_ohi), at<bf16>(ws, p->o_olo), (long)p->M * qd, st));
+    a.res_w = at<bf16>(ws, p->o_x);
+    if (want_split) {
+      a.out_hi = at<bf16>(ws, p->o_hphi);
+      a.out_lo = at<bf16>(ws, p->o_hplo);
+    }
+  } else {
+    a.res_f32 = at<float>(ws, p->o_x);
+  }
+  MatSeg& s = a.seg[0];
+  s.w = w->wo;
+  s.x = o;
+  s.a_hi = p->tc_nodes ? at<bf16>(ws, p->o_ohi) : nullptr;
+  s.a_lo = p->tc_nodes ? at<bf16>(ws, p->o_olo) : nullptr;
+  s.ldx = qd;
+  s.rows = d.d;
+  s.out_off = 0;
+  LAUNCH(p, KN_OUT, st, p->tc_nodes ? launch_mma_gemm(a, st) : launch_rowdot(a, d.dtype, st));
+  return MEDUSA_OK;
+}
+
+VerifyArgs verify_args(const medusa_plan* p, const int32_t* tok, medusa_accept acc) {
+  VerifyArgs v{};
+  v.tok = tok;
+  v.parent = p->dparent();
+  v.depth = p->ddepth();
+  v.B = p->d.B;
+  v.n1 = p->n1;
+  v.V = p->d.V;
+  v.K = p->K;
+  v.P = p->P;
+  v.d = p->d.d;
+  v.typical = acc.mode == MEDUSA_TYPICAL && acc.temperature > 0.f;
+  v.temperature = v.typical ? acc.temperature : 1.f;
+  v.eps = acc.eps;
+  v.delta = acc.delta;
+  v.status = p->d_status;
+  return v;
+}
+
+medusa_status vlogits_impl(const medusa_plan* p, const medusa_weights* w, const float* hp,
+                           bool split_ready, const int32_t* tok, medusa_accept acc, float* logits,
+                           int32_t* am, float* stats, void* ws, cudaStream_t st) {
+  const medusa_dims& d = p->d;
+  MatArgs a{};
+  a.nseg = 1;
+  a.M = p->M;
+  a.k = d.d;
+  a.out = logits;
+  a.ldo = d.V;
+  a.epi = EPI_STORE;
+  if (p->tc_nodes && !split_ready)
+    LAUNCH(p, KN_HP_SPLIT, st, launch_split(hp, at<bf16>(ws, p->o_hphi), at<bf16>(ws, p->o_hplo), (long)p->M * d.d, st));
+  MatSeg& s = a.seg[0];
+  s.w = w->lm;
+  s.x = hp;
+  s.a_hi = p->tc_nodes ? at<bf16>(ws, p->o_hphi) : nullptr;
+  s.a_lo = p->tc_nodes ? at<bf16>(ws, p->o_hplo) : nullptr;
+  s.ldx = d.d;
+  s.rows = d.V;
+  s.out_off = 0;
+  LAUNCH(p, KN_VLOGITS, st, p->tc_nodes ? launch_mma_gemm(a, st) : launch_rowdot(a, d.dtype, st));
+  VerifyArgs v = verify_args(p, tok, acc);
+  v.logits = logits;
+  v.am = am;
+  v.stats = stats;
+  LAUNCH(p, KN_VSTATS, st, launch_verify_stats(v, st));
+  return MEDUSA_OK;
+}
+
+medusa_status accept_impl(const medusa_plan* p, const int32_t* tok, const int32_t* am,
+                          const float* stats, const int32_t* retr, const float* hp,
+                          medusa_accept acc, int32_t* out_tok, int32_t* n_acc, int32_t* path,
+                          float* h_next, int32_t* root_next, cudaStream_t st) {
+  VerifyArgs v = verify_args(p, tok, acc);
+  v.am = const_cast<int32_t*>(am);
+  v.stats = const_cast<float*>(stats);
+  v.retrieve = retr;
+  v.hprime = hp;
+  v.out_tok = out_tok;
+  v.n_acc = n_acc;
+  v.path_nodes = path;
+  v.h_next = h_next;
+  v.root_next = root_next;
+  LAUNCH(p, KN_ACCEPT, st, launch_verify_accept(v, st));
+  return MEDUSA_OK;
+}
+
+medusa_status compact_impl(const medusa_plan* p, const medusa_kv* kv, const void* tk, const void* tv,
+                           const int32_t* path, const int32_t* n_acc, cudaStream_t st) {
+  const medusa_dims& d = p->d;
+  CompactArgs c{};
+  c.kc = kv->k;
+  c.vc = kv->v;
+  c.page_table = d.page_size > 0 ? kv->page_table : nullptr;
+  c.page_size = d.page_size > 0 ? d.page_size : 1;
+  c.pages_per_seq = d.page_size > 0 ? d.capacity / d.page_size : 0;
+  c.num_pages = d.num_pages;
+  c.len = kv->len;
+  c.len_out = kv->len_out;
+  c.capacity = d.capacity;
+  c.tk = tk;
+  c.tv = tv;
+  c.path_nodes = path;
+  c.n_acc = n_acc;
+  c.B = d.B;
+  c.n1 = p->n1;
+  c.Hkv = d.Hkv;
+  c.dh = d.dh;
+  c.K = p->K;
+  c.dtype = d.dtype;
+  c.status = p->d_status;
+  LAUNCH(p, KN_COMPACT, st, launch_kv_compact(c, st));
+  return MEDUSA_OK;
+}
+
+medusa_status check_weights(const medusa_plan* p, const medusa_weights* w, bool heads, bool layer, bool lm) {
+  if (!w) return MEDUSA_ERR_INVALID;
+  if (heads && (!aligned16(w->w1) || !aligned16(w->w2))) return MEDUSA_ERR_INVALID;
+  if (lm && !aligned16(w->lm)) return MEDUSA_ERR_INVALID;
+  if (layer && (!aligned16(w->emb) || !aligned16(w->wq) || !aligned16(w->wk) || !aligned16(w->wv) ||
+                !aligned16(w->wo)))
+    return MEDUSA_ERR_INVALID;
+  (void)p;
+  return MEDUSA_OK;
+}
+
+medusa_status check_kv(const medusa_plan* p, const medusa_kv* kv, bool compact) {
+  if (!kv || !kv->k || !kv->v || !kv->len) return MEDUSA_ERR_INVALID;
+  if (p->d.page_size > 0 && !kv->page_table) return MEDUSA_ERR_INVALID;
+  if (compact && !kv->len_out) return MEDUSA_ERR_INVALID;
+  return MEDUSA_OK;
+}
+
+medusa_status check_accept(medusa_accept a) {
+  if (a.mode != MEDUSA_GREEDY && a.mode != MEDUSA_TYPICAL) return MEDUSA_ERR_INVALID;
+  if (a.mode == MEDUSA_TYPICAL) {
+    if (!(a.temperature >= 0.f) || !std::isfinite(a.temperature)) return MEDUSA_ERR_INVALID;
+    if (a.temperature > 0.f && (!(a.eps > 0.f) || !(a.delta > 0.f))) return MEDUSA_ERR_INVALID;
+  }
+  return MEDUSA_OK;
+}
+
+}  // namespace
+
+// ===================================================================== exported API
+extern "C" {
+
+medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec* tree,
+                                 medusa_plan** out) {
+  if (!out) return MEDUSA_ERR_INVALID;
+  *out = nullptr;
+  medusa_status s = check_dims(dims);
+  if (s != MEDUSA_OK) return s;
+  std::vector<int32_t> depth;
+  s = check_tree(dims, tree, depth);
+  if (s != MEDUSA_OK) return s;
+  medusa_plan* p = new (std::nothrow) medusa_plan();
+  if (!p) return MEDUSA_ERR_CUDA;
+  p->d = *dims;
+  p->K = dims->K;
+  p->N = tree->N;
+  p->n1 = tree->N + 1;
+  for (int k = 0; k < MEDUSA_MAX_HEADS; ++k) p->s[k] = k < p->K ? tree->s[k] : 0;
+  p->smax = *std::max_element(p->s, p->s + p->K);
+  p->parent.assign(tree->parent, tree->parent + p->n1);
+  p->rank.assign(tree->rank, tree->rank + p->n1);
+  p->depth = depth;
+  std::vector<int> haschild(p->n1, 0);
+  for (int n = 1; n < p->n1; ++n) haschild[p->parent[n]] = 1;
+  p->P = (int)std::count(haschild.begin(), haschild.end(), 0);
+  p->M = dims->B * p->n1;
+  p->tc_heads = dims->dtype == MEDUSA_BF16 && dims->B > 4;
+  p->tc_nodes = dims->dtype == MEDUSA_BF16;
+
+  cudaGetDevice(&p->device);
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) == cudaSuccess && sms > 0)
+    p->num_sms = sms;
+  // vocab slices for the top-k pass: <= 32 per head, at least 1024 logits each
+  p->topk_splits = std::max(1, std::min(32, (dims->V + 1023) / 1024));
+  p->topk_chunk = (dims->V + p->topk_splits - 1) / p->topk_splits;
+  // attention: query-row blocks and prefix splits so the grid covers the SMs ~2x
+  const int G = dims->Hq / dims->Hkv;
+  const int R = p->n1 * G;
+  p->rpw = R <= 32 ? 4 : (R <= 72 ? 9 : 12);
+  p->rows_per_block = 8 * p->rpw;
+  p->nrb = (R + p->rows_per_block - 1) / p->rows_per_block;
+  const int base = dims->B * dims->Hkv * p->nrb;
+  const int want = std::max(1, (2 * p->num_sms + base - 1) / base);
+  const int max_splits = std::max(1, (dims->capacity + 31) / 32);
+  p->nsplit = std::min(want, max_splits);
+  p->chunk = ((dims->capacity + p->nsplit - 1) / p->nsplit + 31) / 32 * 32;
+  p->nsplit = (dims->capacity + p->chunk - 1) / p->chunk;
+  layout(p);
+
+  std::vector<int32_t> spec(3 * p->n1);
+  for (int n = 0; n < p->n1; ++n) {
+    spec[n] = p->parent[n];
+    spec[p->n1 + n] = p->depth[n];
+    spec[2 * p->n1 + n] = p->rank[n];
+  }
+  if (cudaMalloc(&p->d_spec, spec.size() * sizeof(int32_t)) != cudaSuccess ||
+      cudaMalloc(&p->d_status, sizeof(uint32_t)) != cudaSuccess ||
+      cudaMemcpy(p->d_spec, spec.data(), spec.size() * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemset(p->d_status, 0, sizeof(uint32_t)) != cudaSuccess) {
+    medusa_plan_destroy(p);
+    return MEDUSA_ERR_CUDA;
+  }
+  *out = p;
+  return MEDUSA_OK;
+}
+
+void medusa_plan_destroy(medusa_plan* p) {
+  if (!p) return;
+  p->prof.release();
+  if (p->d_spec) cudaFree(p->d_spec);
+  if (p->d_status) cudaFree(p->d_status);
+  delete p;
+}
+
+size_t medusa_workspace_size(const medusa_plan* p) { return p ? p->ws_bytes : 0; }
+
+medusa_status medusa_profile_start(medusa_plan* p, int max_launches) {
+  if (!p || max_launches < 1) return MEDUSA_ERR_INVALID;
+  p->prof.release();
+  p->prof.ev.resize(2 * (size_t)max_launches);
+  p->prof.name.assign(max_launches, -1);
+  for (auto& e : p->prof.ev)
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      e = nullptr;
+      p->prof.release();
+      return MEDUSA_ERR_CUDA;
+    }
+  p->prof.on = true;
+  return MEDUSA_OK;
+}
+
+medusa_status medusa_profile_stop(medusa_plan* p, void* stream, medusa_kernel_time* out,
+                                  int max_kernels, int* n, int* launches) {
+  if (!p || !n || !launches || (max_kernels > 0 && !out)) return MEDUSA_ERR_INVALID;
+  if (cudaStreamSynchronize(S(stream)) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  std::vector<int> order, count(KN_COUNT, 0);
+  std::vector<double> ms(KN_COUNT, 0.0);
+  for (int i = 0; i < p->prof.used; ++i) {
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, p->prof.ev[2 * i], p->prof.ev[2 * i + 1]) != cudaSuccess) {
+      p->prof.release();
+      return MEDUSA_ERR_CUDA;
+    }
+    const int k = p->prof.name[i];
+    if (count[k]++ == 0) order.push_back(k);
+    ms[k] += t;
+  }
+  *launches = p->prof.used;
+  int m = 0;
+  for (int k : order) {
+    if (m >= max_kernels) break;
+    std::memset(out[m].name, 0, sizeof(out[m].name));
+    std::strncpy(out[m].name, kKernelNames[k], sizeof(out[m].name) - 1);
+    out[m].launches = count[k];
+    out[m].total_ms = ms[k];
+    ++m;
+  }
+  *n = m;
+  p->prof.release();
+  return MEDUSA_OK;
+}
+
+medusa_status medusa_get_status(const medusa_plan* p, void* stream, uint32_t* flags) {
+  if (!p || !flags) return MEDUSA_ERR_INVALID;
+  uint32_t v = 0;
+  if (cudaStreamSynchronize(S(stream)) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  if (cudaMemcpy(&v, p->d_status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  if (cudaMemset(p->d_status, 0, sizeof(v)) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  *flags = v;
+  return v ? MEDUSA_ERR_DEVICE : MEDUSA_OK;
+}
+
+medusa_status medusa_heads(const medusa_plan* p, const float* h, const int32_t* root_in,
+                           const medusa_weights* w, float* logits, int32_t* topk_tok,
+                           float* topk_val, int32_t* root, void* ws, size_t ws_bytes, void* stream) {
+  if (!p || !h || !topk_tok || !topk_val || !root) return MEDUSA_ERR_INVALID;
+  medusa_status s = check_weights(p, w, true, false, true);
+  if (s != MEDUSA_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MEDUSA_OK) return s;
+  if (!logits) logits = at<float>(ws, p->o_logits);
+  return heads_impl(p, h, root_in, w, logits, topk_tok, topk_val, root, ws, S(stream));
+}
+
+medusa_status medusa_tree_build(const medusa_plan* p, const int32_t* topk_tok, const int32_t* root,
+                                const int32_t* len, int32_t* tok, int32_t* pos, uint32_t* mask,
+                                int32_t* retrieve, void* stream) {
+  if (!p || !topk_tok || !root || !len || !tok || !pos || !mask || !retrieve) return MEDUSA_ERR_INVALID;
+  return tree_impl(p, topk_tok, root, len, tok, pos, mask, retrieve, S(stream));
+}
+
+medusa_status medusa_layer_qkv(const medusa_plan* p, const medusa_weights* w, const int32_t* tok,
+                               const int32_t* pos, float* q, void* tk, void* tv, void* ws,
+                               size_t ws_bytes, void* stream) {
+  if (!p || !tok || !pos || !q || !tk || !tv) return MEDUSA_ERR_INVALID;
+  medusa_status s = check_weights(p, w, false, true, false);
+  if (s != MEDUSA_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MEDUSA_OK) return s;
+  if ((s = gather_impl(p, w, tok, ws, S(stream))) != MEDUSA_OK) return s;
+  return qkv_impl(p, w, pos, q, tk, tv, ws, S(stream));
+}
+
+medusa_status medusa_tree_attention(const medusa_plan* p, const float* q, const medusa_kv* kv,
+                                    const void* tk, const void* tv, const uint32_t* mask, float* o,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  if (!p || !q || !tk || !tv || !mask || !o) return MEDUSA_ERR_INVALID;
+  medusa_status s = check_kv(p, kv, false);
+  if (s != MEDUSA_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MEDUSA_OK) return s;
+  return attn_impl(p, q, kv, tk, tv, mask, o, false, ws, S(stream));
+}
+
+medusa_status medusa_layer_out(const medusa_plan* p, const medusa_weights* w, const int32_t* tok,
+                               const float* o, float* hprime, void* ws, size_t ws_bytes, void* stream) {
+  if (!p || !tok || !o || !hprime) return MEDUSA_ERR_INVALID;
+  medusa_status s = check_weights(p, w, false, true, false);
+  if (s != MEDUSA_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MEDUSA_OK) return s;
+  if ((s = gather_impl(p, w, tok, ws, S(stream))) != MEDUSA_OK) return s;
+  return out_impl(p, w, o, false, hprime, false, ws, S(stream));
+}
+
+medusa_status medusa_verify_logits(const medusa_plan* p, const medusa_weights* w, const float* hprime,
+                                   const int32_t* tok, medusa_accept acc, float* logits, int32_t* am,
+                                   float* stats, void* ws, size_t ws_bytes, void* stream) {
+  if (!p || !hprime || !tok || !am || !stats) return MEDUSA_ERR_INVALID;
+  medusa_status s = check_weights(p, w, false, false, true);
+  if (s != MEDUSA_OK) return s;
+  if ((s = check_accept(acc)) != MEDUSA_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MEDUSA_OK) return s;
+  if (!logits) logits = at<float>(ws, p->o_vlog);
+  return vlogits_impl(p, w, hprime, false, tok, acc, logits, am, stats, ws, S(stream));
+}
+
+medusa_status medusa_verify(const medusa_plan* p, const int32_t* tok, const int32_t* am,
+                            const float* stats, const int32_t* retrieve, const float* hprime,
+                            medusa_accept acc, const medusa_outputs* out, void* stream) {
+  if (!p || !tok || !am || !stats || !retrieve || !hprime || !out) return MEDUSA_ERR_INVALID;
+  if (!out->out_tok || !out->n_acc || !out->h_next || !out->root_next) return MEDUSA_ERR_INVALID;
+  medusa_status s = check_accept(acc);
+  if (s != MEDUSA_OK) return s;
+  return accept_impl(p, tok, am, stats, retrieve, hprime, acc, out->out_tok, out->n_acc,
+                     out->path_nodes, out->h_next, out->root_next, S(stream));
+}
+
+medusa_status medusa_kv_compact(const medusa_plan* p, const medusa_kv* kv, const void* tk,
+                                const void* tv, const int32_t* path_nodes, const int32_t* n_acc,
+                                void* stream) {
+  if (!p || !tk || !tv || !path_nodes || !n_acc) return MEDUSA_ERR_INVALID;
+  medusa_status s = check_kv(p, kv, true);
+  if (s != MEDUSA_OK) return s;
+  return compact_impl(p, kv, tk, tv, path_nodes, n_acc, S(stream));
+}
+
+medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* root_in,
+                          const medusa_weights* w, const medusa_kv* kv, medusa_accept acc,
+                          const medusa_outputs* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!p || !h || !out) return MEDUSA_ERR_INVALID;
+  if (!out->out_tok || !out->n_acc || !out->h_next || !out->root_next) return MEDUSA_ERR_INVALID;
+  medusa_status s = check_weights(p, w, true, true, true);
+  if (s != MEDUSA_OK) return s;
+  if ((s = check_kv(p, kv, true)) != MEDUSA_OK) return s;
+  if ((s = check_accept(acc)) != MEDUSA_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MEDUSA_OK) return s;
+  const cudaStream_t st = S(stream);
+  int32_t* ttok = at<int32_t>(ws, p->o_ttok);
+  int32_t* root = at<int32_t>(ws, p->o_root);
+  int32_t* tok = at<int32_t>(ws, p->o_tok);
+  int32_t* pos = at<int32_t>(ws, p->o_pos);
+  uint32_t* mask = at<uint32_t>(ws, p->o_mask);
+  int32_t* retr = at<int32_t>(ws, p->o_retr);
+  float* q = at<float>(ws, p->o_q);
+  void* tk = at<char>(ws, p->o_tk);
+  void* tv = at<char>(ws, p->o_tv);
+  float* o = at<float>(ws, p->o_o);
+  float* hp = at<float>(ws, p->o_hp);
+  int32_t* am = at<int32_t>(ws, p->o_am);
+  float* stats = at<float>(ws, p->o_stats);
+  int32_t* path = out->path_nodes ? out->path_nodes : at<int32_t>(ws, p->o_path);
+  if ((s = heads_impl(p, h, root_in, w, at<float>(ws, p->o_logits), ttok, at<float>(ws, p->o_tval),
+                      root, ws, st)) != MEDUSA_OK)
+    return s;
+  if ((s = tree_impl(p, ttok, root, kv->len, tok, pos, mask, retr, st)) != MEDUSA_OK) return s;
+  if ((s = gather_impl(p, w, tok, ws, st)) != MEDUSA_OK) return s;
+  if ((s = qkv_impl(p, w, pos, q, tk, tv, ws, st)) != MEDUSA_OK) return s;
+  if ((s = attn_impl(p, q, kv, tk, tv, mask, o, true, ws, st)) != MEDUSA_OK) return s;
+  if ((s = out_impl(p, w, o, true, hp, true, ws, st)) != MEDUSA_OK) return s;
+  if ((s = vlogits_impl(p, w, hp, true, tok, acc, at<float>(ws, p->o_vlog), am, stats, ws, st)) != MEDUSA_OK)
+    return s;
+  if ((s = accept_impl(p, tok, am, stats, retr, hp, acc, out->out_tok, out->n_acc, path, out->h_next,
+                       out->root_next, st)) != MEDUSA_OK)
+    return s;
+  return compact_impl(p, kv, tk, tv, path, out->n_acc, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,225 @@
+// Candidate selection and tree construction of the Medusa step.
+//   topk_partial  per (sequence, head, vocab slice): the 16 best (logit, token) pairs
+//   tree_build    merge of the slices -> per-head top-s_k and the root; node tokens and
+//                 depth position ids; ancestor bitmask and root->leaf paths
+//   rope_split    q/k/v of the tree nodes with rotary embedding at the node positions
+// Sources: "Medusa: Simple LLM Inference Acceleration Framework with Multiple Decoding
+// Heads" §3.4 Tree Attention, Steps 1-4; "MEDUSA 精读" section 6 (tree mask, tree position
+// ids, flatten/restore indices).  Order of candidates: larger logit first, lower token id
+// on equal logits.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace medusa {
+
+#define NEG_INF (-INFINITY)
+constexpr int NO_IDX = 0x7fffffff;
+
+// Sorted (descending) per-thread candidate list kept in registers.
+struct TopList {
+  float v[kTops];
+  int i[kTops];
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int t = 0; t < kTops; ++t) { v[t] = NEG_INF; i[t] = NO_IDX; }
+  }
+  __device__ __forceinline__ void insert(float x, int idx) {
+    if (!better(x, idx, v[kTops - 1], i[kTops - 1])) return;
+    v[kTops - 1] = x;
+    i[kTops - 1] = idx;
+#pragma unroll
+    for (int t = kTops - 1; t > 0; --t) {
+      if (better(v[t], i[t], v[t - 1], i[t - 1])) {
+        float tv = v[t]; v[t] = v[t - 1]; v[t - 1] = tv;
+        int ti = i[t]; i[t] = i[t - 1]; i[t - 1] = ti;
+      }
+    }
+  }
+  __device__ __forceinline__ void pop() {
+#pragma unroll
+    for (int t = 0; t < kTops - 1; ++t) { v[t] = v[t + 1]; i[t] = i[t + 1]; }
+    v[kTops - 1] = NEG_INF;
+    i[kTops - 1] = NO_IDX;
+  }
+};
+
+// Merge the 32 lanes' sorted lists: kTops rounds of a warp argmax over the list heads;
+// the winning lane pops.  Token ids are distinct across lanes (sentinels aside).
+__device__ __forceinline__ void warp_merge(TopList& L, float* ov, int* oi) {
+  const int lane = threadIdx.x & 31;
+  for (int t = 0; t < kTops; ++t) {
+    float v = L.v[0];
+    int i = L.i[0];
+    warp_argmax(v, i);
+    if (L.i[0] == i && L.v[0] == v) L.pop();
+    if (lane == 0) { ov[t] = v; oi[t] = i; }
+  }
+}
+
+__global__ void __launch_bounds__(256) topk_partial_kernel(TopkArgs a) {
+  __shared__ float sv[8][kTops];
+  __shared__ int si[8][kTops];
+  const int sp = blockIdx.x, k = blockIdx.y, b = blockIdx.z;
+  const float* z = a.logits + ((long)b * a.nh + k) * a.V;
+  const int lo = sp * a.chunk, hi = min(a.V, lo + a.chunk);
+  TopList L;
+  L.init();
+  for (int v = lo + threadIdx.x; v < hi; v += blockDim.x) L.insert(z[v], v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  warp_merge(L, sv[warp], si[warp]);
+  __syncthreads();
+  if (warp == 0) {
+    L.init();
+    if (lane < 8) {
+#pragma unroll
+      for (int t = 0; t < kTops; ++t) { L.v[t] = sv[lane][t]; L.i[t] = si[lane][t]; }
+    }
+    const long o = (((long)b * a.nh + k) * a.splits + sp) * kTops;
+    warp_merge(L, a.cand_val + o, a.cand_idx + o);
+  }
+}
+
+cudaError_t launch_topk_partial(const TopkArgs& a, cudaStream_t st) {
+  dim3 grid(a.splits, a.nh, a.B);
+  topk_partial_kernel<<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// One CTA per sequence.  Warp w merges the vocab slices of heads w, w+8 (head 0 is the
+// LM head, heads 1..K the Medusa heads) into the final top-16 of each head.
+__global__ void __launch_bounds__(256) topk_merge_kernel(MergeArgs a) {
+  __shared__ float tv[MEDUSA_MAX_HEADS + 1][kTops];
+  __shared__ int ti[MEDUSA_MAX_HEADS + 1][kTops];
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nh = a.K + 1;
+  for (int k = warp; k < nh; k += 8) {
+    TopList L;
+    L.init();
+    if (lane < a.splits) {
+      const long o = (((long)b * nh + k) * a.splits + lane) * kTops;
+#pragma unroll
+      for (int t = 0; t < kTops; ++t) { L.v[t] = a.cand_val[o + t]; L.i[t] = a.cand_idx[o + t]; }
+    }
+    warp_merge(L, tv[k], ti[k]);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int r = a.root_in ? a.root_in[b] : ti[0][0];
+    if (r < 0 || r >= a.V) { set_flag(a.status, MEDUSA_FLAG_TOKEN_RANGE); r = 0; }
+    a.root_out[b] = r;
+  }
+  for (int e = tid; e < a.K * kTops; e += blockDim.x) {
+    const int k = e / kTops, t = e - k * kTops;
+    a.topk_tok[(long)b * a.K * kTops + e] = ti[k + 1][t];
+    a.topk_val[(long)b * a.K * kTops + e] = tv[k + 1][t];
+  }
+}
+
+cudaError_t launch_topk_merge(const MergeArgs& a, cudaStream_t st) {
+  topk_merge_kernel<<<a.B, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// One CTA per sequence: node tokens and position ids.  Block 0 also writes the per-tree
+// tables (ancestor bitmask, root->leaf paths), which are the same for every sequence.
+__global__ void __launch_bounds__(256) tree_build_kernel(TreeArgs a) {
+  __shared__ int haschild[MEDUSA_MAX_NODES];
+  __shared__ int leafidx[MEDUSA_MAX_NODES];
+  const int b = blockIdx.x, tid = threadIdx.x;
+  int L = a.len[b];
+  if (L < 0) L = 0;
+  for (int n = tid; n < a.n1; n += blockDim.x) {
+    int t = a.root[b];
+    if (n > 0) t = a.topk_tok[((long)b * a.K + a.depth[n] - 1) * kTops + a.rank[n]];
+    if (t < 0 || t >= a.V) { set_flag(a.status, MEDUSA_FLAG_TOKEN_RANGE); t = 0; }
+    a.tok[(long)b * a.n1 + n] = t;
+    a.pos[(long)b * a.n1 + n] = L + a.depth[n];
+  }
+  if (b != 0) return;
+  for (int n = tid; n < MEDUSA_MAX_NODES; n += blockDim.x) haschild[n] = 0;
+  __syncthreads();
+  for (int n = tid; n < a.n1; n += blockDim.x) {
+    uint32_t wmask[kMaskWords];
+#pragma unroll
+    for (int q = 0; q < kMaskWords; ++q) wmask[q] = 0u;
+    for (int j = n, guard = 0; j >= 0 && guard <= MEDUSA_MAX_HEADS + 1; j = a.parent[j], ++guard)
+      wmask[j >> 5] |= 1u << (j & 31);
+#pragma unroll
+    for (int q = 0; q < kMaskWords; ++q) a.mask[(long)n * kMaskWords + q] = wmask[q];
+    if (n > 0) haschild[a.parent[n]] = 1;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int c = 0;
+    for (int n = 0; n < a.n1; ++n) leafidx[n] = haschild[n] ? -1 : c++;
+  }
+  const int W = a.K + 1;
+  for (int e = tid; e < a.n1 * W; e += blockDim.x) a.retrieve[e] = -1;
+  __syncthreads();
+  for (int n = tid; n < a.n1; n += blockDim.x) {
+    const int p = leafidx[n];
+    if (p < 0) continue;
+    for (int j = n; j >= 0; j = a.parent[j]) a.retrieve[(long)p * W + a.depth[j]] = j;
+  }
+}
+
+cudaError_t launch_tree_build(const TreeArgs& a, cudaStream_t st) {
+  tree_build_kernel<<<a.B, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// One CTA per node row.  cos/sin of pos * base^(-2i/dh) are computed once per row in
+// double precision and applied to every query and key head (rotate-half convention).
+template <typename T>
+__global__ void rope_split_kernel(const float* qkv, const int32_t* pos, int Hq, int Hkv, int dh,
+                                  float base, float* q, T* tk, T* tv) {
+  extern __shared__ float cs[];                      // [dh/2] cos, [dh/2] sin
+  const int m = blockIdx.x, half = dh / 2;
+  const double p = (double)pos[m];
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    const double theta = pow((double)base, -2.0 * i / dh);
+    double sn, cn;
+    sincos(p * theta, &sn, &cn);
+    cs[i] = (float)cn;
+    cs[half + i] = (float)sn;
+  }
+  __syncthreads();
+  const int W = (Hq + 2 * Hkv) * dh;
+  const float* row = qkv + (long)m * W;
+  for (int e = threadIdx.x; e < (Hq + Hkv) * half; e += blockDim.x) {
+    const int h = e / half, i = e - h * half;
+    const float* x = row + h * dh;
+    const float c = cs[i], s = cs[half + i];
+    const float y0 = x[i] * c - x[i + half] * s;
+    const float y1 = x[i + half] * c + x[i] * s;
+    if (h < Hq) {
+      float* qo = q + ((long)m * Hq + h) * dh;
+      qo[i] = y0;
+      qo[i + half] = y1;
+    } else {
+      T* ko = tk + ((long)m * Hkv + (h - Hq)) * dh;
+      ko[i] = from_f32<T>(y0);
+      ko[i + half] = from_f32<T>(y1);
+    }
+  }
+  const float* vr = row + (Hq + Hkv) * dh;
+  for (int e = threadIdx.x; e < Hkv * dh; e += blockDim.x) tv[(long)m * Hkv * dh + e] = from_f32<T>(vr[e]);
+}
+
+cudaError_t launch_rope_split(const float* qkv, const int32_t* pos, int M, int Hq, int Hkv, int dh,
+                              float base, int dtype, float* q, void* tk, void* tv,
+                              cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  const size_t smem = dh * sizeof(float);
+  if (dtype == 0)
+    rope_split_kernel<float><<<M, 256, smem, st>>>(qkv, pos, Hq, Hkv, dh, base, q,
+                                                   reinterpret_cast<float*>(tk),
+                                                   reinterpret_cast<float*>(tv));
+  else
+    rope_split_kernel<bf16><<<M, 256, smem, st>>>(qkv, pos, Hq, Hkv, dh, base, q,
+                                                  reinterpret_cast<bf16*>(tk),
+                                                  reinterpret_cast<bf16*>(tv));
+  return cudaGetLastError();
+}
+
+}  // namespace medusa

@@ -1,0 +1,133 @@
+// Internal launcher interface between the C ABI (capi.cu) and the kernel files.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace medusa {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr int kMaxSeg = 10;     // LM head + up to 8 Medusa heads (+1 spare)
+constexpr int kTops = 16;       // candidates kept per head (MEDUSA_MAX_TOPS)
+constexpr int kMaskWords = 8;   // 256 nodes / 32
+
+enum Epi { EPI_STORE = 0, EPI_SILU_RES = 1, EPI_RES_ADD = 2 };
+
+// One row block of a stacked projection Y[m][out_off + r] = sum_k X[m][k] W[r][k].
+struct MatSeg {
+  const void* w;                 // [rows][k] weights (dtype)
+  const float* x;                // CUDA-core path: fp32 activations [M][ldx]
+  const __nv_bfloat16* a_hi;     // tensor-core path: bf16 activations [M][ldx]
+  const __nv_bfloat16* a_lo;     // low halves of the fp32 activations, or null
+  long ldx;                      // activation row stride (elements)
+  int rows;
+  int out_off;
+};
+
+struct MatArgs {
+  MatSeg seg[kMaxSeg];
+  int nseg;
+  int tile_off[kMaxSeg + 1];     // tensor-core path: first row tile of each segment
+  int M, k;
+  float* out;                    // out[m * ldo + out_off + r]
+  long ldo;
+  int epi;
+  const float* res_f32;          // residual res[m * ldr + r] (fp32) ...
+  const void* res_w;             // ... or in the weights' dtype
+  long ldr;
+  __nv_bfloat16* out_hi;         // optional bf16 hi/lo copies of out (same indexing)
+  __nv_bfloat16* out_lo;
+};
+
+// CUDA-core row-dot projection: dtype 0 = f32 weights, 1 = bf16.
+cudaError_t launch_rowdot(const MatArgs& a, int dtype, cudaStream_t st);
+// Tensor-core (mma.sync bf16) projection; bf16 weights only.
+cudaError_t launch_mma_gemm(MatArgs a, cudaStream_t st);
+// fp32 -> bf16 hi/lo split of n elements.
+cudaError_t launch_split(const float* x, __nv_bfloat16* hi, __nv_bfloat16* lo, long n,
+                         cudaStream_t st);
+// X[m][:] = E[tok[m]][:], written as fp32 (xf) or bf16 (xb); one of them non-null.
+cudaError_t launch_gather(const void* emb, int dtype, const int32_t* tok, int M, int d, int V,
+                          float* xf, __nv_bfloat16* xb, cudaStream_t st);
+
+// ---- heads top-k and tree
+struct TopkArgs {
+  const float* logits;   // [B][nh][V]
+  int B, nh, V, splits, chunk;
+  float* cand_val;       // [B][nh][splits][kTops]
+  int32_t* cand_idx;
+};
+cudaError_t launch_topk_partial(const TopkArgs& a, cudaStream_t st);
+
+// Merge of the vocab slices: per-head top-16 (head 0 = LM head) and the root token.
+struct MergeArgs {
+  const float* cand_val; const int32_t* cand_idx;
+  int B, K, V, splits;
+  const int32_t* root_in;
+  int32_t* topk_tok; float* topk_val; int32_t* root_out;              // [B][K][kTops], [B]
+  uint32_t* status;
+};
+cudaError_t launch_topk_merge(const MergeArgs& a, cudaStream_t st);
+
+struct TreeArgs {
+  const int32_t* topk_tok; const int32_t* root; const int32_t* len;
+  int B, K, V, n1;
+  const int32_t* parent; const int32_t* depth; const int32_t* rank;   // device spec [n1]
+  int32_t* tok; int32_t* pos;                                         // [B][n1]
+  uint32_t* mask; int32_t* retrieve;                                  // [n1][8], [n1][K+1]
+  uint32_t* status;
+};
+cudaError_t launch_tree_build(const TreeArgs& a, cudaStream_t st);
+
+// qkv [M][(Hq+2Hkv)*dh] fp32 -> q [M][Hq][dh] fp32 (RoPE), tree k (RoPE) / v in dtype.
+cudaError_t launch_rope_split(const float* qkv, const int32_t* pos, int M, int Hq, int Hkv, int dh,
+                              float base, int dtype, float* q, void* tk, void* tv,
+                              cudaStream_t st);
+
+// ---- attention
+struct AttnArgs {
+  const float* q;
+  const void* kc; const void* vc;
+  const int32_t* page_table; int page_size; int pages_per_seq; int num_pages;
+  const int32_t* len; int capacity;
+  const void* tk; const void* tv;
+  const uint32_t* mask;
+  int B, n1, Hq, Hkv, G, dh;
+  int nsplit, chunk;
+  int rows_per_block, nrb, rpw;
+  float* part_o; float* part_ml;
+  float* o; __nv_bfloat16* o_hi; __nv_bfloat16* o_lo;
+  uint32_t* status;
+  float scale;
+};
+cudaError_t launch_tree_attention(const AttnArgs& a, int dtype, cudaStream_t st);
+cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st);
+
+// ---- verify
+struct VerifyArgs {
+  const float* logits;      // [M][V]
+  const int32_t* tok; const int32_t* parent; const int32_t* depth;
+  int B, n1, V, K, P, d;
+  int typical; float temperature, eps, delta;
+  int32_t* am; float* stats;                        // [M], [M][4]
+  const int32_t* retrieve; const float* hprime;     // [n1][K+1], [M][d]
+  int32_t* out_tok; int32_t* n_acc; int32_t* path_nodes; float* h_next; int32_t* root_next;
+  uint32_t* status;
+};
+cudaError_t launch_verify_stats(const VerifyArgs& a, cudaStream_t st);
+cudaError_t launch_verify_accept(const VerifyArgs& a, cudaStream_t st);
+
+struct CompactArgs {
+  void* kc; void* vc;
+  const int32_t* page_table; int page_size; int pages_per_seq; int num_pages;
+  const int32_t* len; int32_t* len_out; int capacity;
+  const void* tk; const void* tv;
+  const int32_t* path_nodes; const int32_t* n_acc;
+  int B, n1, Hkv, dh, K, dtype;
+  uint32_t* status;
+};
+cudaError_t launch_kv_compact(const CompactArgs& a, cudaStream_t st);
+
+}  // namespace medusa

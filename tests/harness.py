@@ -1,0 +1,238 @@
+"""Helpers of the GPU parity tests: set up a workload on the device, run the library's
+stages through the C ABI, run the oracle on the same seeded inputs, and compare under
+the stated rules:
+
+* indices, tree tables, tokens and accepted paths bit-exact;
+* a decision whose fp64 oracle margin is below 1e-3 (top-2 logit gap, top-s neighbour
+  gap, |log p - log threshold|) is flagged, not failed; once a flagged decision differs,
+  the comparison of that sequence stops for the step;
+* floats (logits, q/k/v, attention outputs, h', cache rows) within |gpu - oracle| <=
+  2e-2 + 1e-2 |oracle|.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+import oracle as O
+import synthetic as S
+from medusa_head_speculative_gb300 import binding as Bnd
+
+ATOL, RTOL = 2e-2, 1e-2
+NEAR = O.NEAR
+
+
+def ensure_built():
+    import os
+    if not os.path.exists(Bnd.LIB_PATH):
+        from medusa_head_speculative_gb300 import build
+        build.build()
+    Bnd.lib()
+
+
+def close(g, o, atol=ATOL, rtol=RTOL):
+    g = np.asarray(g, dtype=np.float64)
+    o = np.asarray(o, dtype=np.float64)
+    assert g.shape == o.shape, (g.shape, o.shape)
+    err = np.abs(g - o) - (atol + rtol * np.abs(o))
+    return float(err.max()) if err.size else -1.0
+
+
+def spec_for(w: S.Workload):
+    """(product-built parent/rank, oracle-built TreeSpec); asserted equal."""
+    if w.tree == "cartesian":
+        parent, rank = Bnd.tree_cartesian(w.s)
+        spec = O.cartesian_tree(w.s)
+    else:
+        a = S.score_table(w.K, max(w.s))
+        parent, rank = Bnd.tree_greedy(w.s, a, w.N)
+        spec = O.greedy_tree(a, w.s, w.N)
+    assert list(parent) == spec.parent and list(rank) == spec.rank
+    return parent, rank, spec
+
+
+@dataclass
+class Device:
+    w: S.Workload
+    plan: Bnd.Plan
+    wts: dict
+    wstruct: object
+    h: torch.Tensor
+    kc: torch.Tensor
+    vc: torch.Tensor
+    pt: torch.Tensor
+    length: torch.Tensor
+    ws: torch.Tensor
+    spec: O.TreeSpec
+    cpu: dict = field(default_factory=dict)
+
+
+def setup(w: S.Workload, wts_cpu=None, h_cpu=None):
+    ensure_built()
+    parent, rank, spec = spec_for(w)
+    dtype = Bnd.F32 if w.dtype == "f32" else Bnd.BF16
+    num_pages = w.B * w.pages_per_seq if w.page_size else 0
+    plan = Bnd.Plan(w.B, w.d, w.V, w.K, w.Hq, w.Hkv, w.dh, dtype, w.capacity, w.s, parent, rank,
+                    rope_base=w.rope_base, page_size=w.page_size, num_pages=num_pages)
+    wts_cpu = wts_cpu if wts_cpu is not None else S.weights(w)
+    wts = {k: v.cuda() for k, v in wts_cpu.items()}
+    h_cpu = h_cpu if h_cpu is not None else S.hidden(w)
+    kc, vc, pt = S.kv_cache(w)
+    dev = Device(w, plan, wts, Bnd.weights_struct(wts), h_cpu.cuda(), kc.cuda(), vc.cuda(),
+                 None if pt is None else pt.cuda(),
+                 torch.tensor(w.lengths, dtype=torch.int32, device="cuda"),
+                 torch.empty(plan.workspace_size, dtype=torch.uint8, device="cuda"), spec)
+    dev.cpu = {"wts": wts_cpu, "h": h_cpu}
+    return dev
+
+
+def accept_of(w: S.Workload):
+    return {"mode": w.mode, "temperature": w.temperature, "eps": w.eps, "delta": w.delta}
+
+
+def run_stages(dev: Device, root_in=None):
+    """Every stage through its own entry point, chained on the GPU; returns CPU copies."""
+    w, p = dev.w, dev.plan
+    B, K, V, d, n1 = w.B, w.K, w.V, w.d, p.n1
+    f32, i32 = dict(dtype=torch.float32, device="cuda"), dict(dtype=torch.int32, device="cuda")
+    kvdt = dict(dtype=w.torch_dtype, device="cuda")
+    r = {}
+    logits = torch.empty(B, K + 1, V, **f32)
+    ttok = torch.empty(B, K, 16, **i32)
+    tval = torch.empty(B, K, 16, **f32)
+    root = torch.empty(B, **i32)
+    Bnd.heads(p, dev.h, root_in, dev.wstruct, logits, ttok, tval, root, dev.ws)
+    tok = torch.empty(B, n1, **i32)
+    pos = torch.empty(B, n1, **i32)
+    mask = torch.empty(n1, 8, dtype=torch.int32, device="cuda")
+    retr = torch.empty(n1, K + 1, **i32)
+    Bnd.tree_build(p, ttok, root, dev.length, tok, pos, mask, retr)
+    q = torch.empty(B, n1, w.Hq, w.dh, **f32)
+    tk = torch.empty(B, n1, w.Hkv, w.dh, **kvdt)
+    tv = torch.empty(B, n1, w.Hkv, w.dh, **kvdt)
+    Bnd.layer_qkv(p, dev.wstruct, tok, pos, q, tk, tv, dev.ws)
+    kv = Bnd.kv_struct(dev.kc, dev.vc, dev.length, None, dev.pt)
+    o = torch.empty(B, n1, w.Hq, w.dh, **f32)
+    Bnd.tree_attention(p, q, kv, tk, tv, mask, o, dev.ws)
+    hp = torch.empty(B, n1, d, **f32)
+    Bnd.layer_out(p, dev.wstruct, tok, o, hp, dev.ws)
+    acc = Bnd.accept_struct(**accept_of(w))
+    vlog = torch.empty(B, n1, V, **f32)
+    am = torch.empty(B, n1, **i32)
+    stats = torch.empty(B, n1, 4, **f32)
+    Bnd.verify_logits(p, dev.wstruct, hp, tok, acc, vlog, am, stats, dev.ws)
+    out_tok = torch.empty(B, K + 1, **i32)
+    n_acc = torch.empty(B, **i32)
+    path = torch.empty(B, K + 1, **i32)
+    h_next = torch.empty(B, d, **f32)
+    root_next = torch.empty(B, **i32)
+    outs = Bnd.outputs_struct(out_tok, n_acc, path, h_next, root_next)
+    Bnd.verify(p, tok, am, stats, retr, hp, acc, outs)
+    torch.cuda.synchronize()
+    for name, t in [("logits", logits), ("topk_tok", ttok), ("topk_val", tval), ("root", root),
+                    ("tok", tok), ("pos", pos), ("mask", mask), ("retrieve", retr), ("q", q),
+                    ("tk", tk), ("tv", tv), ("o", o), ("hp", hp), ("vlog", vlog), ("am", am),
+                    ("stats", stats), ("out_tok", out_tok), ("n_acc", n_acc), ("path", path),
+                    ("h_next", h_next), ("root_next", root_next)]:
+        r[name] = t.float().cpu().numpy() if t.dtype == torch.bfloat16 else t.cpu().numpy()
+    r["_dev"] = dict(tk=tk, tv=tv, path=path, n_acc=n_acc)
+    return r
+
+
+def run_step(dev: Device, root_in=None, len_out=None):
+    """One medusa_step; the cache is updated in place, lengths into len_out (or in place)."""
+    w, p = dev.w, dev.plan
+    B, K, d = w.B, w.K, w.d
+    i32 = dict(dtype=torch.int32, device="cuda")
+    out_tok = torch.empty(B, K + 1, **i32)
+    n_acc = torch.empty(B, **i32)
+    path = torch.empty(B, K + 1, **i32)
+    h_next = torch.empty(B, d, dtype=torch.float32, device="cuda")
+    root_next = torch.empty(B, **i32)
+    len_out = dev.length if len_out is None else len_out
+    kv = Bnd.kv_struct(dev.kc, dev.vc, dev.length, len_out, dev.pt)
+    outs = Bnd.outputs_struct(out_tok, n_acc, path, h_next, root_next)
+    Bnd.step(p, dev.h, root_in, dev.wstruct, kv, Bnd.accept_struct(**accept_of(w)), outs, dev.ws)
+    torch.cuda.synchronize()
+    return dict(out_tok=out_tok.cpu().numpy(), n_acc=n_acc.cpu().numpy(), path=path.cpu().numpy(),
+                h_next=h_next, root_next=root_next, len_out=len_out.cpu().numpy())
+
+
+def oracle_step(dev: Device, b: int, ow=None, root=None):
+    w = dev.w
+    ow = ow if ow is not None else O.oracle_weights(dev.cpu["wts"])
+    k, v = S.kv_prefix(w, b)
+    dims = {"Hq": w.Hq, "Hkv": w.Hkv, "dh": w.dh, "rope_base": w.rope_base}
+    return O.medusa_step(ow, dev.cpu["h"][b], k, v, dev.spec, dims, accept_of(w), root=root,
+                         s=list(w.s))
+
+
+class Flagged(Exception):
+    """A flagged (near-tie) decision differs: the rest of the sequence is not compared."""
+
+
+def compare_sequence(g: dict, r: O.StepResult, b: int, spec: O.TreeSpec, w: S.Workload,
+                     report: dict):
+    """Compare GPU stage outputs of sequence b with the oracle's step.  Raises
+    AssertionError on a real mismatch, Flagged when a flagged decision differs."""
+    K, n1 = w.K, spec.N + 1
+    report.setdefault("flags", 0)
+    # heads
+    assert close(g["logits"][b, 0], r.z0) <= 0, "LM-head logits"
+    assert close(g["logits"][b, 1:], r.zk) <= 0, "head logits"
+    if g["root"][b] != r.root:
+        if r.root_margin < NEAR:
+            raise Flagged("root")
+        raise AssertionError(f"root {g['root'][b]} != {r.root}")
+    for k in range(K):
+        for rk in range(w.s[k]):
+            if g["topk_tok"][b, k, rk] != r.topk[k, rk]:
+                if r.topk_margin[k, rk] < NEAR:
+                    raise Flagged(f"top-s head {k + 1} rank {rk}")
+                raise AssertionError(f"top-s head {k + 1} rank {rk}: {g['topk_tok'][b, k, rk]} "
+                                     f"!= {r.topk[k, rk]}")
+            if r.topk_margin[k, rk] < NEAR:
+                report["flags"] += 1
+    # tree
+    assert (g["tok"][b] == r.tok).all(), "node tokens"
+    assert (g["pos"][b] == r.pos).all(), "positions"
+    M = O.tree_mask(spec)
+    bits = g["mask"].view(np.uint32)
+    for i in range(n1):
+        for j in range(n1):
+            assert ((bits[i, j // 32] >> (j % 32)) & 1) == M[i, j], f"mask {i},{j}"
+        for j in range(n1, 256):
+            assert ((bits[i, j // 32] >> (j % 32)) & 1) == 0
+    paths = O.retrieve_paths(spec)
+    for pi, path in enumerate(paths):
+        assert list(g["retrieve"][pi, :len(path)]) == path
+        assert (g["retrieve"][pi, len(path):] == -1).all()
+    assert (g["retrieve"][len(paths):] == -1).all()
+    # synthetic layer and attention
+    assert close(g["q"][b], r.q) <= 0, "q"
+    assert close(g["tk"][b], r.k) <= 0, "tree k"
+    assert close(g["tv"][b], r.v) <= 0, "tree v"
+    assert close(g["o"][b], r.o) <= 0, "attention o"
+    assert close(g["hp"][b], r.hp) <= 0, "h'"
+    assert close(g["vlog"][b], r.zv) <= 0, "verification logits"
+    for n in range(n1):
+        if g["am"][b, n] != r.am[n]:
+            if r.am_margin[n] < NEAR:
+                raise Flagged(f"argmax node {n}")
+            raise AssertionError(f"argmax node {n}")
+    # acceptance: recompute the GPU's decisions from its statistics only to locate flags
+    for c in range(1, n1):
+        if r.acc_margin[c] < NEAR:
+            report["flags"] += 1
+    gm = int(g["n_acc"][b]) - 1
+    if gm != r.m or list(g["path"][b, :gm + 1]) != list(r.path_nodes):
+        if any(r.acc_margin[c] < NEAR for c in range(1, n1)):
+            raise Flagged("acceptance")
+        raise AssertionError(f"accepted path {g['path'][b]} (m={gm}) != {r.path_nodes} (m={r.m})")
+    assert (g["path"][b, gm + 1:] == -1).all()
+    assert list(g["out_tok"][b, :gm + 1]) == list(r.out_tok)
+    assert (g["out_tok"][b, gm + 1:] == -1).all()
+    assert g["root_next"][b] == r.root_next or r.am_margin[r.path_nodes[-1]] < NEAR
+    assert close(g["h_next"][b], r.h_next) <= 0, "h_next"

@@ -1,0 +1,198 @@
+"""GPU parity: every stage of the CUDA path against the fp64 oracle on the same seeded
+inputs, called through the C ABI.  Sizes run from the tiny workload through ragged
+multi-tile cases to the full Vicuna/Zephyr-shaped workloads (oracle on sampled
+sequences where the batch is large)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synthetic as S
+from medusa_head_speculative_gb300 import binding as Bnd
+
+from harness import (Flagged, close, compare_sequence, oracle_step, run_stages, run_step, setup)
+
+pytestmark = pytest.mark.gpu
+
+
+def _mid(**kw):
+    """Ragged multi-tile bf16 case: GQA 8/2, vocab and rows not multiples of the tiles."""
+    base = dict(name="mid", B=3, d=256, V=1000, Hq=8, Hkv=2, dh=64, K=4, dtype="bf16",
+                lengths=(37, 100, 257), tree="greedy", s=(10, 10, 10, 10), N=30)
+    base.update(kw)
+    return S.Workload(**base)
+
+
+CASES = {
+    "tiny": (S.workload("tiny"), None),
+    "mid_greedy": (_mid(), None),
+    "mid_typical": (_mid(mode="typical", temperature=0.7), None),
+    "mid_paged": (_mid(page_size=16), None),
+    "mid_b6_typical": (_mid(B=6, lengths=(1, 45, 64, 65, 130, 300), dh=128, Hq=4, Hkv=4,
+                            mode="typical", temperature=1.3, s=(4, 3, 2, 2), tree="cartesian",
+                            N=4 + 12 + 24 + 48), None),
+    "mid_fp32_gqa": (_mid(dtype="f32", d=96, V=700, lengths=(5, 70, 33)), None),
+    "vicuna7b": (S.workload("vicuna7b"), None),
+    "vicuna7b_typical": (S.workload("vicuna7b_typical"), None),
+    "vicuna13b": (S.workload("vicuna13b"), (0, 5)),
+    "zephyr7b": (S.workload("zephyr7b"), (3, 12)),
+    "vicuna33b_b4_l1024_n16": (S.vicuna33b(4, 1024, 16), (2,)),
+}
+
+
+def _check(name):
+    w, sample = CASES[name]
+    dev = setup(w)
+    g = run_stages(dev)
+    ow = O.oracle_weights(dev.cpu["wts"])
+    seqs = list(sample) if sample else list(range(w.B))
+    report, flagged = {}, []
+    for b in seqs:
+        r = oracle_step(dev, b, ow)
+        try:
+            compare_sequence(g, r, b, dev.spec, w, report)
+        except Flagged as e:
+            flagged.append((b, str(e)))
+    assert len(flagged) <= max(1, len(seqs) // 2), flagged
+    # the fused step equals the chained stages exactly, and compacts the cache
+    len_out = torch.empty_like(dev.length)
+    s = run_step(dev, len_out=len_out)
+    np.testing.assert_array_equal(s["out_tok"], g["out_tok"])
+    np.testing.assert_array_equal(s["n_acc"], g["n_acc"])
+    np.testing.assert_array_equal(s["path"], g["path"])
+    np.testing.assert_array_equal(s["root_next"].cpu().numpy(), g["root_next"])
+    np.testing.assert_array_equal(s["h_next"].cpu().numpy(), g["h_next"])
+    np.testing.assert_array_equal(s["len_out"], np.array(w.lengths) + g["n_acc"])
+    assert dev.plan.status() == 0
+    kc = _logical_cache(dev, dev.kc)
+    vc = _logical_cache(dev, dev.vc)
+    for b in range(w.B):
+        L, n = w.lengths[b], int(g["n_acc"][b])
+        for l in range(n):
+            node = g["path"][b, l]
+            np.testing.assert_array_equal(kc[b, L + l], g["tk"][b, node])
+            np.testing.assert_array_equal(vc[b, L + l], g["tv"][b, node])
+        k0, v0 = S.kv_prefix(w, b)
+        np.testing.assert_array_equal(kc[b, :L], k0.float().numpy())   # prefix untouched
+        assert not kc[b, L + n:].any()                                # nothing past the path
+    return g, report, flagged
+
+
+def _logical_cache(dev, t):
+    """[B][capacity][Hkv][dh] float view of the device cache (pages unscrambled)."""
+    w = dev.w
+    x = t.float().cpu()
+    if not w.page_size:
+        return x.numpy()
+    pt = dev.pt.cpu().long()
+    return x[pt].reshape(w.B, w.capacity, w.Hkv, w.dh).numpy()
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_step_matches_oracle(name):
+    _check(name)
+
+
+def test_fp32_tiny_tight_tolerance():
+    w = S.workload("tiny")
+    dev = setup(w)
+    g = run_stages(dev)
+    r = oracle_step(dev, 0)
+    assert close(g["logits"][0, 0], r.z0, 2e-5, 1e-5) <= 0
+    assert close(g["o"][0], r.o, 2e-5, 1e-5) <= 0
+    assert close(g["vlog"][0], r.zv, 5e-5, 1e-5) <= 0
+
+
+def test_generate_loop_matches_sequential_greedy():
+    """Steps chained on the GPU (root_next and h_next carried, cache compacted in place)
+    emit the same tokens as the oracle's Medusa loop and plain greedy decoding."""
+    w = S.workload("tiny")
+    wts = S.planted_weights(w)
+    h0 = wts["emb"][7].float().unsqueeze(0).clone()
+    dev = setup(w, wts_cpu=wts, h_cpu=h0)
+    ow = O.oracle_weights(wts)
+    dims = {"Hq": w.Hq, "Hkv": w.Hkv, "dh": w.dh, "rope_base": w.rope_base}
+    k0, v0 = S.kv_prefix(w, 0)
+    steps = 8
+    toks_o, steps_o, kc_o, vc_o = O.medusa_generate(ow, h0[0], k0, v0, dev.spec, dims,
+                                                    {"mode": "greedy"}, steps)
+    seq, _, _ = O.sequential_greedy(ow, h0[0], k0, v0, dims, len(toks_o))
+    assert toks_o == seq
+    toks_g, root = [], None
+    for _ in range(steps):
+        s = run_step(dev, root_in=root)
+        n = int(s["n_acc"][0])
+        toks_g += list(s["out_tok"][0, :n])
+        dev.h = s["h_next"]
+        root = s["root_next"]
+    assert toks_g == toks_o
+    assert int(dev.length[0]) == kc_o.shape[0]
+    kc = dev.kc[0, :kc_o.shape[0]].float().cpu().numpy()
+    assert close(kc, kc_o, 1e-4, 1e-4) <= 0
+    assert max(s_.m for s_ in steps_o) >= 2
+
+
+def test_exact_ties_take_the_lowest_token_id():
+    """Duplicated LM-head / head rows give bitwise-equal logits: the lowest id wins."""
+    w = S.workload("tiny")
+    wts = S.head_init_weights(S.weights(w))
+    lm = wts["lm"].clone()
+    h = S.hidden(w)
+    z = lm.double() @ h[0].double()
+    best = int(torch.argmax(z))
+    dup = best - 5 if best >= 5 else best + 5
+    lm[dup] = lm[best]                   # an exact copy of the best row
+    lo, hi = min(dup, best), max(dup, best)
+    wts["lm"] = lm
+    wts["w2"] = lm.unsqueeze(0).expand_as(wts["w2"]).contiguous()
+    dev = setup(w, wts_cpu=wts, h_cpu=h)
+    g = run_stages(dev)
+    assert g["logits"][0, 0, lo] == g["logits"][0, 0, hi]
+    assert g["root"][0] == lo
+    assert g["topk_tok"][0, 0, 0] == lo and g["topk_tok"][0, 0, 1] == hi
+
+
+def test_root_only_tree_and_empty_prefix():
+    w = S.Workload("root_only", B=2, d=128, V=512, Hq=4, Hkv=2, dh=32, K=1, dtype="bf16",
+                   lengths=(0, 9), tree="greedy", s=(3,), N=0)
+    dev = setup(w)
+    g = run_stages(dev)
+    for b in range(2):
+        compare_sequence(g, oracle_step(dev, b), b, dev.spec, w, {})
+
+
+def test_typical_at_temperature_zero_is_greedy():
+    wg = _mid()
+    wt = dataclasses.replace(wg, mode="typical", temperature=0.0)
+    g1 = run_stages(setup(wg))
+    g2 = run_stages(setup(wt))
+    np.testing.assert_array_equal(g1["out_tok"], g2["out_tok"])
+    np.testing.assert_array_equal(g1["n_acc"], g2["n_acc"])
+
+
+def test_capacity_overflow_sets_flag_and_clamps():
+    w = dataclasses.replace(S.workload("tiny"), reserve=0)     # capacity = 64 = prefix
+    dev = setup(w)
+    len_out = torch.empty_like(dev.length)
+    run_step(dev, len_out=len_out)
+    assert dev.plan.status() & Bnd.FLAG_KV_CAPACITY
+    assert int(len_out[0]) == w.capacity
+    assert dev.plan.status() == 0                               # reading clears the word
+
+
+def test_page_out_of_range_sets_flag():
+    w = _mid(page_size=16)
+    dev = setup(w)
+    dev.pt[1, 0] = 10 ** 6                                      # checked before any access
+    run_stages(dev)
+    assert dev.plan.status() & Bnd.FLAG_PAGE_RANGE
+
+
+def test_workspace_too_small_is_rejected():
+    dev = setup(S.workload("tiny"))
+    dev.ws = dev.ws[:-256]
+    with pytest.raises(Bnd.MedusaError) as e:
+        run_step(dev)
+    assert e.value.code == Bnd.MEDUSA_ERR_WORKSPACE
