@@ -168,6 +168,26 @@ medusa_status medusa_heads(const medusa_plan* plan, const float* h, const int32_
                            const medusa_weights* w, float* logits, int32_t* topk_tok,
                            float* topk_val, int32_t* root, void* workspace, size_t ws_bytes,
                            void* stream);
+/* (a') Heads stage without a workspace.  The paper has no counterpart to this: it is a
+ * deployment aid for callers that cannot allocate device memory when they run the heads
+ * (an engine that plans every buffer up front and forbids allocation while decoding, a
+ * plug-in confined to another framework's memory pool, code that may run while the
+ * stream is being captured into a CUDA graph).  It computes exactly what medusa_heads()
+ * computes and writes the same topk_tok / topk_val / root outputs (the logits are not
+ * returned).  Its scratch lives in one library-owned device array of
+ * MEDUSA_NOALLOC_SCRATCH_BYTES, present on every GPU that loads the library until the
+ * process exits; no cudaMalloc, cudaFree or other allocating call is made.
+ *   - Plans whose heads scratch exceeds the array (about B*(K+1)*V*4 bytes of logits plus
+ *     small extras) get MEDUSA_ERR_UNSUPPORTED and nothing is launched.
+ *   - The first call on a device looks up the array's address with that device current;
+ *     make that first call before any stream capture begins.
+ *   - All calls share the array and it keeps the last call's contents (nothing in it
+ *     needs to start at zero).  Calls whose GPU work overlaps race on it: order them on
+ *     one stream. */
+#define MEDUSA_NOALLOC_SCRATCH_BYTES (4u << 20)
+medusa_status medusa_heads_noalloc(const medusa_plan* plan, const float* h, const int32_t* root_in,
+                                   const medusa_weights* w, int32_t* topk_tok, float* topk_val,
+                                   int32_t* root, void* stream);
 /* (b) Tree build ([MEDUSA] §3.4 Tree Attention Steps 2-4; [READING] section 6).
  * tok [B][N+1] node tokens, pos [B][N+1] = len + depth, mask [N+1][8] uint32 ancestor
  * bitmask (bit j of word j/32 set iff node j is on the root->n path), retrieve [N+1][K+1]

@@ -86,6 +86,7 @@ def lib():
         "medusa_step": (I, [P, P, P, C.POINTER(Weights), C.POINTER(KV), Accept,
                             C.POINTER(Outputs), P, SZ, P]),
         "medusa_heads": (I, [P, P, P, C.POINTER(Weights), P, P, P, P, P, SZ, P]),
+        "medusa_heads_noalloc": (I, [P, P, P, C.POINTER(Weights), P, P, P, P]),
         "medusa_tree_build": (I, [P, P, P, P, P, P, P, P, P]),
         "medusa_layer_qkv": (I, [P, C.POINTER(Weights), P, P, P, P, P, P, SZ, P]),
         "medusa_tree_attention": (I, [P, P, C.POINTER(KV), P, P, P, P, P, SZ, P]),
@@ -239,6 +240,14 @@ def heads(plan, h, root_in, wts, logits, topk_tok, topk_val, root, ws, stream=No
                                               ptr(logits), ptr(topk_tok), ptr(topk_val), ptr(root),
                                               ptr(ws), ws.numel() * ws.element_size(),
                                               _stream(stream)))
+
+
+def heads_noalloc(plan, h, root_in, wts, topk_tok, topk_val, root, stream=None):
+    """Heads stage with no workspace: scratch in the library's fixed device array."""
+    _check("medusa_heads_noalloc", lib().medusa_heads_noalloc(plan.handle, ptr(h), ptr(root_in),
+                                                              C.byref(wts), ptr(topk_tok),
+                                                              ptr(topk_val), ptr(root),
+                                                              _stream(stream)))
 
 
 def tree_build(plan, topk_tok, root, length, tok, pos, mask, retrieve, stream=None):

@@ -511,6 +511,18 @@ medusa_status check_accept(medusa_accept a) {
 
 }  // namespace
 
+// Read-only view of the plan fields the workspace-free heads entry point needs.
+bool medusa::heads_plan_view(const medusa_plan* p, HeadsPlanView* v) {
+  if (!p || !v) return false;
+  v->dims = p->d;
+  v->K = p->K;
+  v->tc_heads = p->tc_heads;
+  v->topk_splits = p->topk_splits;
+  v->topk_chunk = p->topk_chunk;
+  v->status = p->d_status;
+  return true;
+}
+
 // ===================================================================== exported API
 extern "C" {
 

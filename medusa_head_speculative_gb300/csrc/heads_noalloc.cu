@@ -1,0 +1,162 @@
+// Workspace-free variant of the heads stage: medusa_heads_noalloc().
+//
+// Some callers cannot allocate device memory when they want to run the heads: a serving
+// engine that sizes every buffer up front and forbids allocation on its decode path, a
+// plug-in that lives inside another framework's memory pool and may not call cudaMalloc
+// behind its back, or code that must not allocate because the stream may be in the
+// middle of being captured into a CUDA graph.  This entry point needs no workspace from
+// them: its scratch (the logits, the head activations and the top-k candidates) lives in
+// one fixed array in device global memory that belongs to this library.
+//
+// Limits and behaviour:
+//   * The array holds MEDUSA_NOALLOC_SCRATCH_BYTES (4 MiB) on every GPU that loads the
+//     library, for as long as the process lives.  Plans whose heads scratch needs more
+//     (roughly B * (K+1) * V * 4 bytes of logits plus small extras) are rejected with
+//     MEDUSA_ERR_UNSUPPORTED before anything is launched.
+//   * The first call on a device looks up the array's device address (a CUDA runtime
+//     symbol lookup, no allocation) with that device current; make that first call
+//     before starting any stream capture.
+//   * Every call shares the one array and leaves its last contents there; nothing in it
+//     has to start at zero, since each call overwrites everything it reads.  Calls whose
+//     GPU work overlaps (different streams, or different plans at the same time) race on
+//     the array: order them on one stream.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/medusa.h"
+#include "kernels.h"
+
+using namespace medusa;
+
+// The scratch array itself (file scope, one copy per GPU that loads the library).
+static __device__ __align__(256) unsigned char g_heads_scratch[MEDUSA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {};     // device address of g_heads_scratch, per device
+
+// Host code must not use g_heads_scratch's name as an address: it is only a host-side
+// stand-in for the device symbol.  Look the real address up once per device.
+medusa_status scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MEDUSA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_heads_scratch) != cudaSuccess || !p) return MEDUSA_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return MEDUSA_OK;
+}
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct Layout {
+  size_t logits, u, uhi, ulo, hhi, hlo, cv, ci, total;
+};
+
+Layout layout_of(const HeadsPlanView& v) {
+  const size_t B = v.dims.B, K = v.K, V = v.dims.V, D = v.dims.d;
+  const size_t tc = v.tc_heads ? 1 : 0;
+  Layout l{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = up256(off + bytes); return o; };
+  l.logits = take(B * (K + 1) * V * 4);
+  l.u = take(B * K * D * 4);
+  l.uhi = take(tc * B * K * D * 2);
+  l.ulo = take(tc * B * K * D * 2);
+  l.hhi = take(tc * B * D * 2);
+  l.hlo = take(tc * B * D * 2);
+  l.cv = take(B * (K + 1) * v.topk_splits * kTops * 4);
+  l.ci = take(B * (K + 1) * v.topk_splits * kTops * 4);
+  l.total = off;
+  return l;
+}
+
+bool ok16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" medusa_status medusa_heads_noalloc(const medusa_plan* plan, const float* h,
+                                              const int32_t* root_in, const medusa_weights* w,
+                                              int32_t* topk_tok, float* topk_val, int32_t* root,
+                                              void* stream) {
+  HeadsPlanView v;
+  if (!heads_plan_view(plan, &v)) return MEDUSA_ERR_INVALID;
+  const Layout l = layout_of(v);
+  if (l.total > (size_t)MEDUSA_NOALLOC_SCRATCH_BYTES) return MEDUSA_ERR_UNSUPPORTED;
+  if (!h || !w || !topk_tok || !topk_val || !root) return MEDUSA_ERR_INVALID;
+  if (!ok16(w->w1) || !ok16(w->w2) || !ok16(w->lm)) return MEDUSA_ERR_INVALID;
+  void* base = nullptr;
+  medusa_status s = scratch_address(&base);
+  if (s != MEDUSA_OK) return s;
+  char* sc = static_cast<char*>(base);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int B = v.dims.B, K = v.K, D = v.dims.d, V = v.dims.V;
+  const size_t es = v.dims.dtype == MEDUSA_F32 ? 4 : 2;
+  float* logits = reinterpret_cast<float*>(sc + l.logits);
+  float* u = reinterpret_cast<float*>(sc + l.u);
+  bf16* uhi = v.tc_heads ? reinterpret_cast<bf16*>(sc + l.uhi) : nullptr;
+  bf16* ulo = v.tc_heads ? reinterpret_cast<bf16*>(sc + l.ulo) : nullptr;
+  bf16* hhi = v.tc_heads ? reinterpret_cast<bf16*>(sc + l.hhi) : nullptr;
+  bf16* hlo = v.tc_heads ? reinterpret_cast<bf16*>(sc + l.hlo) : nullptr;
+
+  // u_k = SiLU(W1_k h) + h
+  MatArgs a{};
+  a.nseg = K;
+  a.M = B;
+  a.k = D;
+  a.out = u;
+  a.ldo = (long)K * D;
+  a.epi = EPI_SILU_RES;
+  a.res_f32 = h;
+  a.ldr = D;
+  a.out_hi = uhi;
+  a.out_lo = ulo;
+  if (v.tc_heads && launch_split(h, hhi, hlo, (long)B * D, st) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  for (int k = 0; k < K; ++k) {
+    MatSeg& g = a.seg[k];
+    g.w = static_cast<const char*>(w->w1) + (size_t)k * D * D * es;
+    g.x = h; g.a_hi = hhi; g.a_lo = hlo; g.ldx = D;
+    g.rows = D;
+    g.out_off = k * D;
+  }
+  if ((v.tc_heads ? launch_mma_gemm(a, st) : launch_rowdot(a, v.dims.dtype, st)) != cudaSuccess)
+    return MEDUSA_ERR_CUDA;
+  // z_0 = LM h, z_k = W2_k u_k
+  MatArgs b{};
+  b.nseg = K + 1;
+  b.M = B;
+  b.k = D;
+  b.out = logits;
+  b.ldo = (long)(K + 1) * V;
+  b.epi = EPI_STORE;
+  b.seg[0].w = w->lm;
+  b.seg[0].x = h; b.seg[0].a_hi = hhi; b.seg[0].a_lo = hlo; b.seg[0].ldx = D;
+  b.seg[0].rows = V;
+  b.seg[0].out_off = 0;
+  for (int k = 1; k <= K; ++k) {
+    MatSeg& g = b.seg[k];
+    g.w = static_cast<const char*>(w->w2) + (size_t)(k - 1) * V * D * es;
+    g.x = u + (size_t)(k - 1) * D;
+    g.a_hi = uhi ? uhi + (size_t)(k - 1) * D : nullptr;
+    g.a_lo = ulo ? ulo + (size_t)(k - 1) * D : nullptr;
+    g.ldx = (long)K * D;
+    g.rows = V;
+    g.out_off = k * V;
+  }
+  if ((v.tc_heads ? launch_mma_gemm(b, st) : launch_rowdot(b, v.dims.dtype, st)) != cudaSuccess)
+    return MEDUSA_ERR_CUDA;
+  float* cv = reinterpret_cast<float*>(sc + l.cv);
+  int32_t* ci = reinterpret_cast<int32_t*>(sc + l.ci);
+  TopkArgs t{logits, B, K + 1, V, v.topk_splits, v.topk_chunk, cv, ci};
+  if (launch_topk_partial(t, st) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  MergeArgs mg{cv, ci, B, K, V, v.topk_splits, root_in, topk_tok, topk_val, root, v.status};
+  if (launch_topk_merge(mg, st) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  return MEDUSA_OK;
+}

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/medusa.h"
+
 namespace medusa {
 
 typedef __nv_bfloat16 bf16;
@@ -129,5 +131,15 @@ struct CompactArgs {
   uint32_t* status;
 };
 cudaError_t launch_kv_compact(const CompactArgs& a, cudaStream_t st);
+
+// Plan fields used by the workspace-free heads entry point (defined in capi.cu).
+struct HeadsPlanView {
+  medusa_dims dims;
+  int K;
+  bool tc_heads;
+  int topk_splits, topk_chunk;
+  uint32_t* status;
+};
+bool heads_plan_view(const medusa_plan* p, HeadsPlanView* v);
 
 }  // namespace medusa
