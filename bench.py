@@ -314,12 +314,18 @@ def plan_tc_heads(w: S.Workload):
 
 
 def load_traffic(workload: str, kernel: str):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if one exists for
-    this workload and kernel (profiles/<kernel>__<workload>.json); else None."""
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary
+    (profiles/<kernel>__<workload>.json), only while the kernel's source files still hash
+    to what they were when the counters were taken; else None."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.json")
     try:
         with open(path) as f:
-            return json.load(f).get("traffic_bytes_per_launch")
+            rec = json.load(f)
+        src = b"".join(open(os.path.join(ROOT, x), "rb").read() for x in rec["source_files"])
+        if hashlib.sha256(src).hexdigest()[:16] != rec["source_sha256_16"]:
+            return None
+        return rec.get("traffic_bytes_per_launch")
     except Exception:
         return None
 
