@@ -65,6 +65,7 @@ enum { MEDUSA_GREEDY = 0, MEDUSA_TYPICAL = 1 };
 #define MEDUSA_FLAG_KV_CAPACITY 0x2u  /* len + tree/path length would exceed capacity */
 #define MEDUSA_FLAG_PAGE_RANGE  0x4u  /* a page-table entry fell outside [0, num_pages) */
 #define MEDUSA_FLAG_NONFINITE   0x8u  /* a logit or softmax statistic was NaN or Inf */
+#define MEDUSA_FLAG_TIMEOUT     0x10u /* a bounded wait in a pipelined kernel expired */
 
 typedef struct medusa_plan medusa_plan;   /* opaque */
 

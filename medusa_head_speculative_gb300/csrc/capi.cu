@@ -230,7 +230,7 @@ medusa_status heads_impl(const medusa_plan* p, const float* h, const int32_t* ro
     s.rows = D;
     s.out_off = k * D;
   }
-  LAUNCH(p, KN_H_W1, st, p->tc_heads ? launch_mma_gemm(a, st) : launch_rowdot(a, d.dtype, st));
+  LAUNCH(p, KN_H_W1, st, p->tc_heads ? launch_umma_gemm(a, p->d_status, st) : launch_rowdot(a, d.dtype, st));
   // z_0 = LM h, z_k = W2_k u_k
   MatArgs b{};
   b.nseg = K + 1;
@@ -253,7 +253,7 @@ medusa_status heads_impl(const medusa_plan* p, const float* h, const int32_t* ro
     s.rows = V;
     s.out_off = k * V;
   }
-  LAUNCH(p, KN_H_VOCAB, st, p->tc_heads ? launch_mma_gemm(b, st) : launch_rowdot(b, d.dtype, st));
+  LAUNCH(p, KN_H_VOCAB, st, p->tc_heads ? launch_umma_gemm(b, p->d_status, st) : launch_rowdot(b, d.dtype, st));
   TopkArgs t{logits, B, K + 1, V, p->topk_splits, p->topk_chunk, at<float>(ws, p->o_cv),
              at<int32_t>(ws, p->o_ci)};
   LAUNCH(p, KN_TOPK_PARTIAL, st, launch_topk_partial(t, st));
@@ -306,7 +306,7 @@ medusa_status qkv_impl(const medusa_plan* p, const medusa_weights* w, const int3
     s.rows = rows[i];
     s.out_off = offs[i];
   }
-  LAUNCH(p, KN_QKV, st, p->tc_nodes ? launch_mma_gemm(a, st) : launch_rowdot(a, d.dtype, st));
+  LAUNCH(p, KN_QKV, st, p->tc_nodes ? launch_umma_gemm(a, p->d_status, st) : launch_rowdot(a, d.dtype, st));
   LAUNCH(p, KN_ROPE, st, launch_rope_split(qkv, pos, p->M, d.Hq, d.Hkv, d.dh, d.rope_base, d.dtype, q, tk, tv, st));
   return MEDUSA_OK;
 }
@@ -383,7 +383,7 @@ medusa_status out_impl(const medusa_plan* p, const medusa_weights* w, const floa
   s.ldx = qd;
   s.rows = d.d;
   s.out_off = 0;
-  LAUNCH(p, KN_OUT, st, p->tc_nodes ? launch_mma_gemm(a, st) : launch_rowdot(a, d.dtype, st));
+  LAUNCH(p, KN_OUT, st, p->tc_nodes ? launch_umma_gemm(a, p->d_status, st) : launch_rowdot(a, d.dtype, st));
   return MEDUSA_OK;
 }
 
@@ -427,7 +427,7 @@ medusa_status vlogits_impl(const medusa_plan* p, const medusa_weights* w, const 
   s.ldx = d.d;
   s.rows = d.V;
   s.out_off = 0;
-  LAUNCH(p, KN_VLOGITS, st, p->tc_nodes ? launch_mma_gemm(a, st) : launch_rowdot(a, d.dtype, st));
+  LAUNCH(p, KN_VLOGITS, st, p->tc_nodes ? launch_umma_gemm(a, p->d_status, st) : launch_rowdot(a, d.dtype, st));
   VerifyArgs v = verify_args(p, tok, acc);
   v.logits = logits;
   v.am = am;

@@ -126,7 +126,7 @@ extern "C" medusa_status medusa_heads_noalloc(const medusa_plan* plan, const flo
     g.rows = D;
     g.out_off = k * D;
   }
-  if ((v.tc_heads ? launch_mma_gemm(a, st) : launch_rowdot(a, v.dims.dtype, st)) != cudaSuccess)
+  if ((v.tc_heads ? launch_umma_gemm(a, v.status, st) : launch_rowdot(a, v.dims.dtype, st)) != cudaSuccess)
     return MEDUSA_ERR_CUDA;
   // z_0 = LM h, z_k = W2_k u_k
   MatArgs b{};
@@ -150,7 +150,7 @@ extern "C" medusa_status medusa_heads_noalloc(const medusa_plan* plan, const flo
     g.rows = V;
     g.out_off = k * V;
   }
-  if ((v.tc_heads ? launch_mma_gemm(b, st) : launch_rowdot(b, v.dims.dtype, st)) != cudaSuccess)
+  if ((v.tc_heads ? launch_umma_gemm(b, v.status, st) : launch_rowdot(b, v.dims.dtype, st)) != cudaSuccess)
     return MEDUSA_ERR_CUDA;
   float* cv = reinterpret_cast<float*>(sc + l.cv);
   int32_t* ci = reinterpret_cast<int32_t*>(sc + l.ci);

@@ -4,10 +4,9 @@
 //   EPI_SILU_RES  Medusa head W1       y = SiLU(acc) + h    ("Medusa: Simple LLM Inference
 //                 Acceleration Framework with Multiple Decoding Heads", §3.4 head equation)
 //   EPI_RES_ADD   synthetic layer out  y = acc + x
-// Two kernels: a CUDA-core streaming row-dot for few activation rows (decode at small
-// batch is a pure HBM stream of the weights), and a tensor-core GEMM for tens to
-// thousands of rows, where the fp32 activations enter as bf16 hi + lo halves so the
-// products keep ~fp32 accuracy.
+// This file holds the CUDA-core streaming row-dot for few activation rows (decode at
+// small batch is a pure HBM stream of the weights); the tensor-core path for tens to
+// thousands of rows is in k_umma.cu.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -132,141 +131,6 @@ cudaError_t launch_rowdot(const MatArgs& a, int dtype, cudaStream_t st) {
     case 3: return rowdot_go<bf16, 3>(a, st);
     default: return rowdot_go<bf16, 4>(a, st);
   }
-}
-
-// =========================================================== tensor-core GEMM (mma.sync)
-// CTA = 128 weight rows x (MT*8) activation rows; 8 warps each own 16 weight rows.  The
-// weights are the MMA's A operand (16x16 row fragments), the activations its B operand,
-// so small activation counts waste no MMA work.  K is streamed in 64-wide tiles through a
-// 3-stage cp.async ring with a 16-byte-chunk XOR swizzle for conflict-free ldmatrix.
-constexpr int GB_R = 128, GB_K = 64, G_STAGES = 3;
-
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {   // byte offset in a tile
-  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
-template <int MT>
-__global__ void __launch_bounds__(256) mma_gemm_kernel(MatArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int AR = MT * 8;                               // activation rows per CTA
-  constexpr int W_BYTES = GB_R * 128, A_BYTES = AR * 128;
-  constexpr int STAGE = W_BYTES + 2 * A_BYTES;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-  // segment and tile of this CTA
-  int si = 0;
-  while (si + 1 < a.nseg && (int)blockIdx.y >= a.tile_off[si + 1]) ++si;
-  const MatSeg& s = a.seg[si];
-  const int rbase = ((int)blockIdx.y - a.tile_off[si]) * GB_R;
-  const int m0 = blockIdx.x * AR;
-  const bool has_lo = s.a_lo != nullptr;
-  const int k = a.k, nk = (k + GB_K - 1) / GB_K;
-  const bf16* w = reinterpret_cast<const bf16*>(s.w);
-  const uint32_t sbase = smem_u32(smem);
-
-  auto load_stage = [&](int st, int kt) {
-    const uint32_t ws = sbase + st * STAGE, as = ws + W_BYTES, ls = as + A_BYTES;
-    const int k0 = kt * GB_K;
-    for (int c = tid; c < GB_R * 8; c += 256) {
-      const int row = c >> 3, ch = c & 7;
-      const int gr = rbase + row, kk = k0 + ch * 8;
-      const bool ok = gr < s.rows && kk < k;
-      const bf16* src = w + (ok ? (long)gr * k + kk : 0);
-      cp_async16(ws + swz(row, ch), src, ok ? 16 : 0);
-    }
-    for (int c = tid; c < AR * 8; c += 256) {
-      const int row = c >> 3, ch = c & 7;
-      const int gm = m0 + row, kk = k0 + ch * 8;
-      const bool ok = gm < a.M && kk < k;
-      const long off = ok ? (long)gm * s.ldx + kk : 0;
-      cp_async16(as + swz(row, ch), s.a_hi + off, ok ? 16 : 0);
-      if (has_lo) cp_async16(ls + swz(row, ch), s.a_lo + off, ok ? 16 : 0);
-    }
-  };
-
-  float acc[MT][4];
-#pragma unroll
-  for (int j = 0; j < MT; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
-
-#pragma unroll
-  for (int st = 0; st < G_STAGES - 1; ++st) {
-    if (st < nk) load_stage(st, st);
-    cp_async_commit();
-  }
-  const int wrow = warp * 16;
-  for (int kt = 0; kt < nk; ++kt) {
-    cp_async_wait<G_STAGES - 2>();
-    __syncthreads();
-    const int nxt = kt + G_STAGES - 1;
-    if (nxt < nk) load_stage(nxt % G_STAGES, nxt);
-    cp_async_commit();
-    const uint32_t ws = sbase + (kt % G_STAGES) * STAGE, as = ws + W_BYTES, ls = as + A_BYTES;
-#pragma unroll
-    for (int ks = 0; ks < GB_K / 16; ++ks) {
-      uint32_t af[4];
-      {
-        const int row = wrow + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int ch = ks * 2 + (lane >> 4);
-        ldsm_x4(ws + swz(row, ch), af[0], af[1], af[2], af[3]);
-      }
-#pragma unroll
-      for (int j = 0; j < MT; ++j) {
-        const int row = j * 8 + (lane & 7);
-        const int ch = ks * 2 + ((lane >> 3) & 1);
-        if (has_lo) {
-          uint32_t b0, b1, c0, c1;
-          const uint32_t base = (lane < 16) ? as : ls;
-          ldsm_x4(base + swz(row, ch), b0, b1, c0, c1);
-          mma_bf16_16816(acc[j], af, b0, b1);
-          mma_bf16_16816(acc[j], af, c0, c1);
-        } else {
-          uint32_t b0, b1;
-          ldsm_x2(as + swz(row, ch), b0, b1);
-          mma_bf16_16816(acc[j], af, b0, b1);
-        }
-      }
-    }
-  }
-  cp_async_wait<0>();
-
-  // C fragment: rows (weights) wrow + lane/4 (+8), columns (activations) 2*(lane%4) (+1)
-#pragma unroll
-  for (int j = 0; j < MT; ++j) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int r = rbase + wrow + (lane >> 2) + (e >> 1) * 8;
-      const int m = m0 + j * 8 + (lane & 3) * 2 + (e & 1);
-      if (r < s.rows && m < a.M) epilogue_store(a, s, m, r, acc[j][e]);
-    }
-  }
-}
-
-template <int MT>
-static cudaError_t mma_go(MatArgs& a, cudaStream_t st) {
-  constexpr int AR = MT * 8;
-  const size_t smem = (size_t)G_STAGES * (GB_R * 128 + 2 * AR * 128);
-  cudaError_t e = cudaFuncSetAttribute(mma_gemm_kernel<MT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((a.M + AR - 1) / AR, a.tile_off[a.nseg]);
-  mma_gemm_kernel<MT><<<grid, 256, smem, st>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_mma_gemm(MatArgs a, cudaStream_t st) {
-  a.tile_off[0] = 0;
-  for (int i = 0; i < a.nseg; ++i)
-    a.tile_off[i + 1] = a.tile_off[i] + (a.seg[i].rows + GB_R - 1) / GB_R;
-  const int tiles8 = (a.M + 7) / 8;
-  if (tiles8 <= 1) return mma_go<1>(a, st);
-  if (tiles8 <= 2) return mma_go<2>(a, st);
-  if (tiles8 <= 4) return mma_go<4>(a, st);
-  if (tiles8 <= 6) return mma_go<6>(a, st);
-  if (tiles8 <= 9) return mma_go<9>(a, st);
-  if (tiles8 <= 12) return mma_go<12>(a, st);
-  return mma_go<16>(a, st);
 }
 
 // =========================================================== small helpers

@@ -1,0 +1,346 @@
+// Tensor-core (tcgen05) weight-streaming projection for sm_103a:
+//   Y[m][r] = sum_k X[m][k] W[r][k]   (+ the step's epilogues, see MatArgs)
+// for tens to hundreds of activation rows X against a weight matrix W that is read once.
+//
+// One CTA owns 128 weight rows and `nbox` activation rows.  The weights are the MMA's A
+// operand (M = 128), the activations its B operand (N = nbox), both K-major bf16 tiles of
+// 64 columns with the 128-byte swizzle, staged by TMA through an mbarrier ring.  fp32
+// activations arrive as bf16 hi + lo halves; both MMAs accumulate into one fp32 TMEM
+// accumulator, so the products keep ~fp32 accuracy at no extra TMEM.  Warp 0 lane 0
+// issues the TMA loads, warp 1 lane 0 the MMAs; then all four warps read their 32 TMEM
+// lanes and run the epilogue (one weight row per thread, coalesced over r).
+//
+// Every wait is bounded (~1 s of GPU time): on expiry the CTA sets MEDUSA_FLAG_TIMEOUT,
+// drains (again bounded) the copies it issued, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace medusa {
+
+constexpr int UM_R = 128;           // weight rows per CTA (MMA M)
+constexpr int UM_K = 64;            // K per stage (one 128-byte swizzle row)
+constexpr uint32_t UM_W_BYTES = UM_R * 128;
+constexpr uint64_t UM_TIMEOUT_NS = 1000000000ull;
+
+struct UmmaArgs {
+  CUtensorMap tw[kMaxSeg];   // weights of each segment: dims {k, rows}, box {64, 128}
+  CUtensorMap ta[kMaxSeg];   // activations (hi): dims {k, M}, box {64, nbox}
+  CUtensorMap tl[kMaxSeg];   // activations (lo)
+  MatArgs m;
+  int nbox;                  // activation rows per CTA = MMA N (multiple of 16, <= 256)
+  int stages;
+  uint32_t tmem_cols;
+  uint32_t* status;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase of `parity` to complete; false after the time limit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = gtimer();
+  while (!mbar_try(bar, parity))
+    if (gtimer() - t0 > limit_ns) return false;
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// D[tmem] (+)= A(smem desc) * B(smem desc)^T, kind::f16 (bf16 inputs, fp32 accumulate)
+__device__ __forceinline__ void umma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor of a K-major tile with the 128-byte swizzle: rows of
+// 128 bytes, 8-row groups 1024 bytes apart (tile base 1024-byte aligned).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address, 16-byte units
+  d |= (uint64_t)1 << 16;                             // leading offset (unused: swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;                   // stride offset between 8-row groups
+  d |= (uint64_t)1 << 46;                             // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                             // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_epilogue(const MatArgs& a, const MatSeg& s, int m, int r,
+                                              float acc) {
+  float y = acc;
+  if (a.epi == EPI_SILU_RES) {
+    y = silu(acc) + a.res_f32[(long)m * a.ldr + r];
+  } else if (a.epi == EPI_RES_ADD) {
+    const float res = a.res_f32 ? a.res_f32[(long)m * a.ldr + r]
+                                : to_f32(reinterpret_cast<const bf16*>(a.res_w)[(long)m * a.ldr + r]);
+    y = acc + res;
+  }
+  const long o = (long)m * a.ldo + s.out_off + r;
+  a.out[o] = y;
+  if (a.out_hi) {
+    bf16 hi, lo;
+    split_hi_lo(y, hi, lo);
+    a.out_hi[o] = hi;
+    a.out_lo[o] = lo;
+  }
+}
+
+template <bool HAS_LO>
+__global__ void __launch_bounds__(128, 1) umma_gemm_kernel(const __grid_constant__ UmmaArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bars[2 * 8 + 1];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int s_issued, s_consumed;
+  const MatArgs& a = g.m;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int si = 0;
+  while (si + 1 < a.nseg && (int)blockIdx.y >= a.tile_off[si + 1]) ++si;
+  const MatSeg& s = a.seg[si];
+  const int rbase = ((int)blockIdx.y - a.tile_off[si]) * UM_R;
+  const int m0 = (int)blockIdx.x * g.nbox;
+  const int nk = (a.k + UM_K - 1) / UM_K;
+  const int S = g.stages;
+  const uint32_t A_BYTES = (uint32_t)g.nbox * 128;
+  const uint32_t STAGE = UM_W_BYTES + A_BYTES * (HAS_LO ? 2 : 1);
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int i) { return bar0 + 8u * i; };
+  auto empty = [&](int i) { return bar0 + 8u * (8 + i); };
+  const uint32_t accb = bar0 + 8u * 16;
+
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full(i), 1);
+      mbar_init(empty(i), 1);
+    }
+    mbar_init(accb, 1);
+    s_issued = 0;
+    s_consumed = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), g.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  bool timed_out = false;
+
+  if (warp == 0 && lane == 0) {                         // ---- TMA producer
+    const uint64_t pw = policy_evict_first(), pa = policy_evict_last();
+    int kt = 0;
+    for (; kt < nk; ++kt) {
+      const int st = kt % S;
+      if (!mbar_wait(empty(st), ((kt / S) & 1) ^ 1, UM_TIMEOUT_NS)) { timed_out = true; break; }
+      mbar_expect_tx(full(st), STAGE);
+      const uint32_t ws = base + st * STAGE;
+      tma_load_2d(ws, &g.tw[si], kt * UM_K, rbase, full(st), pw);
+      tma_load_2d(ws + UM_W_BYTES, &g.ta[si], kt * UM_K, m0, full(st), pa);
+      if (HAS_LO) tma_load_2d(ws + UM_W_BYTES + A_BYTES, &g.tl[si], kt * UM_K, m0, full(st), pa);
+    }
+    s_issued = kt;
+  } else if (warp == 1 && lane == 0) {                  // ---- MMA issuer
+    const uint32_t idesc = idesc_bf16(UM_R, g.nbox);
+    int kt = 0;
+    for (; kt < nk; ++kt) {
+      const int st = kt % S;
+      if (!mbar_wait(full(st), (kt / S) & 1, UM_TIMEOUT_NS)) { timed_out = true; break; }
+      tc_fence_after();
+      const uint32_t ws = base + st * STAGE;
+      const uint64_t ad = sw128_desc(ws), bd = sw128_desc(ws + UM_W_BYTES);
+      const uint64_t ld = sw128_desc(ws + UM_W_BYTES + A_BYTES);
+#pragma unroll
+      for (int ks = 0; ks < UM_K / 16; ++ks) {          // +32 bytes along K per step
+        umma_bf16(tmem, ad + 2 * ks, bd + 2 * ks, idesc, (kt | ks) != 0);
+        if (HAS_LO) umma_bf16(tmem, ad + 2 * ks, ld + 2 * ks, idesc, 1);
+      }
+      umma_commit(empty(st));                           // frees the stage when read
+    }
+    s_consumed = kt;
+    umma_commit(accb);                                  // accumulator complete
+  }
+  __syncwarp();
+  // ---- epilogue: thread = TMEM lane = weight row
+  const bool acc_ok = mbar_wait(accb, 0, UM_TIMEOUT_NS);
+  tc_fence_after();
+  __syncwarp();
+  if (acc_ok) {
+    const int r = rbase + warp * 32 + lane;
+    for (int c0 = 0; c0 < g.nbox; c0 += 16) {
+      float v[16];
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+      if (r < s.rows) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = m0 + c0 + j;
+          if (m < a.M) umma_epilogue(a, s, m, r, v[j]);
+        }
+      }
+    }
+  }
+  if (timed_out || !acc_ok) set_flag(g.status, MEDUSA_FLAG_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {                                       // drain copies issued but not consumed
+    for (int kt = s_consumed; kt < s_issued; ++kt)
+      mbar_wait(full(kt % S), (kt / S) & 1, UM_TIMEOUT_NS / 16);
+  }
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, g.tmem_cols);
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map: `rows` rows of `cols` elements at `ld` elements apart; box
+// {64, box_rows}, 128-byte swizzle, zero fill out of bounds.
+static bool make_map(CUtensorMap* map, const void* ptr, long cols, long rows, long ld, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn || !ptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)UM_K, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st) {
+  static UmmaArgs g;                      // ~4.5 KB: keep it off the host stack
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  std::memset(&g, 0, sizeof(g));
+  g.m = m;
+  MatArgs& a = g.m;
+  a.tile_off[0] = 0;
+  for (int i = 0; i < a.nseg; ++i) a.tile_off[i + 1] = a.tile_off[i] + (a.seg[i].rows + UM_R - 1) / UM_R;
+  const bool has_lo = a.seg[0].a_lo != nullptr;
+  for (int i = 1; i < a.nseg; ++i)
+    if ((a.seg[i].a_lo != nullptr) != has_lo) return cudaErrorInvalidValue;
+  int nbox = (a.M + 15) / 16 * 16;
+  const int cap = has_lo ? 128 : 256;
+  nbox = nbox > cap ? cap : nbox;
+  g.nbox = nbox;
+  uint32_t cols = 32;
+  while (cols < (uint32_t)nbox) cols <<= 1;
+  g.tmem_cols = cols;
+  const uint32_t stage = UM_W_BYTES + (uint32_t)nbox * 128 * (has_lo ? 2 : 1);
+  int stages = (int)((200u * 1024u) / stage);
+  g.stages = stages > 8 ? 8 : stages;
+  if (g.stages < 2) return cudaErrorInvalidValue;
+  g.status = status;
+  for (int i = 0; i < a.nseg; ++i) {
+    const MatSeg& s = a.seg[i];
+    if (!make_map(&g.tw[i], s.w, a.k, s.rows, a.k, UM_R)) return cudaErrorInvalidValue;
+    if (!make_map(&g.ta[i], s.a_hi, a.k, a.M, s.ldx, nbox)) return cudaErrorInvalidValue;
+    if (has_lo && !make_map(&g.tl[i], s.a_lo, a.k, a.M, s.ldx, nbox)) return cudaErrorInvalidValue;
+  }
+  const size_t smem = (size_t)g.stages * stage + 1024;
+  auto kern = has_lo ? umma_gemm_kernel<true> : umma_gemm_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.M + nbox - 1) / nbox, a.tile_off[a.nseg]);
+  kern<<<grid, 128, smem, st>>>(g);
+  return cudaGetLastError();
+}
+
+}  // namespace medusa

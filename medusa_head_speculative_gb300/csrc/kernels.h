@@ -45,8 +45,9 @@ struct MatArgs {
 
 // CUDA-core row-dot projection: dtype 0 = f32 weights, 1 = bf16.
 cudaError_t launch_rowdot(const MatArgs& a, int dtype, cudaStream_t st);
-// Tensor-core (mma.sync bf16) projection; bf16 weights only.
-cudaError_t launch_mma_gemm(MatArgs a, cudaStream_t st);
+// Tensor-core (tcgen05 + TMA + TMEM) projection; bf16 weights only.  Sets
+// MEDUSA_FLAG_TIMEOUT in *status if a pipeline wait expires.
+cudaError_t launch_umma_gemm(const MatArgs& a, uint32_t* status, cudaStream_t st);
 // fp32 -> bf16 hi/lo split of n elements.
 cudaError_t launch_split(const float* x, __nv_bfloat16* hi, __nv_bfloat16* lo, long n,
                          cudaStream_t st);
