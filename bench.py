@@ -211,21 +211,42 @@ def run_ours(args, w: S.Workload):
     one_step()
     _, per_step = plan.profile_stop()
 
+    # The step as a CUDA graph (the same kernels and arguments, replayed without per-launch
+    # host overhead); direct calls if capture is not possible.
+    graph, launch_mode = None, "direct"
+    if not args.no_graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                Bnd.step(plan, st["h"], None, st["wstruct"], st["kv"], st["acc"], st["outs"],
+                         st["ws"])
+            g.replay()
+            torch.cuda.synchronize(device)
+            graph, launch_mode = g, "cuda_graph"
+        except Exception as exc:                        # noqa: BLE001
+            launch_mode = f"direct (graph capture failed: {exc})"[:160]
+    run = graph.replay if graph is not None else one_step
+
     K = args.steps
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     barrier()
     clocks.start()
     time.sleep(0.3)                      # let the sampler attach before the region starts
-    plan.profile_start(K * per_step + 16)
     e0.record(stream)
     for _ in range(K):
-        one_step()
+        run()
     e1.record(stream)
     barrier()
-    kernels, launches = plan.profile_stop()
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
+    launches = K * per_step
+    # per-kernel times: CUDA events around every launch, in a second timed region
+    kp = min(K, 300)
+    plan.profile_start(kp * per_step + 16)
+    for _ in range(kp):
+        one_step()
+    kernels, _ = plan.profile_stop()
     t = torch.tensor([ms], dtype=torch.float64, device=device)
     if dist is not None:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -301,6 +322,7 @@ def run_ours(args, w: S.Workload):
                 "d2h_bytes_per_step": int(tok_host.numel() * 4 + nacc_host.numel() * 4)},
         "clocks": clk,
         "gpu_launches": int(launches),
+        "launch": launch_mode,
     }
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, st, plan_spec=(st["parent"], st["rank"]))
@@ -400,6 +422,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="vicuna7b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time direct calls, not a CUDA graph")
     args = ap.parse_args()
     w = S.workload(args.workload)
     res = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)

@@ -30,12 +30,13 @@ bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15
 enum KernelName {
   KN_H_SPLIT, KN_H_W1, KN_H_VOCAB, KN_TOPK_PARTIAL, KN_TOPK_MERGE, KN_TREE_BUILD, KN_GATHER,
   KN_QKV, KN_ROPE, KN_ATTN, KN_COMBINE, KN_O_SPLIT, KN_OUT, KN_HP_SPLIT, KN_VLOGITS, KN_VSTATS,
-  KN_ACCEPT, KN_COMPACT, KN_COUNT
+  KN_ACCEPT, KN_COMPACT, KN_QCAST, KN_COUNT
 };
 static const char* const kKernelNames[KN_COUNT] = {
   "split_h", "heads_w1", "heads_vocab", "topk_partial", "topk_merge", "tree_build",
   "embed_gather", "layer_qkv", "rope_split", "tree_attention", "attn_combine", "split_o",
-  "layer_out", "split_hprime", "verify_logits", "verify_stats", "verify_accept", "kv_compact"};
+  "layer_out", "split_hprime", "verify_logits", "verify_stats", "verify_accept", "kv_compact",
+  "cast_q"};
 
 struct Profiler {
   bool on = false;
@@ -61,6 +62,7 @@ struct medusa_plan {
   uint32_t* d_status = nullptr;
   int device = 0, num_sms = 148;
   bool tc_heads = false, tc_nodes = false;   // tensor-core projections
+  bool tc_attn = false;                      // tensor-core tree attention
   int M;                                     // node rows B * n1
   int topk_splits, topk_chunk;
   int nsplit, chunk, rpw, rows_per_block, nrb;
@@ -68,7 +70,7 @@ struct medusa_plan {
   size_t o_logits, o_u, o_uhi, o_ulo, o_hhi, o_hlo, o_cv, o_ci, o_ttok, o_tval, o_root;
   size_t o_tok, o_pos, o_mask, o_retr, o_x, o_qkv, o_q, o_tk, o_tv, o_po, o_pml;
   size_t o_o, o_ohi, o_olo, o_hp, o_hphi, o_hplo, o_vlog, o_am, o_stats, o_path, o_nacc;
-  size_t o_otok, o_hnext, o_rnext;
+  size_t o_otok, o_hnext, o_rnext, o_qb;
   size_t ws_bytes;
 
   const int32_t* dparent() const { return d_spec; }
@@ -186,6 +188,7 @@ void layout(medusa_plan* p) {
   p->o_otok = take(B * (K + 1) * 4);
   p->o_hnext = take(B * D * 4);
   p->o_rnext = take(B * 4);
+  p->o_qb = take(p->tc_attn ? M * qd * 2 : 0);
   p->ws_bytes = off;
 }
 
@@ -307,12 +310,13 @@ medusa_status qkv_impl(const medusa_plan* p, const medusa_weights* w, const int3
     s.out_off = offs[i];
   }
   LAUNCH(p, KN_QKV, st, p->tc_nodes ? launch_umma_gemm(a, p->d_status, st) : launch_rowdot(a, d.dtype, st));
-  LAUNCH(p, KN_ROPE, st, launch_rope_split(qkv, pos, p->M, d.Hq, d.Hkv, d.dh, d.rope_base, d.dtype, q, tk, tv, st));
+  LAUNCH(p, KN_ROPE, st, launch_rope_split(qkv, pos, p->M, d.Hq, d.Hkv, d.dh, d.rope_base, d.dtype, q,
+                                           p->tc_attn ? at<bf16>(ws, p->o_qb) : nullptr, tk, tv, st));
   return MEDUSA_OK;
 }
 
 medusa_status attn_impl(const medusa_plan* p, const float* q, const medusa_kv* kv, const void* tk,
-                        const void* tv, const uint32_t* mask, float* o, bool split_out, void* ws,
+                        const void* tv, const uint32_t* mask, float* o, bool split_out, bool q_ready, void* ws,
                         cudaStream_t st) {
   const medusa_dims& d = p->d;
   AttnArgs a{};
@@ -346,7 +350,13 @@ medusa_status attn_impl(const medusa_plan* p, const float* q, const medusa_kv* k
   a.o_lo = split_out && p->tc_nodes ? at<bf16>(ws, p->o_olo) : nullptr;
   a.status = p->d_status;
   a.scale = 1.0f / std::sqrt((float)d.dh);
-  LAUNCH(p, KN_ATTN, st, launch_tree_attention(a, d.dtype, st));
+  if (p->tc_attn) {
+    bf16* qb = at<bf16>(ws, p->o_qb);
+    if (!q_ready) LAUNCH(p, KN_QCAST, st, launch_to_bf16(q, qb, (long)p->M * d.Hq * d.dh, st));
+    LAUNCH(p, KN_ATTN, st, launch_tree_attention_tc(a, qb, st));
+  } else {
+    LAUNCH(p, KN_ATTN, st, launch_tree_attention(a, d.dtype, st));
+  }
   LAUNCH(p, KN_COMBINE, st, launch_attn_combine(a, st));
   return MEDUSA_OK;
 }
@@ -563,14 +573,16 @@ medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec
   // attention: query-row blocks and prefix splits so the grid covers the SMs ~2x
   const int G = dims->Hq / dims->Hkv;
   const int R = p->n1 * G;
+  p->tc_attn = tree_attention_tc_supported(dims->dtype, dims->dh, G, dims->page_size);
   p->rpw = R <= 32 ? 4 : (R <= 72 ? 9 : 12);
-  p->rows_per_block = 8 * p->rpw;
+  p->rows_per_block = p->tc_attn ? 128 : 8 * p->rpw;
   p->nrb = (R + p->rows_per_block - 1) / p->rows_per_block;
   const int base = dims->B * dims->Hkv * p->nrb;
   const int want = std::max(1, (2 * p->num_sms + base - 1) / base);
-  const int max_splits = std::max(1, (dims->capacity + 31) / 32);
+  const int gran = p->tc_attn ? 64 : 32;              // keys per chunk of the kernel
+  const int max_splits = std::max(1, (dims->capacity + gran - 1) / gran);
   p->nsplit = std::min(want, max_splits);
-  p->chunk = ((dims->capacity + p->nsplit - 1) / p->nsplit + 31) / 32 * 32;
+  p->chunk = ((dims->capacity + p->nsplit - 1) / p->nsplit + gran - 1) / gran * gran;
   p->nsplit = (dims->capacity + p->chunk - 1) / p->chunk;
   layout(p);
 
@@ -693,7 +705,7 @@ medusa_status medusa_tree_attention(const medusa_plan* p, const float* q, const 
   medusa_status s = check_kv(p, kv, false);
   if (s != MEDUSA_OK) return s;
   if ((s = check_ws(p, ws, ws_bytes)) != MEDUSA_OK) return s;
-  return attn_impl(p, q, kv, tk, tv, mask, o, false, ws, S(stream));
+  return attn_impl(p, q, kv, tk, tv, mask, o, false, false, ws, S(stream));
 }
 
 medusa_status medusa_layer_out(const medusa_plan* p, const medusa_weights* w, const int32_t* tok,
@@ -769,7 +781,7 @@ medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* r
   if ((s = tree_impl(p, ttok, root, kv->len, tok, pos, mask, retr, st)) != MEDUSA_OK) return s;
   if ((s = gather_impl(p, w, tok, ws, st)) != MEDUSA_OK) return s;
   if ((s = qkv_impl(p, w, pos, q, tk, tv, ws, st)) != MEDUSA_OK) return s;
-  if ((s = attn_impl(p, q, kv, tk, tv, mask, o, true, ws, st)) != MEDUSA_OK) return s;
+  if ((s = attn_impl(p, q, kv, tk, tv, mask, o, true, true, ws, st)) != MEDUSA_OK) return s;
   if ((s = out_impl(p, w, o, true, hp, true, ws, st)) != MEDUSA_OK) return s;
   if ((s = vlogits_impl(p, w, hp, true, tok, acc, at<float>(ws, p->o_vlog), am, stats, ws, st)) != MEDUSA_OK)
     return s;

@@ -1,0 +1,361 @@
+// Tensor-core (tcgen05) tree attention for sm_103a, bf16 caches with dh = 64 or 128.
+//
+// Same split-KV decomposition and partial format as the CUDA-core kernel in k_attn.cu
+// ("Medusa: Simple LLM Inference Acceleration Framework with Multiple Decoding Heads"
+// §3.4 Tree Attention, Steps 3 and 5): CTA (split, kv head g, sequence b, row block) covers
+// one chunk of the prefix, or (split == nsplit) the tree keys under the ancestor bitmask,
+// for 128 query rows (node, query head of the group).  Inside the CTA the keys are walked
+// in 64-key chunks:
+//   warp 4 (one lane)  TMA: Q once, then K and V chunks through a 3-stage mbarrier ring
+//                      (paged caches: one box per page)
+//   warp 5 (one lane)  MMAs: S = Q K^T into one of two TMEM buffers (issued one chunk
+//                      ahead), then O = P V with V as an MN-major operand
+//   warps 0-3          one query row per thread: masked online softmax of S, P written as
+//                      bf16 into swizzled shared memory, O accumulated in registers
+// Each CTA writes one unnormalised partial (o, max, sum) per row, merged by
+// attn_combine_kernel.  Every wait is bounded; on expiry MEDUSA_FLAG_TIMEOUT is set.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace medusa {
+
+constexpr int AT_ROWS = 128;      // query rows per CTA (MMA M, TMEM lanes)
+constexpr int AT_KEYS = 64;       // keys per chunk (S columns, PV reduction)
+constexpr int AT_STAGES = 3;      // K/V ring depth
+constexpr uint32_t AT_TMEM_COLS = 256;   // S0 [0,64), S1 [64,128), O [128, 128+dh)
+
+struct AttnTcArgs {
+  CUtensorMap tq;        // q bf16:    dims {dh, Hq, B*n1},   box {64, G, 128/G}
+  CUtensorMap tk, tv;    // cache:     dims {dh, Hkv, slots}, box {64, 1, kbox}
+  CUtensorMap ttk, ttv;  // tree K/V:  dims {dh, Hkv, B*n1},  box {64, 1, 64}
+  AttnArgs a;
+  int kbox;              // cache rows per TMA box: 64 (contiguous) or the page size
+};
+
+enum { BQ = 0, BKVF = 1, BKVE = BKVF + AT_STAGES, BSF = BKVE + AT_STAGES, BOF = BSF + 2, BPR = BOF + 1,
+       BCOUNT = BPR + 1 };
+
+template <int DH>
+__global__ void __launch_bounds__(192, 1) tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
+  constexpr int H = DH / 64;                        // 64-column halves of a head
+  constexpr uint32_t QH = AT_ROWS * 128;            // one half of Q: 16 KB
+  constexpr uint32_t KVH = AT_KEYS * 128;           // one half of a 64-key K or V tile: 8 KB
+  constexpr uint32_t KV_STAGE = 2 * H * KVH;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bars[BCOUNT];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int s_issued, s_waited, s_qok;
+  const AttnArgs& a = g.a;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x, gk = blockIdx.y;
+  const int b = blockIdx.z / a.nrb, rb = blockIdx.z % a.nrb;
+  const int G = a.G, R = a.n1 * G;
+  const int row0 = rb * AT_ROWS, node0 = row0 / G;
+  const bool tree = split == a.nsplit;
+  int L = a.len[b];
+  L = L < 0 ? 0 : (L > a.capacity ? a.capacity : L);
+  const int kbeg = tree ? 0 : split * a.chunk;
+  const int kend = tree ? a.n1 : min(L, kbeg + a.chunk);
+  const int nch = kend > kbeg ? (kend - kbeg + AT_KEYS - 1) / AT_KEYS : 0;
+  const uint32_t sraw = smem_u32(smem_raw);
+  const uint32_t base = (sraw + 1023u) & ~1023u;
+  const uint32_t qs = base, kv0 = base + H * QH, ps = kv0 + AT_STAGES * KV_STAGE;
+  const uint32_t bar0 = smem_u32(bars);
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+
+  if (tid == 0) {
+    mbar_init(bar(BQ), 1);
+    for (int i = 0; i < AT_STAGES; ++i) {
+      mbar_init(bar(BKVF + i), 1);
+      mbar_init(bar(BKVE + i), 1);
+    }
+    mbar_init(bar(BSF), 1);
+    mbar_init(bar(BSF + 1), 1);
+    mbar_init(bar(BOF), 1);
+    mbar_init(bar(BPR), AT_ROWS);
+    s_issued = 0;
+    s_waited = 0;
+    s_qok = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 5) tmem_alloc(smem_u32(&tmem_slot), AT_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  bool timed_out = false;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && nch > 0) {
+      const uint64_t pol_kv = policy_evict_first(), pol_q = policy_evict_last();
+      mbar_expect_tx(bar(BQ), H * QH);
+#pragma unroll
+      for (int h = 0; h < H; ++h)
+        tma_load_3d(qs + h * QH, &g.tq, h * 64, gk * G, b * a.n1 + node0, bar(BQ), pol_q);
+      int i = 0;
+      for (; i < nch; ++i) {
+        const int st = i % AT_STAGES;
+        if (!mbar_wait(bar(BKVE + st), ((i / AT_STAGES) & 1) ^ 1, TC_TIMEOUT_NS)) {
+          timed_out = true;
+          break;
+        }
+        mbar_expect_tx(bar(BKVF + st), KV_STAGE);
+        const uint32_t ks = kv0 + st * KV_STAGE, vs = ks + H * KVH;
+        const int t0 = kbeg + i * AT_KEYS;
+        if (tree) {
+#pragma unroll
+          for (int h = 0; h < H; ++h) {
+            tma_load_3d(ks + h * KVH, &g.ttk, h * 64, gk, b * a.n1 + t0, bar(BKVF + st), pol_kv);
+            tma_load_3d(vs + h * KVH, &g.ttv, h * 64, gk, b * a.n1 + t0, bar(BKVF + st), pol_kv);
+          }
+        } else if (a.page_table) {
+          for (int j = 0; j < AT_KEYS; j += g.kbox) {
+            const int t = t0 + j;
+            int page = 0;
+            if (t < a.capacity) {
+              page = a.page_table[(long)b * a.pages_per_seq + t / a.page_size];
+              if (page < 0 || page >= a.num_pages) {
+                set_flag(a.status, MEDUSA_FLAG_PAGE_RANGE);
+                page = 0;
+              }
+            }
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+              tma_load_3d(ks + h * KVH + j * 128, &g.tk, h * 64, gk, page * a.page_size, bar(BKVF + st), pol_kv);
+              tma_load_3d(vs + h * KVH + j * 128, &g.tv, h * 64, gk, page * a.page_size, bar(BKVF + st), pol_kv);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < H; ++h) {
+            tma_load_3d(ks + h * KVH, &g.tk, h * 64, gk, b * a.capacity + t0, bar(BKVF + st), pol_kv);
+            tma_load_3d(vs + h * KVH, &g.tv, h * 64, gk, b * a.capacity + t0, bar(BKVF + st), pol_kv);
+          }
+        }
+      }
+      s_issued = i;
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nch > 0) {
+      int waited = 0;
+      if (!mbar_wait(bar(BQ), 0, TC_TIMEOUT_NS)) {
+        timed_out = true;
+      } else {
+        s_qok = 1;
+        const uint32_t id_qk = idesc_bf16(AT_ROWS, AT_KEYS);
+        const uint32_t id_pv = idesc_bf16(AT_ROWS, DH) | IDESC_B_MN_MAJOR;
+        auto issue_qk = [&](int i) -> bool {
+          const int st = i % AT_STAGES;
+          if (!mbar_wait(bar(BKVF + st), (i / AT_STAGES) & 1, TC_TIMEOUT_NS)) return false;
+          waited = i + 1;
+          tc_fence_after();
+          const uint32_t ks = kv0 + st * KV_STAGE, d = tmem + (uint32_t)(i & 1) * AT_KEYS;
+#pragma unroll
+          for (int h = 0; h < H; ++h)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(d, sw128_desc(qs + h * QH) + 2 * kk, sw128_desc(ks + h * KVH) + 2 * kk, id_qk,
+                        (h | kk) != 0);
+          umma_commit(bar(BSF + (i & 1)));
+          return true;
+        };
+        if (!issue_qk(0)) timed_out = true;
+        for (int i = 0; i < nch && !timed_out; ++i) {
+          if (i + 1 < nch && !issue_qk(i + 1)) { timed_out = true; break; }
+          if (!mbar_wait(bar(BPR), i & 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+          tc_fence_after();
+          const uint32_t vs = kv0 + (i % AT_STAGES) * KV_STAGE + H * KVH;
+#pragma unroll
+          for (int kk = 0; kk < AT_KEYS / 16; ++kk)
+            umma_bf16(tmem + 128, sw128_desc(ps) + 2 * kk, sw128_desc_mn(vs + kk * 2048, KVH), id_pv,
+                      kk != 0);
+          umma_commit(bar(BOF));
+          umma_commit(bar(BKVE + i % AT_STAGES));
+        }
+      }
+      s_waited = waited;
+    }
+  } else {
+    // ------------------------------------------------------------ softmax rows
+    const int gr = row0 + tid;
+    const int node = gr / G;
+    const bool row_ok = gr < R;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    uint8_t* pgen = smem_raw + (ps - sraw);
+    float o_acc[DH];
+#pragma unroll
+    for (int c = 0; c < DH; ++c) o_acc[c] = 0.f;
+    float m_acc = -INFINITY, l_acc = 0.f, m_run = -INFINITY, m_prev = -INFINITY, l_prev = 0.f;
+
+    auto accumulate = [&](int j) -> bool {     // fold chunk j's P V into o_acc
+      if (!mbar_wait(bar(BOF), j & 1, TC_TIMEOUT_NS)) return false;
+      tc_fence_after();
+      __syncwarp();
+      const float sc = m_acc == -INFINITY ? 0.f : __expf(m_acc - m_prev);
+#pragma unroll
+      for (int c = 0; c < DH; c += 16) {
+        float v[16];
+        tmem_ld16(lane_base + 128 + c, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o_acc[c + e] = o_acc[c + e] * sc + v[e];
+      }
+      l_acc = l_acc * sc + l_prev;
+      m_acc = m_prev;
+      return true;
+    };
+
+    for (int i = 0; i < nch; ++i) {
+      if (!mbar_wait(bar(BSF + (i & 1)), (i >> 1) & 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+      tc_fence_after();
+      __syncwarp();
+      float s[AT_KEYS];
+#pragma unroll
+      for (int c = 0; c < AT_KEYS; c += 16) {
+        float v[16];
+        tmem_ld16(lane_base + (uint32_t)(i & 1) * AT_KEYS + c, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) s[c + e] = v[e];
+      }
+      const int t0 = kbeg + i * AT_KEYS;
+      uint32_t w0 = 0xffffffffu, w1 = 0xffffffffu;
+      if (tree) {
+        w0 = row_ok ? a.mask[(long)node * kMaskWords + (t0 >> 5)] : 0u;
+        w1 = row_ok && (t0 >> 5) + 1 < kMaskWords ? a.mask[(long)node * kMaskWords + (t0 >> 5) + 1] : 0u;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < AT_KEYS; ++j) {
+        const bool bit = ((j < 32 ? w0 : w1) >> (j & 31)) & 1u;
+        const bool valid = (t0 + j < kend) && bit;
+        s[j] = valid ? s[j] * a.scale : -INFINITY;
+        mx = fmaxf(mx, s[j]);
+      }
+      const float m_new = fmaxf(m_run, mx);
+      float lsum = 0.f;
+#pragma unroll
+      for (int j = 0; j < AT_KEYS; ++j) {
+        const float p = s[j] == -INFINITY ? 0.f : __expf(s[j] - m_new);
+        s[j] = p;
+        lsum += p;
+      }
+      if (i > 0 && !accumulate(i - 1)) { timed_out = true; break; }
+      // P row (bf16) into the 128-byte-swizzled K-major tile the PV MMA reads
+#pragma unroll
+      for (int c = 0; c < AT_KEYS / 8; ++c) {
+        uint4 u;
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(s[8 * c + 0], s[8 * c + 1]);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(s[8 * c + 2], s[8 * c + 3]);
+        __nv_bfloat162 p2 = __floats2bfloat162_rn(s[8 * c + 4], s[8 * c + 5]);
+        __nv_bfloat162 p3 = __floats2bfloat162_rn(s[8 * c + 6], s[8 * c + 7]);
+        u.x = *reinterpret_cast<uint32_t*>(&p0);
+        u.y = *reinterpret_cast<uint32_t*>(&p1);
+        u.z = *reinterpret_cast<uint32_t*>(&p2);
+        u.w = *reinterpret_cast<uint32_t*>(&p3);
+        *reinterpret_cast<uint4*>(pgen + tid * 128 + ((c ^ (tid & 7)) << 4)) = u;
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(bar(BPR));
+      m_prev = m_new;
+      l_prev = lsum;
+      m_run = m_new;
+    }
+    if (!timed_out && nch > 0 && !accumulate(nch - 1)) timed_out = true;
+    if (row_ok) {
+      const long pr = (((long)b * a.Hkv + gk) * (a.nsplit + 1) + split) * R + gr;
+      float4* dst = reinterpret_cast<float4*>(a.part_o + pr * DH);
+#pragma unroll
+      for (int c = 0; c < DH; c += 4) dst[c / 4] = make_float4(o_acc[c], o_acc[c + 1], o_acc[c + 2], o_acc[c + 3]);
+      a.part_ml[pr * 2] = m_acc;
+      a.part_ml[pr * 2 + 1] = l_acc;
+    }
+  }
+  if (timed_out) set_flag(a.status, MEDUSA_FLAG_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && nch > 0) {                 // drain copies issued but never waited for
+    if (!s_qok) mbar_wait(bar(BQ), 0, TC_TIMEOUT_NS / 16);
+    for (int i = s_waited; i < s_issued; ++i)
+      mbar_wait(bar(BKVF + i % AT_STAGES), (i / AT_STAGES) & 1, TC_TIMEOUT_NS / 16);
+  }
+  __syncthreads();
+  if (warp == 5) tmem_dealloc(tmem, AT_TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode3_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 [z][y][x] tensor (x contiguous, x = dh), box {64, by, bz}, 128-byte swizzle.
+static bool make_map3(CUtensorMap* map, const void* ptr, long x, long y, long z, int by, int bz) {
+  auto fn = encode3_fn();
+  if (!fn || !ptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)x, (cuuint64_t)y, (cuuint64_t)z};
+  cuuint64_t strides[2] = {(cuuint64_t)x * 2, (cuuint64_t)(x * y) * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)by, (cuuint32_t)bz};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tree_attention_tc_supported(int dtype, int dh, int G, int page_size) {
+  if (dtype != 1 || (dh != 64 && dh != 128)) return false;
+  if (G < 1 || G > AT_ROWS || AT_ROWS % G != 0) return false;
+  if (page_size > 0 && (page_size < 8 || page_size > AT_KEYS || AT_KEYS % page_size != 0)) return false;
+  return true;
+}
+
+cudaError_t launch_tree_attention_tc(const AttnArgs& a, const void* q_bf16, cudaStream_t st) {
+  static AttnTcArgs g;                     // ~700 bytes of tensor maps: kept off the stack
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  std::memset(&g, 0, sizeof(g));
+  g.a = a;
+  const long nodes = (long)a.B * a.n1;
+  if (!make_map3(&g.tq, q_bf16, a.dh, a.Hq, nodes, a.G, AT_ROWS / a.G)) return cudaErrorInvalidValue;
+  if (a.page_table) {
+    g.kbox = a.page_size;
+    const long slots = (long)a.num_pages * a.page_size;
+    if (!make_map3(&g.tk, a.kc, a.dh, a.Hkv, slots, 1, a.page_size)) return cudaErrorInvalidValue;
+    if (!make_map3(&g.tv, a.vc, a.dh, a.Hkv, slots, 1, a.page_size)) return cudaErrorInvalidValue;
+  } else {
+    g.kbox = AT_KEYS;
+    const long slots = (long)a.B * a.capacity;
+    if (!make_map3(&g.tk, a.kc, a.dh, a.Hkv, slots, 1, AT_KEYS)) return cudaErrorInvalidValue;
+    if (!make_map3(&g.tv, a.vc, a.dh, a.Hkv, slots, 1, AT_KEYS)) return cudaErrorInvalidValue;
+  }
+  if (!make_map3(&g.ttk, a.tk, a.dh, a.Hkv, nodes, 1, AT_KEYS)) return cudaErrorInvalidValue;
+  if (!make_map3(&g.ttv, a.tv, a.dh, a.Hkv, nodes, 1, AT_KEYS)) return cudaErrorInvalidValue;
+  const int H = a.dh / 64;
+  const size_t smem = 1024 + (size_t)H * AT_ROWS * 128 + (size_t)AT_STAGES * 2 * H * AT_KEYS * 128 +
+                      (size_t)AT_ROWS * 128;
+  auto kern = a.dh == 128 ? tree_attn_tc_kernel<128> : tree_attn_tc_kernel<64>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.nsplit + 1, a.Hkv, a.B * a.nrb);
+  kern<<<grid, 192, smem, st>>>(g);
+  return cudaGetLastError();
+}
+
+}  // namespace medusa

@@ -101,9 +101,22 @@ __global__ void __launch_bounds__(256) rowdot_kernel(MatArgs a, int rows_per_cta
 
 template <typename W, int MT>
 static cudaError_t rowdot_go(const MatArgs& a, cudaStream_t st) {
+  static int num_sms = 0;
+  if (!num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      num_sms = 148;
+  }
   int maxrows = 0;
-  for (int i = 0; i < a.nseg; ++i) maxrows = maxrows > a.seg[i].rows ? maxrows : a.seg[i].rows;
-  const int rows_per_cta = 64;
+  long total = 0;
+  for (int i = 0; i < a.nseg; ++i) {
+    maxrows = maxrows > a.seg[i].rows ? maxrows : a.seg[i].rows;
+    total += a.seg[i].rows;
+  }
+  // about 8 CTAs per SM (two rounds of 4 resident) so the row stream balances across SMs
+  int rows_per_cta = (int)(total / ((long)num_sms * 8)) / 8 * 8;
+  rows_per_cta = rows_per_cta < 8 ? 8 : (rows_per_cta > 64 ? 64 : rows_per_cta);
   dim3 grid((maxrows + rows_per_cta - 1) / rows_per_cta, a.nseg);
   const size_t smem = (size_t)MT * a.k * sizeof(float);
   if (smem > 48 * 1024) {
@@ -146,12 +159,30 @@ cudaError_t launch_split(const float* x, bf16* hi, bf16* lo, long n, cudaStream_
   return cudaGetLastError();
 }
 
+__global__ void to_bf16_kernel(const float* x, bf16* y, long n) {
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x)
+    y[i] = __float2bfloat16_rn(x[i]);
+}
+
+cudaError_t launch_to_bf16(const float* x, bf16* y, long n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const long blocks = (n + 255) / 256;
+  to_bf16_kernel<<<(int)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(x, y, n);
+  return cudaGetLastError();
+}
+
 template <typename W>
 __global__ void gather_kernel(const W* emb, const int32_t* tok, int d, int V, float* xf, bf16* xb) {
   const int m = blockIdx.x;
   int t = tok[m];
   t = (t < 0 || t >= V) ? 0 : t;                    // ids were range-checked upstream
   const W* src = emb + (long)t * d;
+  if (sizeof(W) == 2 && xb && !xf && d % 8 == 0) {        // bf16 -> bf16: 16-byte copies
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(xb + (long)m * d);
+    for (int j = threadIdx.x; j < d / 8; j += blockDim.x) d4[j] = s4[j];
+    return;
+  }
   for (int j = threadIdx.x; j < d; j += blockDim.x) {
     const float v = to_f32(src[j]);
     if (xf) xf[(long)m * d + j] = v;

@@ -7,6 +7,8 @@
 // Heads" §3.4 Tree Attention, Steps 1-4; "MEDUSA 精读" section 6 (tree mask, tree position
 // ids, flatten/restore indices).  Order of candidates: larger logit first, lower token id
 // on equal logits.
+#include <cmath>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -168,18 +170,22 @@ cudaError_t launch_tree_build(const TreeArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// One CTA per node row.  cos/sin of pos * base^(-2i/dh) are computed once per row in
-// double precision and applied to every query and key head (rotate-half convention).
+// One CTA per node row.  cos/sin of pos * theta_i (theta_i = base^(-2i/dh), computed on
+// the host in double) are evaluated once per row in double precision and applied to every
+// query and key head (rotate-half convention).
+struct RopeFreq {
+  double theta[64];
+};
+
 template <typename T>
 __global__ void rope_split_kernel(const float* qkv, const int32_t* pos, int Hq, int Hkv, int dh,
-                                  float base, float* q, T* tk, T* tv) {
+                                  RopeFreq f, float* q, bf16* qb, T* tk, T* tv) {
   extern __shared__ float cs[];                      // [dh/2] cos, [dh/2] sin
   const int m = blockIdx.x, half = dh / 2;
   const double p = (double)pos[m];
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    const double theta = pow((double)base, -2.0 * i / dh);
     double sn, cn;
-    sincos(p * theta, &sn, &cn);
+    sincos(p * f.theta[i], &sn, &cn);
     cs[i] = (float)cn;
     cs[half + i] = (float)sn;
   }
@@ -193,9 +199,13 @@ __global__ void rope_split_kernel(const float* qkv, const int32_t* pos, int Hq, 
     const float y0 = x[i] * c - x[i + half] * s;
     const float y1 = x[i + half] * c + x[i] * s;
     if (h < Hq) {
-      float* qo = q + ((long)m * Hq + h) * dh;
-      qo[i] = y0;
-      qo[i + half] = y1;
+      const long o = ((long)m * Hq + h) * dh;
+      q[o + i] = y0;
+      q[o + i + half] = y1;
+      if (qb) {
+        qb[o + i] = __float2bfloat16_rn(y0);
+        qb[o + i + half] = __float2bfloat16_rn(y1);
+      }
     } else {
       T* ko = tk + ((long)m * Hkv + (h - Hq)) * dh;
       ko[i] = from_f32<T>(y0);
@@ -207,16 +217,19 @@ __global__ void rope_split_kernel(const float* qkv, const int32_t* pos, int Hq, 
 }
 
 cudaError_t launch_rope_split(const float* qkv, const int32_t* pos, int M, int Hq, int Hkv, int dh,
-                              float base, int dtype, float* q, void* tk, void* tv,
+                              float base, int dtype, float* q, bf16* qb, void* tk, void* tv,
                               cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
+  if (dh > 128) return cudaErrorInvalidValue;
+  RopeFreq f;
+  for (int i = 0; i < dh / 2; ++i) f.theta[i] = std::pow((double)base, -2.0 * i / dh);
   const size_t smem = dh * sizeof(float);
   if (dtype == 0)
-    rope_split_kernel<float><<<M, 256, smem, st>>>(qkv, pos, Hq, Hkv, dh, base, q,
+    rope_split_kernel<float><<<M, 256, smem, st>>>(qkv, pos, Hq, Hkv, dh, f, q, qb,
                                                    reinterpret_cast<float*>(tk),
                                                    reinterpret_cast<float*>(tv));
   else
-    rope_split_kernel<bf16><<<M, 256, smem, st>>>(qkv, pos, Hq, Hkv, dh, base, q,
+    rope_split_kernel<bf16><<<M, 256, smem, st>>>(qkv, pos, Hq, Hkv, dh, f, q, qb,
                                                   reinterpret_cast<bf16*>(tk),
                                                   reinterpret_cast<bf16*>(tv));
   return cudaGetLastError();

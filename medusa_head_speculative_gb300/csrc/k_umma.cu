@@ -20,13 +20,13 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace medusa {
 
 constexpr int UM_R = 128;           // weight rows per CTA (MMA M)
 constexpr int UM_K = 64;            // K per stage (one 128-byte swizzle row)
 constexpr uint32_t UM_W_BYTES = UM_R * 128;
-constexpr uint64_t UM_TIMEOUT_NS = 1000000000ull;
 
 struct UmmaArgs {
   CUtensorMap tw[kMaxSeg];   // weights of each segment: dims {k, rows}, box {64, 128}
@@ -38,119 +38,6 @@ struct UmmaArgs {
   uint32_t tmem_cols;
   uint32_t* status;
 };
-
-// ------------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint64_t gtimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Wait for the phase of `parity` to complete; false after the time limit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_try(bar, parity)) return true;
-  const uint64_t t0 = gtimer();
-  while (!mbar_try(bar, parity))
-    if (gtimer() - t0 > limit_ns) return false;
-  return true;
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-// D[tmem] (+)= A(smem desc) * B(smem desc)^T, kind::f16 (bf16 inputs, fp32 accumulate)
-__device__ __forceinline__ void umma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive on `bar` once every MMA this thread issued so far has completed.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-// 16 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Shared-memory matrix descriptor of a K-major tile with the 128-byte swizzle: rows of
-// 128 bytes, 8-row groups 1024 bytes apart (tile base 1024-byte aligned).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address, 16-byte units
-  d |= (uint64_t)1 << 16;                             // leading offset (unused: swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;                   // stride offset between 8-row groups
-  d |= (uint64_t)1 << 46;                             // descriptor version for tcgen05
-  d |= (uint64_t)2 << 61;                             // 128-byte swizzle
-  return d;
-}
-// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, both K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
 
 __device__ __forceinline__ void umma_epilogue(const MatArgs& a, const MatSeg& s, int m, int r,
                                               float acc) {
@@ -217,7 +104,7 @@ __global__ void __launch_bounds__(128, 1) umma_gemm_kernel(const __grid_constant
     int kt = 0;
     for (; kt < nk; ++kt) {
       const int st = kt % S;
-      if (!mbar_wait(empty(st), ((kt / S) & 1) ^ 1, UM_TIMEOUT_NS)) { timed_out = true; break; }
+      if (!mbar_wait(empty(st), ((kt / S) & 1) ^ 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
       mbar_expect_tx(full(st), STAGE);
       const uint32_t ws = base + st * STAGE;
       tma_load_2d(ws, &g.tw[si], kt * UM_K, rbase, full(st), pw);
@@ -230,7 +117,7 @@ __global__ void __launch_bounds__(128, 1) umma_gemm_kernel(const __grid_constant
     int kt = 0;
     for (; kt < nk; ++kt) {
       const int st = kt % S;
-      if (!mbar_wait(full(st), (kt / S) & 1, UM_TIMEOUT_NS)) { timed_out = true; break; }
+      if (!mbar_wait(full(st), (kt / S) & 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
       tc_fence_after();
       const uint32_t ws = base + st * STAGE;
       const uint64_t ad = sw128_desc(ws), bd = sw128_desc(ws + UM_W_BYTES);
@@ -247,7 +134,7 @@ __global__ void __launch_bounds__(128, 1) umma_gemm_kernel(const __grid_constant
   }
   __syncwarp();
   // ---- epilogue: thread = TMEM lane = weight row
-  const bool acc_ok = mbar_wait(accb, 0, UM_TIMEOUT_NS);
+  const bool acc_ok = mbar_wait(accb, 0, TC_TIMEOUT_NS);
   tc_fence_after();
   __syncwarp();
   if (acc_ok) {
@@ -269,7 +156,7 @@ __global__ void __launch_bounds__(128, 1) umma_gemm_kernel(const __grid_constant
   __syncthreads();
   if (tid == 0) {                                       // drain copies issued but not consumed
     for (int kt = s_consumed; kt < s_issued; ++kt)
-      mbar_wait(full(kt % S), (kt / S) & 1, UM_TIMEOUT_NS / 16);
+      mbar_wait(full(kt % S), (kt / S) & 1, TC_TIMEOUT_NS / 16);
   }
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, g.tmem_cols);

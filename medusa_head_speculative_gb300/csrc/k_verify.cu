@@ -1,6 +1,7 @@
 // Verification and commit of the Medusa step.
 //   verify_stats   per node row of the verification logits: greedy token (lowest id on
-//                  ties) and, for typical acceptance, max z/T, log-sum-exp and entropy
+//                  ties) and, for typical acceptance, max z/T, log-sum-exp and entropy, in
+//                  one pass (running max with rescaled sums)
 //   verify_accept  accept flags, longest accepted root->leaf path, step outputs
 //   kv_compact     copies the kept nodes' keys/values into the cache after the prefix
 // Sources: "Medusa: Simple LLM Inference Acceleration Framework with Multiple Decoding
@@ -29,72 +30,118 @@ __device__ __forceinline__ void block_argmax(float& v, int& i, float* sv, int* s
   i = si[0];
 }
 
-__device__ __forceinline__ float block_sum(float v, float* sv) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  v = warp_sum(v);
-  __syncthreads();
-  if (lane == 0) sv[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    v = lane < nw ? sv[lane] : 0.f;
-    v = warp_sum(v);
-    if (lane == 0) sv[0] = v;
+// Softmax statistics relative to a running max m: S = sum e^(y-m), U = sum (y-m) e^(y-m).
+struct SoftStat {
+  float m, S, U;
+};
+__device__ __forceinline__ SoftStat stat_merge(SoftStat a, SoftStat b) {
+  const float M = fmaxf(a.m, b.m);
+  if (M == -INFINITY) return a;
+  SoftStat r{M, 0.f, 0.f};
+  if (a.m != -INFINITY) {
+    const float e = __expf(a.m - M);
+    r.S += e * a.S;
+    r.U += e * (a.U + (a.m - M) * a.S);
   }
-  __syncthreads();
-  return sv[0];
+  if (b.m != -INFINITY) {
+    const float e = __expf(b.m - M);
+    r.S += e * b.S;
+    r.U += e * (b.U + (b.m - M) * b.S);
+  }
+  return r;
+}
+__device__ __forceinline__ void stat_add(SoftStat& s, float y) {
+  if (y > s.m) {
+    if (s.m != -INFINITY) {
+      const float e = __expf(s.m - y);
+      s.U = e * (s.U + (s.m - y) * s.S);
+      s.S *= e;
+    }
+    s.m = y;
+  }
+  const float e = __expf(y - s.m);
+  s.S += e;
+  s.U += (y - s.m) * e;
 }
 
-// One CTA per node row (b, n).
-__global__ void __launch_bounds__(256) verify_stats_kernel(VerifyArgs a) {
-  __shared__ float sv[32];
+// One 1024-thread CTA per node row (b, n).
+__global__ void __launch_bounds__(1024) verify_stats_kernel(VerifyArgs a) {
+  __shared__ float sv[32], sS[32], sU[32];
   __shared__ int si[32];
   const int row = blockIdx.x;
   const int b = row / a.n1, n = row - b * a.n1;
   const float* z = a.logits + (long)row * a.V;
+  const bool typ = a.typical != 0;
+  const float T = a.temperature;
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   bool nonfinite = false;
-  for (int v = threadIdx.x; v < a.V; v += blockDim.x) {
-    const float x = z[v];
+  SoftStat st{-INFINITY, 0.f, 0.f};
+  auto take = [&](float x, int v) {
     nonfinite |= !isfinite(x);
     if (better(x, v, bv, bi)) { bv = x; bi = v; }
+    if (typ) stat_add(st, x / T);
+  };
+  if ((a.V & 3) == 0) {
+    const float4* z4 = reinterpret_cast<const float4*>(z);
+    for (int q = threadIdx.x; q < a.V / 4; q += blockDim.x) {
+      const float4 x = z4[q];
+      take(x.x, 4 * q);
+      take(x.y, 4 * q + 1);
+      take(x.z, 4 * q + 2);
+      take(x.w, 4 * q + 3);
+    }
+  } else {
+    for (int v = threadIdx.x; v < a.V; v += blockDim.x) take(z[v], v);
   }
   if (nonfinite) set_flag(a.status, MEDUSA_FLAG_NONFINITE);
-  block_argmax(bv, bi, sv, si);
-  if (bi < 0 || bi >= a.V) { set_flag(a.status, MEDUSA_FLAG_TOKEN_RANGE); bi = 0; }
-  float st[4] = {bv, 0.f, 0.f, 0.f};
-  if (a.typical) {
-    const float T = a.temperature;
-    const float ymax = bv / T;
-    float S = 0.f, U = 0.f;
-    for (int v = threadIdx.x; v < a.V; v += blockDim.x) {
-      const float y = z[v] / T - ymax;
-      const float e = __expf(y);
-      S += e;
-      U += y * e;
+  if (typ) {                                   // merge the rows' statistics across the CTA
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      SoftStat other{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.S, o),
+                     __shfl_xor_sync(0xffffffffu, st.U, o)};
+      st = stat_merge(st, other);
     }
-    S = block_sum(S, sv);
-    U = block_sum(U, sv);
-    const float logS = logf(S);
-    st[0] = ymax;
-    st[1] = logS;
-    st[2] = logS - U / S;                         // H = log S - sum(y e^y) / S
+    if (lane == 0) { sv[warp] = st.m; sS[warp] = st.S; sU[warp] = st.U; }
+    __syncthreads();
+    if (warp == 0) {
+      st = lane < nw ? SoftStat{sv[lane], sS[lane], sU[lane]} : SoftStat{-INFINITY, 0.f, 0.f};
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        SoftStat other{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.S, o),
+                       __shfl_xor_sync(0xffffffffu, st.U, o)};
+        st = stat_merge(st, other);
+      }
+      if (lane == 0) { sv[0] = st.m; sS[0] = st.S; sU[0] = st.U; }
+    }
+    __syncthreads();
+    st = SoftStat{sv[0], sS[0], sU[0]};
+    __syncthreads();
+  }
+  block_argmax(bv, bi, sv, si);
+  if (threadIdx.x != 0) return;
+  if (bi < 0 || bi >= a.V) { set_flag(a.status, MEDUSA_FLAG_TOKEN_RANGE); bi = 0; }
+  float out[4] = {bv, 0.f, 0.f, 0.f};
+  if (typ) {
+    const float logS = logf(st.S);
+    out[0] = st.m;
+    out[1] = logS;
+    out[2] = logS - st.U / st.S;               // H = log S - sum(y e^y) / S
     if (n > 0) {
       const int p = a.parent[n];
       const int t = a.tok[(long)b * a.n1 + n];
-      st[3] = a.logits[((long)b * a.n1 + p) * a.V + t] / T;
+      out[3] = a.logits[((long)b * a.n1 + p) * a.V + t] / T;
     }
-    if (!isfinite(st[1]) || !isfinite(st[2])) set_flag(a.status, MEDUSA_FLAG_NONFINITE);
+    if (!isfinite(out[1]) || !isfinite(out[2])) set_flag(a.status, MEDUSA_FLAG_NONFINITE);
   }
-  if (threadIdx.x == 0) {
-    a.am[row] = bi;
+  a.am[row] = bi;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) a.stats[(long)row * 4 + q] = st[q];
-  }
+  for (int q = 0; q < 4; ++q) a.stats[(long)row * 4 + q] = out[q];
 }
 
 cudaError_t launch_verify_stats(const VerifyArgs& a, cudaStream_t st) {
-  verify_stats_kernel<<<a.B * a.n1, 256, 0, st>>>(a);
+  verify_stats_kernel<<<a.B * a.n1, 1024, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -136,22 +183,21 @@ __global__ void __launch_bounds__(256) verify_accept_kernel(VerifyArgs a) {
     if (better((float)m, p, bv, bi)) { bv = (float)m; bi = p; }
   }
   block_argmax(bv, bi, sv, si);
-  if (tid == 0) {
-    const int m = (int)bv, best = bi;
-    int last = 0;
-    for (int l = 0; l < W; ++l) {
-      const int node = l <= m ? a.retrieve[(long)best * W + l] : -1;
-      if (node >= 0) last = node;
-      if (a.path_nodes) a.path_nodes[(long)b * W + l] = node;
-      a.out_tok[(long)b * W + l] = node >= 0 ? a.tok[rb + node] : -1;
+  if (tid < W) {
+    const int m = (int)bv, best = bi, l = tid;
+    const int node = l <= m ? a.retrieve[(long)best * W + l] : -1;
+    if (a.path_nodes) a.path_nodes[(long)b * W + l] = node;
+    a.out_tok[(long)b * W + l] = node >= 0 ? a.tok[rb + node] : -1;
+    if (l == m) {
+      a.n_acc[b] = m + 1;
+      a.root_next[b] = a.am[rb + node];
+      s_last = node;
     }
-    a.n_acc[b] = m + 1;
-    a.root_next[b] = a.am[rb + last];
-    s_last = last;
   }
   __syncthreads();
-  const float* src = a.hprime + (rb + s_last) * a.d;
-  for (int j = tid; j < a.d; j += blockDim.x) a.h_next[(long)b * a.d + j] = src[j];
+  const float4* src = reinterpret_cast<const float4*>(a.hprime + (rb + s_last) * a.d);
+  float4* dst = reinterpret_cast<float4*>(a.h_next + (long)b * a.d);
+  for (int j = tid; j < a.d / 4; j += blockDim.x) dst[j] = src[j];
 }
 
 cudaError_t launch_verify_accept(const VerifyArgs& a, cudaStream_t st) {
@@ -159,11 +205,14 @@ cudaError_t launch_verify_accept(const VerifyArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// One CTA per sequence: slot len + l <- tree node path_nodes[l], l < n_acc.
+// One CTA per sequence: slot len + l <- tree node path_nodes[l], l < n_acc, in 16-byte
+// pieces spread over all threads.
 template <typename T>
 __global__ void __launch_bounds__(256) kv_compact_kernel(CompactArgs a) {
   __shared__ int s_len, s_n;
+  __shared__ long s_dst[MEDUSA_MAX_HEADS + 1], s_src[MEDUSA_MAX_HEADS + 1];
   const int b = blockIdx.x;
+  const long row = (long)a.Hkv * a.dh;                // elements per cached token
   if (threadIdx.x == 0) {
     int L = a.len[b];
     L = L < 0 ? 0 : L;
@@ -173,39 +222,48 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(CompactArgs a) {
       set_flag(a.status, MEDUSA_FLAG_KV_CAPACITY);
       n = a.capacity > L ? a.capacity - L : 0;
     }
+    int kept = 0;
+    for (int l = 0; l < n; ++l) {
+      const int node = a.path_nodes[(long)b * (a.K + 1) + l];
+      const int t = L + l;
+      long slot = -1;
+      if (node >= 0 && node < a.n1) {
+        if (a.page_table) {
+          const int page = a.page_table[(long)b * a.pages_per_seq + t / a.page_size];
+          if (page < 0 || page >= a.num_pages)
+            set_flag(a.status, MEDUSA_FLAG_PAGE_RANGE);
+          else
+            slot = (long)page * a.page_size + t % a.page_size;
+        } else {
+          slot = (long)b * a.capacity + t;
+        }
+      }
+      s_dst[l] = slot * row;
+      s_src[l] = ((long)b * a.n1 + (node < 0 ? 0 : node)) * row;
+      kept += slot >= 0;
+    }
+    (void)kept;
     s_len = L;
     s_n = n;
   }
   __syncthreads();
-  const int L = s_len, n = s_n;
-  const int row = a.Hkv * a.dh;
-  T* kc = reinterpret_cast<T*>(a.kc);
-  T* vc = reinterpret_cast<T*>(a.vc);
-  const T* tk = reinterpret_cast<const T*>(a.tk);
-  const T* tv = reinterpret_cast<const T*>(a.tv);
-  for (int l = 0; l < n; ++l) {
-    const int node = a.path_nodes[(long)b * (a.K + 1) + l];
-    if (node < 0 || node >= a.n1) continue;
-    const int t = L + l;
-    long slot;
-    if (a.page_table) {
-      const int page = a.page_table[(long)b * a.pages_per_seq + t / a.page_size];
-      if (page < 0 || page >= a.num_pages) {
-        if (threadIdx.x == 0) set_flag(a.status, MEDUSA_FLAG_PAGE_RANGE);
-        continue;
-      }
-      slot = (long)page * a.page_size + t % a.page_size;
-    } else {
-      slot = (long)b * a.capacity + t;
-    }
-    const long src = ((long)b * a.n1 + node) * row, dst = slot * row;
-    for (int e = threadIdx.x; e < row; e += blockDim.x) {
-      kc[dst + e] = tk[src + e];
-      vc[dst + e] = tv[src + e];
-    }
+  const int n = s_n;
+  const int per = (int)(row * sizeof(T) / 16);         // 16-byte pieces per token row
+  uint4* kc = reinterpret_cast<uint4*>(a.kc);
+  uint4* vc = reinterpret_cast<uint4*>(a.vc);
+  const uint4* tk = reinterpret_cast<const uint4*>(a.tk);
+  const uint4* tv = reinterpret_cast<const uint4*>(a.tv);
+  constexpr int EPV = 16 / sizeof(T);                   // elements per piece
+  for (int e = threadIdx.x; e < n * per; e += blockDim.x) {
+    const int l = e / per, c = e - l * per;
+    if (s_dst[l] < 0) continue;
+    const long d = s_dst[l] / EPV + c, s = s_src[l] / EPV + c;
+    const uint4 k = tk[s], v = tv[s];
+    kc[d] = k;
+    vc[d] = v;
   }
   __syncthreads();
-  if (threadIdx.x == 0) a.len_out[b] = L + n;
+  if (threadIdx.x == 0) a.len_out[b] = s_len + n;
 }
 
 cudaError_t launch_kv_compact(const CompactArgs& a, cudaStream_t st) {

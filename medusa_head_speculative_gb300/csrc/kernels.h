@@ -84,9 +84,10 @@ struct TreeArgs {
 };
 cudaError_t launch_tree_build(const TreeArgs& a, cudaStream_t st);
 
-// qkv [M][(Hq+2Hkv)*dh] fp32 -> q [M][Hq][dh] fp32 (RoPE), tree k (RoPE) / v in dtype.
+// qkv [M][(Hq+2Hkv)*dh] fp32 -> q [M][Hq][dh] fp32 (RoPE; also as bf16 into qb when
+// non-null), tree k (RoPE) / v in dtype.
 cudaError_t launch_rope_split(const float* qkv, const int32_t* pos, int M, int Hq, int Hkv, int dh,
-                              float base, int dtype, float* q, void* tk, void* tv,
+                              float base, int dtype, float* q, __nv_bfloat16* qb, void* tk, void* tv,
                               cudaStream_t st);
 
 // ---- attention
@@ -107,6 +108,12 @@ struct AttnArgs {
 };
 cudaError_t launch_tree_attention(const AttnArgs& a, int dtype, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st);
+// Tensor-core tree attention (bf16, dh 64/128, G | 128, page size 8..64 dividing 64):
+// rows_per_block must be 128 and chunk a multiple of 64.  q_bf16: [B*n1][Hq][dh].
+bool tree_attention_tc_supported(int dtype, int dh, int G, int page_size);
+cudaError_t launch_tree_attention_tc(const AttnArgs& a, const void* q_bf16, cudaStream_t st);
+// fp32 -> bf16 (round to nearest) of n elements.
+cudaError_t launch_to_bf16(const float* x, __nv_bfloat16* y, long n, cudaStream_t st);
 
 // ---- verify
 struct VerifyArgs {
