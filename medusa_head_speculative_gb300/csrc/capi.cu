@@ -30,13 +30,13 @@ bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15
 enum KernelName {
   KN_H_SPLIT, KN_H_W1, KN_H_VOCAB, KN_TOPK_PARTIAL, KN_TOPK_MERGE, KN_TREE_BUILD, KN_GATHER,
   KN_QKV, KN_ROPE, KN_ATTN, KN_COMBINE, KN_O_SPLIT, KN_OUT, KN_HP_SPLIT, KN_VLOGITS, KN_VSTATS,
-  KN_ACCEPT, KN_COMPACT, KN_QCAST, KN_COUNT
+  KN_ACCEPT, KN_COMPACT, KN_QCAST, KN_SELECT, KN_COMMIT, KN_COUNT
 };
 static const char* const kKernelNames[KN_COUNT] = {
   "split_h", "heads_w1", "heads_vocab", "topk_partial", "topk_merge", "tree_build",
   "embed_gather", "layer_qkv", "rope_split", "tree_attention", "attn_combine", "split_o",
   "layer_out", "split_hprime", "verify_logits", "verify_stats", "verify_accept", "kv_compact",
-  "cast_q"};
+  "cast_q", "heads_select", "verify_commit"};
 
 struct Profiler {
   bool on = false;
@@ -60,6 +60,12 @@ struct medusa_plan {
   std::vector<int32_t> parent, rank, depth;
   int32_t* d_spec = nullptr;        // device [3][n1]: parent, depth, rank
   uint32_t* d_status = nullptr;
+  float* d_rope = nullptr;          // device [rope_rows][dh]: cos | sin of p * theta_i
+  int rope_rows = 0;
+  size_t o_kpart = 0, kpart_bytes = 0;   // split-K partials of the node projections
+  size_t o_cnt = 0;                      // per-sequence completion counters of fused kernels
+  uint32_t* d_mask = nullptr;            // device [n1][8] ancestor bitmask of the tree
+  int32_t* d_retr = nullptr;             // device [n1][K+1] root->leaf paths
   int device = 0, num_sms = 148;
   bool tc_heads = false, tc_nodes = false;   // tensor-core projections
   bool tc_attn = false;                      // tensor-core tree attention
@@ -189,6 +195,10 @@ void layout(medusa_plan* p) {
   p->o_hnext = take(B * D * 4);
   p->o_rnext = take(B * 4);
   p->o_qb = take(p->tc_attn ? M * qd * 2 : 0);
+  const size_t widest = std::max(std::max(D, qd), std::min<size_t>(V, 128 * 148));
+  p->kpart_bytes = p->tc_nodes ? std::min<size_t>(8 * M * widest * 4, (size_t)64 << 20) : 0;
+  p->o_kpart = take(p->kpart_bytes);
+  p->o_cnt = take(2 * B * 4);
   p->ws_bytes = off;
 }
 
@@ -257,11 +267,26 @@ medusa_status heads_impl(const medusa_plan* p, const float* h, const int32_t* ro
     s.out_off = k * V;
   }
   LAUNCH(p, KN_H_VOCAB, st, p->tc_heads ? launch_umma_gemm(b, p->d_status, st) : launch_rowdot(b, d.dtype, st));
-  TopkArgs t{logits, B, K + 1, V, p->topk_splits, p->topk_chunk, at<float>(ws, p->o_cv),
-             at<int32_t>(ws, p->o_ci)};
+  (void)root_in; (void)ttok; (void)tval; (void)root;
+  return MEDUSA_OK;
+}
+
+TopkArgs topk_args(const medusa_plan* p, const float* logits, void* ws) {
+  return TopkArgs{logits, p->d.B, p->K + 1, p->d.V, p->topk_splits, p->topk_chunk,
+                  at<float>(ws, p->o_cv), at<int32_t>(ws, p->o_ci)};
+}
+MergeArgs merge_args(const medusa_plan* p, const int32_t* root_in, int32_t* ttok, float* tval,
+                     int32_t* root, void* ws) {
+  return MergeArgs{at<float>(ws, p->o_cv), at<int32_t>(ws, p->o_ci), p->d.B, p->K, p->d.V,
+                   p->topk_splits, root_in, ttok, tval, root, p->d_status};
+}
+
+// per-head top-16 and root from the head logits (the heads stage's selection)
+medusa_status heads_topk(const medusa_plan* p, const float* logits, const int32_t* root_in,
+                         int32_t* ttok, float* tval, int32_t* root, void* ws, cudaStream_t st) {
+  const TopkArgs t = topk_args(p, logits, ws);
   LAUNCH(p, KN_TOPK_PARTIAL, st, launch_topk_partial(t, st));
-  MergeArgs mg{at<float>(ws, p->o_cv), at<int32_t>(ws, p->o_ci), B, K, V, p->topk_splits,
-               root_in, ttok, tval, root, p->d_status};
+  const MergeArgs mg = merge_args(p, root_in, ttok, tval, root, ws);
   LAUNCH(p, KN_TOPK_MERGE, st, launch_topk_merge(mg, st));
   return MEDUSA_OK;
 }
@@ -297,6 +322,8 @@ medusa_status qkv_impl(const medusa_plan* p, const medusa_weights* w, const int3
   a.out = qkv;
   a.ldo = qd + 2 * kd;
   a.epi = EPI_STORE;
+  a.kpart = p->kpart_bytes ? at<float>(ws, p->o_kpart) : nullptr;
+  a.kpart_bytes = p->kpart_bytes;
   const void* ws_[3] = {w->wq, w->wk, w->wv};
   const int rows[3] = {qd, kd, kd}, offs[3] = {0, qd, qd + kd};
   for (int i = 0; i < 3; ++i) {
@@ -310,7 +337,8 @@ medusa_status qkv_impl(const medusa_plan* p, const medusa_weights* w, const int3
     s.out_off = offs[i];
   }
   LAUNCH(p, KN_QKV, st, p->tc_nodes ? launch_umma_gemm(a, p->d_status, st) : launch_rowdot(a, d.dtype, st));
-  LAUNCH(p, KN_ROPE, st, launch_rope_split(qkv, pos, p->M, d.Hq, d.Hkv, d.dh, d.rope_base, d.dtype, q,
+  LAUNCH(p, KN_ROPE, st, launch_rope_split(qkv, pos, p->M, d.Hq, d.Hkv, d.dh, p->d_rope, p->rope_rows,
+                                           p->d_status, d.dtype, q,
                                            p->tc_attn ? at<bf16>(ws, p->o_qb) : nullptr, tk, tv, st));
   return MEDUSA_OK;
 }
@@ -374,6 +402,8 @@ medusa_status out_impl(const medusa_plan* p, const medusa_weights* w, const floa
   a.ldo = d.d;
   a.epi = EPI_RES_ADD;
   a.ldr = d.d;
+  a.kpart = p->kpart_bytes ? at<float>(ws, p->o_kpart) : nullptr;
+  a.kpart_bytes = p->kpart_bytes;
   if (p->tc_nodes) {
     if (!split_ready)
       LAUNCH(p, KN_O_SPLIT, st, launch_split(o, at<bf16>(ws, p->o_ohi), at<bf16>(ws, p->o_olo), (long)p->M * qd, st));
@@ -418,7 +448,8 @@ VerifyArgs verify_args(const medusa_plan* p, const int32_t* tok, medusa_accept a
 
 medusa_status vlogits_impl(const medusa_plan* p, const medusa_weights* w, const float* hp,
                            bool split_ready, const int32_t* tok, medusa_accept acc, float* logits,
-                           int32_t* am, float* stats, void* ws, cudaStream_t st) {
+                           int32_t* am, float* stats, void* ws, cudaStream_t st,
+                           bool with_stats = true) {
   const medusa_dims& d = p->d;
   MatArgs a{};
   a.nseg = 1;
@@ -427,6 +458,8 @@ medusa_status vlogits_impl(const medusa_plan* p, const medusa_weights* w, const 
   a.out = logits;
   a.ldo = d.V;
   a.epi = EPI_STORE;
+  a.kpart = p->kpart_bytes ? at<float>(ws, p->o_kpart) : nullptr;
+  a.kpart_bytes = p->kpart_bytes;
   if (p->tc_nodes && !split_ready)
     LAUNCH(p, KN_HP_SPLIT, st, launch_split(hp, at<bf16>(ws, p->o_hphi), at<bf16>(ws, p->o_hplo), (long)p->M * d.d, st));
   MatSeg& s = a.seg[0];
@@ -438,6 +471,7 @@ medusa_status vlogits_impl(const medusa_plan* p, const medusa_weights* w, const 
   s.rows = d.V;
   s.out_off = 0;
   LAUNCH(p, KN_VLOGITS, st, p->tc_nodes ? launch_umma_gemm(a, p->d_status, st) : launch_rowdot(a, d.dtype, st));
+  if (!with_stats) return MEDUSA_OK;
   VerifyArgs v = verify_args(p, tok, acc);
   v.logits = logits;
   v.am = am;
@@ -464,8 +498,8 @@ medusa_status accept_impl(const medusa_plan* p, const int32_t* tok, const int32_
   return MEDUSA_OK;
 }
 
-medusa_status compact_impl(const medusa_plan* p, const medusa_kv* kv, const void* tk, const void* tv,
-                           const int32_t* path, const int32_t* n_acc, cudaStream_t st) {
+CompactArgs compact_args(const medusa_plan* p, const medusa_kv* kv, const void* tk, const void* tv,
+                         const int32_t* path, const int32_t* n_acc) {
   const medusa_dims& d = p->d;
   CompactArgs c{};
   c.kc = kv->k;
@@ -488,6 +522,12 @@ medusa_status compact_impl(const medusa_plan* p, const medusa_kv* kv, const void
   c.K = p->K;
   c.dtype = d.dtype;
   c.status = p->d_status;
+  return c;
+}
+
+medusa_status compact_impl(const medusa_plan* p, const medusa_kv* kv, const void* tk, const void* tv,
+                           const int32_t* path, const int32_t* n_acc, cudaStream_t st) {
+  const CompactArgs c = compact_args(p, kv, tk, tv, path, n_acc);
   LAUNCH(p, KN_COMPACT, st, launch_kv_compact(c, st));
   return MEDUSA_OK;
 }
@@ -582,6 +622,17 @@ medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec
   const int gran = p->tc_attn ? 64 : 32;              // keys per chunk of the kernel
   const int max_splits = std::max(1, (dims->capacity + gran - 1) / gran);
   p->nsplit = std::min(want, max_splits);
+  if (p->tc_attn) {
+    // one resident CTA per SM: minimise rounds x (keys per CTA + fixed per-CTA cost)
+    long best = -1;
+    for (int ns = 1; ns <= std::min(max_splits, 64); ++ns) {
+      const long ctas = (long)base * (ns + 1);
+      const long rounds = (ctas + p->num_sms - 1) / p->num_sms;
+      const long keys = ((dims->capacity + ns - 1) / ns + gran - 1) / gran * gran;
+      const long cost = rounds * (keys + 3 * gran);
+      if (best < 0 || cost < best) { best = cost; p->nsplit = ns; }
+    }
+  }
   p->chunk = ((dims->capacity + p->nsplit - 1) / p->nsplit + gran - 1) / gran * gran;
   p->nsplit = (dims->capacity + p->chunk - 1) / p->chunk;
   layout(p);
@@ -592,9 +643,33 @@ medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec
     spec[p->n1 + n] = p->depth[n];
     spec[2 * p->n1 + n] = p->rank[n];
   }
+  // static tree tables: ancestor bitmask and root->leaf paths (leaves in packed order)
+  std::vector<uint32_t> tmask((size_t)p->n1 * kMaskWords, 0u);
+  std::vector<int32_t> tretr((size_t)p->n1 * (p->K + 1), -1);
+  {
+    std::vector<int> haschild(p->n1, 0);
+    for (int n = 1; n < p->n1; ++n) haschild[p->parent[n]] = 1;
+    int leaf = 0;
+    for (int n = 0; n < p->n1; ++n) {
+      for (int j = n; j >= 0; j = p->parent[j]) tmask[(size_t)n * kMaskWords + j / 32] |= 1u << (j % 32);
+      if (haschild[n]) continue;
+      for (int j = n; j >= 0; j = p->parent[j]) tretr[(size_t)leaf * (p->K + 1) + p->depth[j]] = j;
+      ++leaf;
+    }
+  }
+  // rotary table for every position a step can produce: len + depth <= capacity + K
+  p->rope_rows = dims->capacity + p->K + 1;
+  std::vector<float> rope((size_t)p->rope_rows * dims->dh);
+  rope_table(dims->rope_base, dims->dh, p->rope_rows, rope.data());
   if (cudaMalloc(&p->d_spec, spec.size() * sizeof(int32_t)) != cudaSuccess ||
       cudaMalloc(&p->d_status, sizeof(uint32_t)) != cudaSuccess ||
+      cudaMalloc(&p->d_rope, rope.size() * sizeof(float)) != cudaSuccess ||
+      cudaMalloc(&p->d_mask, tmask.size() * sizeof(uint32_t)) != cudaSuccess ||
+      cudaMalloc(&p->d_retr, tretr.size() * sizeof(int32_t)) != cudaSuccess ||
+      cudaMemcpy(p->d_mask, tmask.data(), tmask.size() * sizeof(uint32_t), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(p->d_retr, tretr.data(), tretr.size() * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemcpy(p->d_spec, spec.data(), spec.size() * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(p->d_rope, rope.data(), rope.size() * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemset(p->d_status, 0, sizeof(uint32_t)) != cudaSuccess) {
     medusa_plan_destroy(p);
     return MEDUSA_ERR_CUDA;
@@ -606,6 +681,9 @@ medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec
 void medusa_plan_destroy(medusa_plan* p) {
   if (!p) return;
   p->prof.release();
+  if (p->d_rope) cudaFree(p->d_rope);
+  if (p->d_mask) cudaFree(p->d_mask);
+  if (p->d_retr) cudaFree(p->d_retr);
   if (p->d_spec) cudaFree(p->d_spec);
   if (p->d_status) cudaFree(p->d_status);
   delete p;
@@ -677,7 +755,9 @@ medusa_status medusa_heads(const medusa_plan* p, const float* h, const int32_t* 
   if (s != MEDUSA_OK) return s;
   if ((s = check_ws(p, ws, ws_bytes)) != MEDUSA_OK) return s;
   if (!logits) logits = at<float>(ws, p->o_logits);
-  return heads_impl(p, h, root_in, w, logits, topk_tok, topk_val, root, ws, S(stream));
+  medusa_status s2 = heads_impl(p, h, root_in, w, logits, topk_tok, topk_val, root, ws, S(stream));
+  if (s2 != MEDUSA_OK) return s2;
+  return heads_topk(p, logits, root_in, topk_tok, topk_val, root, ws, S(stream));
 }
 
 medusa_status medusa_tree_build(const medusa_plan* p, const int32_t* topk_tok, const int32_t* root,
@@ -775,20 +855,42 @@ medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* r
   int32_t* am = at<int32_t>(ws, p->o_am);
   float* stats = at<float>(ws, p->o_stats);
   int32_t* path = out->path_nodes ? out->path_nodes : at<int32_t>(ws, p->o_path);
-  if ((s = heads_impl(p, h, root_in, w, at<float>(ws, p->o_logits), ttok, at<float>(ws, p->o_tval),
-                      root, ws, st)) != MEDUSA_OK)
+  float* logits = at<float>(ws, p->o_logits);
+  int32_t* cnt = at<int32_t>(ws, p->o_cnt);
+  (void)mask;
+  (void)retr;
+  MEDUSA_TRY(cudaMemsetAsync(cnt, 0, 2 * sizeof(int32_t) * p->d.B, st));
+  if ((s = heads_impl(p, h, root_in, w, logits, ttok, at<float>(ws, p->o_tval), root, ws, st)) != MEDUSA_OK)
     return s;
-  if ((s = tree_impl(p, ttok, root, kv->len, tok, pos, mask, retr, st)) != MEDUSA_OK) return s;
+  {   // fused: slice top-k, head merge and node tokens / positions
+    const TopkArgs t = topk_args(p, logits, ws);
+    const MergeArgs mg = merge_args(p, root_in, ttok, at<float>(ws, p->o_tval), root, ws);
+    TreeArgs tr{ttok, root, kv->len, p->d.B, p->K, p->d.V, p->n1, p->dparent(), p->ddepth(), p->drank(),
+                tok, pos, nullptr, nullptr, p->d_status};
+    LAUNCH(p, KN_SELECT, st, launch_heads_select(t, mg, tr, cnt, st));
+  }
   if ((s = gather_impl(p, w, tok, ws, st)) != MEDUSA_OK) return s;
   if ((s = qkv_impl(p, w, pos, q, tk, tv, ws, st)) != MEDUSA_OK) return s;
-  if ((s = attn_impl(p, q, kv, tk, tv, mask, o, true, true, ws, st)) != MEDUSA_OK) return s;
+  if ((s = attn_impl(p, q, kv, tk, tv, p->d_mask, o, true, true, ws, st)) != MEDUSA_OK) return s;
   if ((s = out_impl(p, w, o, true, hp, true, ws, st)) != MEDUSA_OK) return s;
-  if ((s = vlogits_impl(p, w, hp, true, tok, acc, at<float>(ws, p->o_vlog), am, stats, ws, st)) != MEDUSA_OK)
-    return s;
-  if ((s = accept_impl(p, tok, am, stats, retr, hp, acc, out->out_tok, out->n_acc, path, out->h_next,
-                       out->root_next, st)) != MEDUSA_OK)
-    return s;
-  return compact_impl(p, kv, tk, tv, path, out->n_acc, st);
+  float* vlog = at<float>(ws, p->o_vlog);
+  if ((s = vlogits_impl(p, w, hp, true, tok, acc, vlog, am, stats, ws, st, false)) != MEDUSA_OK) return s;
+  {   // fused: per-row statistics, acceptance and KV compaction
+    VerifyArgs v = verify_args(p, tok, acc);
+    v.logits = vlog;
+    v.am = am;
+    v.stats = stats;
+    v.retrieve = p->d_retr;
+    v.hprime = hp;
+    v.out_tok = out->out_tok;
+    v.n_acc = out->n_acc;
+    v.path_nodes = path;
+    v.h_next = out->h_next;
+    v.root_next = out->root_next;
+    const CompactArgs c = compact_args(p, kv, tk, tv, path, out->n_acc);
+    LAUNCH(p, KN_COMMIT, st, launch_verify_commit(v, c, cnt + p->d.B, st));
+  }
+  return MEDUSA_OK;
 }
 
 }  // extern "C"

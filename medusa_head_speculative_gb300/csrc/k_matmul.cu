@@ -33,69 +33,78 @@ __device__ __forceinline__ void epilogue_store(const MatArgs& a, const MatSeg& s
 }
 
 // =========================================================== CUDA-core row-dot
-// One CTA = one chunk of rows of one segment; its activations (MT rows x k fp32) are
-// staged in shared memory; each warp streams whole weight rows with 16-byte loads, U
-// loads in flight per lane, and reduces across the warp.
+// One round of CTAs (as many as fit on the GPU at once): CTA c owns a contiguous, balanced
+// range of the rows of all segments taken in order.  For each segment it meets, it stages
+// that segment's activations (MT rows x k fp32) in shared memory; each warp then streams
+// whole weight rows with 16-byte loads, U loads in flight per lane, and reduces across the
+// warp.  A single round avoids the tail of a partly filled last wave.
 template <typename W, int MT>
-__global__ void __launch_bounds__(256) rowdot_kernel(MatArgs a, int rows_per_cta) {
+__global__ void __launch_bounds__(256) rowdot_kernel(MatArgs a, long total_rows) {
   extern __shared__ float xs[];                       // [MT][k]
   constexpr int VEC = 16 / sizeof(W);
   constexpr int U = 8;
-  const MatSeg& s = a.seg[blockIdx.y];
-  const int r0 = blockIdx.x * rows_per_cta;
-  if (r0 >= s.rows) return;
-  const int r1 = min(s.rows, r0 + rows_per_cta);
+  const long g0 = total_rows * blockIdx.x / gridDim.x;
+  const long g1 = total_rows * (blockIdx.x + 1) / gridDim.x;
   const int k = a.k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const W* w = reinterpret_cast<const W*>(s.w);
-
-  for (int m0 = 0; m0 < a.M; m0 += MT) {
-    const int mt = min(MT, a.M - m0);
-    __syncthreads();
-    for (int i = threadIdx.x; i < MT * k; i += blockDim.x) {
-      const int mm = i / k, kk = i - mm * k;
-      xs[i] = mm < mt ? s.x[(long)(m0 + mm) * s.ldx + kk] : 0.f;
-    }
-    __syncthreads();
-    for (int r = r0 + warp; r < r1; r += 8) {
-      const W* wr = w + (long)r * k;
-      float acc[MT];
-#pragma unroll
-      for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-      for (int kb = lane * VEC; kb < k; kb += 32 * VEC * U) {
-        uint4 buf[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int kk = kb + u * 32 * VEC;
-          if (kk < k) buf[u] = ld_stream16(wr + kk);
+  long seg_start = 0;
+  for (int si = 0; si < a.nseg; ++si) {
+    const MatSeg& s = a.seg[si];
+    const long lo = g0 > seg_start ? g0 : seg_start;
+    const long hi = g1 < seg_start + s.rows ? g1 : seg_start + s.rows;
+    if (lo < hi) {
+      const int r0 = (int)(lo - seg_start), r1 = (int)(hi - seg_start);
+      const W* w = reinterpret_cast<const W*>(s.w);
+      for (int m0 = 0; m0 < a.M; m0 += MT) {
+        const int mt = min(MT, a.M - m0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < MT * k; i += blockDim.x) {
+          const int mm = i / k, kk = i - mm * k;
+          xs[i] = mm < mt ? s.x[(long)(m0 + mm) * s.ldx + kk] : 0.f;
         }
+        __syncthreads();
+        for (int r = r0 + warp; r < r1; r += 8) {
+          const W* wr = w + (long)r * k;
+          float acc[MT];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int kk = kb + u * 32 * VEC;
-          if (kk < k) {
-            float f[VEC];
-            unpack16(buf[u], f);
+          for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+          for (int kb = lane * VEC; kb < k; kb += 32 * VEC * U) {
+            uint4 buf[U];
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-              const float4* xv = reinterpret_cast<const float4*>(xs + m * k + kk);
+            for (int u = 0; u < U; ++u) {
+              const int kk = kb + u * 32 * VEC;
+              if (kk < k) buf[u] = ld_stream16(wr + kk);
+            }
 #pragma unroll
-              for (int e4 = 0; e4 < VEC / 4; ++e4) {
-                const float4 x4 = xv[e4];
-                acc[m] = fmaf(f[4 * e4 + 0], x4.x, acc[m]);
-                acc[m] = fmaf(f[4 * e4 + 1], x4.y, acc[m]);
-                acc[m] = fmaf(f[4 * e4 + 2], x4.z, acc[m]);
-                acc[m] = fmaf(f[4 * e4 + 3], x4.w, acc[m]);
+            for (int u = 0; u < U; ++u) {
+              const int kk = kb + u * 32 * VEC;
+              if (kk < k) {
+                float f[VEC];
+                unpack16(buf[u], f);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                  const float4* xv = reinterpret_cast<const float4*>(xs + m * k + kk);
+#pragma unroll
+                  for (int e4 = 0; e4 < VEC / 4; ++e4) {
+                    const float4 x4 = xv[e4];
+                    acc[m] = fmaf(f[4 * e4 + 0], x4.x, acc[m]);
+                    acc[m] = fmaf(f[4 * e4 + 1], x4.y, acc[m]);
+                    acc[m] = fmaf(f[4 * e4 + 2], x4.z, acc[m]);
+                    acc[m] = fmaf(f[4 * e4 + 3], x4.w, acc[m]);
+                  }
+                }
               }
             }
           }
+#pragma unroll
+          for (int m = 0; m < MT; ++m) acc[m] = warp_sum(acc[m]);
+#pragma unroll
+          for (int m = 0; m < MT; ++m)
+            if (lane == m && m < mt) epilogue_store(a, s, m0 + m, r, acc[m]);
         }
       }
-#pragma unroll
-      for (int m = 0; m < MT; ++m) acc[m] = warp_sum(acc[m]);
-#pragma unroll
-      for (int m = 0; m < MT; ++m)
-        if (lane == m && m < mt) epilogue_store(a, s, m0 + m, r, acc[m]);
     }
+    seg_start += s.rows;
   }
 }
 
@@ -108,23 +117,22 @@ static cudaError_t rowdot_go(const MatArgs& a, cudaStream_t st) {
         cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       num_sms = 148;
   }
-  int maxrows = 0;
   long total = 0;
-  for (int i = 0; i < a.nseg; ++i) {
-    maxrows = maxrows > a.seg[i].rows ? maxrows : a.seg[i].rows;
-    total += a.seg[i].rows;
-  }
-  // about 8 CTAs per SM (two rounds of 4 resident) so the row stream balances across SMs
-  int rows_per_cta = (int)(total / ((long)num_sms * 8)) / 8 * 8;
-  rows_per_cta = rows_per_cta < 8 ? 8 : (rows_per_cta > 64 ? 64 : rows_per_cta);
-  dim3 grid((maxrows + rows_per_cta - 1) / rows_per_cta, a.nseg);
+  for (int i = 0; i < a.nseg; ++i) total += a.seg[i].rows;
   const size_t smem = (size_t)MT * a.k * sizeof(float);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(rowdot_kernel<W, MT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  rowdot_kernel<W, MT><<<grid, 256, smem, st>>>(a, rows_per_cta);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rowdot_kernel<W, MT>, 256, smem) !=
+          cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  long grid = (long)per_sm * num_sms;
+  const long by_rows = (total + 7) / 8;               // at least one row per warp
+  grid = grid < by_rows ? grid : by_rows;
+  rowdot_kernel<W, MT><<<(int)grid, 256, smem, st>>>(a, total);
   return cudaGetLastError();
 }
 

@@ -58,10 +58,10 @@ __device__ __forceinline__ void warp_merge(TopList& L, float* ov, int* oi) {
   }
 }
 
-__global__ void __launch_bounds__(256) topk_partial_kernel(TopkArgs a) {
+// The 16 best (logit, token) pairs of one vocab slice of one head, by a 256-thread CTA.
+__device__ void slice_topk(const TopkArgs& a, int sp, int k, int b) {
   __shared__ float sv[8][kTops];
   __shared__ int si[8][kTops];
-  const int sp = blockIdx.x, k = blockIdx.y, b = blockIdx.z;
   const float* z = a.logits + ((long)b * a.nh + k) * a.V;
   const int lo = sp * a.chunk, hi = min(a.V, lo + a.chunk);
   TopList L;
@@ -81,26 +81,30 @@ __global__ void __launch_bounds__(256) topk_partial_kernel(TopkArgs a) {
   }
 }
 
+__global__ void __launch_bounds__(256) topk_partial_kernel(TopkArgs a) {
+  slice_topk(a, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
 cudaError_t launch_topk_partial(const TopkArgs& a, cudaStream_t st) {
   dim3 grid(a.splits, a.nh, a.B);
   topk_partial_kernel<<<grid, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
-// One CTA per sequence.  Warp w merges the vocab slices of heads w, w+8 (head 0 is the
-// LM head, heads 1..K the Medusa heads) into the final top-16 of each head.
-__global__ void __launch_bounds__(256) topk_merge_kernel(MergeArgs a) {
-  __shared__ float tv[MEDUSA_MAX_HEADS + 1][kTops];
-  __shared__ int ti[MEDUSA_MAX_HEADS + 1][kTops];
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Merge of sequence b's vocab slices: warp w merges heads w, w+8 (head 0 is the LM head,
+// heads 1..K the Medusa heads) into their final top-16; writes the root and the heads'
+// lists.  Candidates are read through L2 (they may come from other CTAs of this launch).
+__device__ void merge_heads(const MergeArgs& a, int b, float (*tv)[kTops], int (*ti)[kTops],
+                            int* s_root) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
   const int nh = a.K + 1;
-  for (int k = warp; k < nh; k += 8) {
+  for (int k = warp; k < nh; k += nw) {
     TopList L;
     L.init();
     if (lane < a.splits) {
       const long o = (((long)b * nh + k) * a.splits + lane) * kTops;
 #pragma unroll
-      for (int t = 0; t < kTops; ++t) { L.v[t] = a.cand_val[o + t]; L.i[t] = a.cand_idx[o + t]; }
+      for (int t = 0; t < kTops; ++t) { L.v[t] = __ldcg(a.cand_val + o + t); L.i[t] = __ldcg(a.cand_idx + o + t); }
     }
     warp_merge(L, tv[k], ti[k]);
   }
@@ -109,16 +113,67 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(MergeArgs a) {
     int r = a.root_in ? a.root_in[b] : ti[0][0];
     if (r < 0 || r >= a.V) { set_flag(a.status, MEDUSA_FLAG_TOKEN_RANGE); r = 0; }
     a.root_out[b] = r;
+    *s_root = r;
   }
   for (int e = tid; e < a.K * kTops; e += blockDim.x) {
     const int k = e / kTops, t = e - k * kTops;
     a.topk_tok[(long)b * a.K * kTops + e] = ti[k + 1][t];
     a.topk_val[(long)b * a.K * kTops + e] = tv[k + 1][t];
   }
+  __syncthreads();
+}
+
+// Node tokens and position ids of sequence b, from the merged lists in shared memory.
+__device__ void node_tokens(const TreeArgs& a, int b, const int (*ti)[kTops], int root) {
+  int L = a.len[b];
+  if (L < 0) L = 0;
+  for (int n = threadIdx.x; n < a.n1; n += blockDim.x) {
+    int t = root;
+    if (n > 0) t = ti[a.depth[n]][a.rank[n]];
+    if (t < 0 || t >= a.V) { set_flag(a.status, MEDUSA_FLAG_TOKEN_RANGE); t = 0; }
+    a.tok[(long)b * a.n1 + n] = t;
+    a.pos[(long)b * a.n1 + n] = L + a.depth[n];
+  }
+}
+
+__global__ void __launch_bounds__(256) topk_merge_kernel(MergeArgs a) {
+  __shared__ float tv[MEDUSA_MAX_HEADS + 1][kTops];
+  __shared__ int ti[MEDUSA_MAX_HEADS + 1][kTops];
+  __shared__ int s_root;
+  merge_heads(a, blockIdx.x, tv, ti, &s_root);
 }
 
 cudaError_t launch_topk_merge(const MergeArgs& a, cudaStream_t st) {
   topk_merge_kernel<<<a.B, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// Fused selection for the whole step: every CTA takes the top-16 of one vocab slice of one
+// head; the last CTA to finish for a sequence (atomic counter, nothing waits) merges that
+// sequence's heads, picks the root and writes the node tokens and positions, then resets
+// the counter for the next launch.
+__global__ void __launch_bounds__(256) heads_select_kernel(TopkArgs t, MergeArgs m, TreeArgs tr,
+                                                           int32_t* counter) {
+  __shared__ float tv[MEDUSA_MAX_HEADS + 1][kTops];
+  __shared__ int ti[MEDUSA_MAX_HEADS + 1][kTops];
+  __shared__ int s_root, s_last;
+  const int b = blockIdx.z;
+  slice_topk(t, blockIdx.x, blockIdx.y, b);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(counter + b, 1) == t.splits * t.nh - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  merge_heads(m, b, tv, ti, &s_root);
+  node_tokens(tr, b, ti, s_root);
+  if (threadIdx.x == 0) counter[b] = 0;
+}
+
+cudaError_t launch_heads_select(const TopkArgs& t, const MergeArgs& m, const TreeArgs& tr,
+                                int32_t* counter, cudaStream_t st) {
+  dim3 grid(t.splits, t.nh, t.B);
+  heads_select_kernel<<<grid, 256, 0, st>>>(t, m, tr, counter);
   return cudaGetLastError();
 }
 
@@ -170,25 +225,22 @@ cudaError_t launch_tree_build(const TreeArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// One CTA per node row.  cos/sin of pos * theta_i (theta_i = base^(-2i/dh), computed on
-// the host in double) are evaluated once per row in double precision and applied to every
-// query and key head (rotate-half convention).
-struct RopeFreq {
-  double theta[64];
-};
-
+// One CTA per node row.  cos/sin of pos * theta_i come from the plan's table (computed on
+// the host in double precision, rounded to float) and are applied to every query and key
+// head (rotate-half convention).  Positions past the table are clamped and flagged.
 template <typename T>
-__global__ void rope_split_kernel(const float* qkv, const int32_t* pos, int Hq, int Hkv, int dh,
-                                  RopeFreq f, float* q, bf16* qb, T* tk, T* tv) {
+__global__ void __launch_bounds__(1024) rope_split_kernel(
+    const float* __restrict__ qkv, const int32_t* __restrict__ pos, int Hq, int Hkv, int dh,
+    const float* __restrict__ table, int rows, uint32_t* status, float* __restrict__ q,
+    bf16* __restrict__ qb, T* __restrict__ tk, T* __restrict__ tv) {
   extern __shared__ float cs[];                      // [dh/2] cos, [dh/2] sin
   const int m = blockIdx.x, half = dh / 2;
-  const double p = (double)pos[m];
-  for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    double sn, cn;
-    sincos(p * f.theta[i], &sn, &cn);
-    cs[i] = (float)cn;
-    cs[half + i] = (float)sn;
+  int p = pos[m];
+  if (p < 0 || p >= rows) {
+    if (threadIdx.x == 0) set_flag(status, MEDUSA_FLAG_KV_CAPACITY);
+    p = p < 0 ? 0 : rows - 1;
   }
+  for (int i = threadIdx.x; i < dh; i += blockDim.x) cs[i] = table[(long)p * dh + i];
   __syncthreads();
   const int W = (Hq + 2 * Hkv) * dh;
   const float* row = qkv + (long)m * W;
@@ -217,22 +269,28 @@ __global__ void rope_split_kernel(const float* qkv, const int32_t* pos, int Hq, 
 }
 
 cudaError_t launch_rope_split(const float* qkv, const int32_t* pos, int M, int Hq, int Hkv, int dh,
-                              float base, int dtype, float* q, bf16* qb, void* tk, void* tv,
-                              cudaStream_t st) {
+                              const float* table, int rows, uint32_t* status, int dtype, float* q,
+                              bf16* qb, void* tk, void* tv, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
-  if (dh > 128) return cudaErrorInvalidValue;
-  RopeFreq f;
-  for (int i = 0; i < dh / 2; ++i) f.theta[i] = std::pow((double)base, -2.0 * i / dh);
   const size_t smem = dh * sizeof(float);
   if (dtype == 0)
-    rope_split_kernel<float><<<M, 256, smem, st>>>(qkv, pos, Hq, Hkv, dh, f, q, qb,
+    rope_split_kernel<float><<<M, 1024, smem, st>>>(qkv, pos, Hq, Hkv, dh, table, rows, status, q, qb,
                                                    reinterpret_cast<float*>(tk),
                                                    reinterpret_cast<float*>(tv));
   else
-    rope_split_kernel<bf16><<<M, 256, smem, st>>>(qkv, pos, Hq, Hkv, dh, f, q, qb,
+    rope_split_kernel<bf16><<<M, 1024, smem, st>>>(qkv, pos, Hq, Hkv, dh, table, rows, status, q, qb,
                                                   reinterpret_cast<bf16*>(tk),
                                                   reinterpret_cast<bf16*>(tv));
   return cudaGetLastError();
+}
+
+void rope_table(float base, int dh, int rows, float* out) {
+  for (int p = 0; p < rows; ++p)
+    for (int i = 0; i < dh / 2; ++i) {
+      const double theta = std::pow((double)base, -2.0 * i / dh);
+      out[(long)p * dh + i] = (float)std::cos(p * theta);
+      out[(long)p * dh + dh / 2 + i] = (float)std::sin(p * theta);
+    }
 }
 
 }  // namespace medusa

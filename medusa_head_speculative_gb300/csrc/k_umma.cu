@@ -35,6 +35,8 @@ struct UmmaArgs {
   MatArgs m;
   int nbox;                  // activation rows per CTA = MMA N (multiple of 16, <= 256)
   int stages;
+  int ksplit;                // K ranges (blockIdx.z); > 1 writes raw partials to kpart
+  float* kpart;
   uint32_t tmem_cols;
   uint32_t* status;
 };
@@ -60,7 +62,7 @@ __device__ __forceinline__ void umma_epilogue(const MatArgs& a, const MatSeg& s,
 }
 
 template <bool HAS_LO>
-__global__ void __launch_bounds__(128, 1) umma_gemm_kernel(const __grid_constant__ UmmaArgs g) {
+__global__ void __launch_bounds__(128, 2) umma_gemm_kernel(const __grid_constant__ UmmaArgs g) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[2 * 8 + 1];
   __shared__ uint32_t tmem_slot;
@@ -73,6 +75,8 @@ __global__ void __launch_bounds__(128, 1) umma_gemm_kernel(const __grid_constant
   const int rbase = ((int)blockIdx.y - a.tile_off[si]) * UM_R;
   const int m0 = (int)blockIdx.x * g.nbox;
   const int nk = (a.k + UM_K - 1) / UM_K;
+  const int kt0 = (int)((long)blockIdx.z * nk / g.ksplit);      // this CTA's K range
+  const int nkl = (int)((long)(blockIdx.z + 1) * nk / g.ksplit) - kt0;
   const int S = g.stages;
   const uint32_t A_BYTES = (uint32_t)g.nbox * 128;
   const uint32_t STAGE = UM_W_BYTES + A_BYTES * (HAS_LO ? 2 : 1);
@@ -101,35 +105,35 @@ __global__ void __launch_bounds__(128, 1) umma_gemm_kernel(const __grid_constant
 
   if (warp == 0 && lane == 0) {                         // ---- TMA producer
     const uint64_t pw = policy_evict_first(), pa = policy_evict_last();
-    int kt = 0;
-    for (; kt < nk; ++kt) {
-      const int st = kt % S;
-      if (!mbar_wait(empty(st), ((kt / S) & 1) ^ 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+    int j = 0;
+    for (; j < nkl; ++j) {
+      const int st = j % S, kx = (kt0 + j) * UM_K;
+      if (!mbar_wait(empty(st), ((j / S) & 1) ^ 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
       mbar_expect_tx(full(st), STAGE);
       const uint32_t ws = base + st * STAGE;
-      tma_load_2d(ws, &g.tw[si], kt * UM_K, rbase, full(st), pw);
-      tma_load_2d(ws + UM_W_BYTES, &g.ta[si], kt * UM_K, m0, full(st), pa);
-      if (HAS_LO) tma_load_2d(ws + UM_W_BYTES + A_BYTES, &g.tl[si], kt * UM_K, m0, full(st), pa);
+      tma_load_2d(ws, &g.tw[si], kx, rbase, full(st), pw);
+      tma_load_2d(ws + UM_W_BYTES, &g.ta[si], kx, m0, full(st), pa);
+      if (HAS_LO) tma_load_2d(ws + UM_W_BYTES + A_BYTES, &g.tl[si], kx, m0, full(st), pa);
     }
-    s_issued = kt;
+    s_issued = j;
   } else if (warp == 1 && lane == 0) {                  // ---- MMA issuer
     const uint32_t idesc = idesc_bf16(UM_R, g.nbox);
-    int kt = 0;
-    for (; kt < nk; ++kt) {
-      const int st = kt % S;
-      if (!mbar_wait(full(st), (kt / S) & 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+    int j = 0;
+    for (; j < nkl; ++j) {
+      const int st = j % S;
+      if (!mbar_wait(full(st), (j / S) & 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
       tc_fence_after();
       const uint32_t ws = base + st * STAGE;
       const uint64_t ad = sw128_desc(ws), bd = sw128_desc(ws + UM_W_BYTES);
       const uint64_t ld = sw128_desc(ws + UM_W_BYTES + A_BYTES);
 #pragma unroll
       for (int ks = 0; ks < UM_K / 16; ++ks) {          // +32 bytes along K per step
-        umma_bf16(tmem, ad + 2 * ks, bd + 2 * ks, idesc, (kt | ks) != 0);
+        umma_bf16(tmem, ad + 2 * ks, bd + 2 * ks, idesc, (j | ks) != 0);
         if (HAS_LO) umma_bf16(tmem, ad + 2 * ks, ld + 2 * ks, idesc, 1);
       }
       umma_commit(empty(st));                           // frees the stage when read
     }
-    s_consumed = kt;
+    s_consumed = j;
     umma_commit(accb);                                  // accumulator complete
   }
   __syncwarp();
@@ -137,7 +141,7 @@ __global__ void __launch_bounds__(128, 1) umma_gemm_kernel(const __grid_constant
   const bool acc_ok = mbar_wait(accb, 0, TC_TIMEOUT_NS);
   tc_fence_after();
   __syncwarp();
-  if (acc_ok) {
+  if (acc_ok && nkl > 0) {
     const int r = rbase + warp * 32 + lane;
     for (int c0 = 0; c0 < g.nbox; c0 += 16) {
       float v[16];
@@ -146,7 +150,11 @@ __global__ void __launch_bounds__(128, 1) umma_gemm_kernel(const __grid_constant
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int m = m0 + c0 + j;
-          if (m < a.M) umma_epilogue(a, s, m, r, v[j]);
+          if (m >= a.M) continue;
+          if (g.ksplit > 1)                             // raw partial sum of this K range
+            g.kpart[((long)blockIdx.z * a.M + m) * a.ldo + s.out_off + r] = v[j];
+          else
+            umma_epilogue(a, s, m, r, v[j]);
         }
       }
     }
@@ -155,11 +163,24 @@ __global__ void __launch_bounds__(128, 1) umma_gemm_kernel(const __grid_constant
   tc_fence_before();
   __syncthreads();
   if (tid == 0) {                                       // drain copies issued but not consumed
-    for (int kt = s_consumed; kt < s_issued; ++kt)
-      mbar_wait(full(kt % S), (kt / S) & 1, TC_TIMEOUT_NS / 16);
+    for (int j = s_consumed; j < s_issued; ++j)
+      mbar_wait(full(j % S), (j / S) & 1, TC_TIMEOUT_NS / 16);
   }
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, g.tmem_cols);
+}
+
+// Sum of the K-range partials over output columns [0, cols), then the epilogue
+// (single-segment launches) or a plain store (multi-segment EPI_STORE launches).
+__global__ void umma_splitk_reduce_kernel(const MatArgs a, const float* kpart, int ksplit, int cols) {
+  const long n = (long)a.M * cols;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+    const int m = (int)(i / cols), c = (int)(i - (long)m * cols);
+    float acc = 0.f;
+    for (int z = 0; z < ksplit; ++z) acc += kpart[((long)z * a.M + m) * a.ldo + c];
+    if (a.nseg == 1) umma_epilogue(a, a.seg[0], m, c, acc);
+    else a.out[(long)m * a.ldo + c] = acc;
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -194,7 +215,14 @@ static bool make_map(CUtensorMap* map, const void* ptr, long cols, long rows, lo
 cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st) {
   static UmmaArgs g;                      // ~4.5 KB: keep it off the host stack
   static std::mutex mu;
+  static int num_sms = 0;
   std::lock_guard<std::mutex> lock(mu);
+  if (!num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      num_sms = 148;
+  }
   std::memset(&g, 0, sizeof(g));
   g.m = m;
   MatArgs& a = g.m;
@@ -210,11 +238,28 @@ cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st
   uint32_t cols = 32;
   while (cols < (uint32_t)nbox) cols <<= 1;
   g.tmem_cols = cols;
+  // ring depth: two CTAs per SM when that leaves >= 3 stages, else one CTA with a deep ring
   const uint32_t stage = UM_W_BYTES + (uint32_t)nbox * 128 * (has_lo ? 2 : 1);
-  int stages = (int)((200u * 1024u) / stage);
+  int stages = (int)((110u * 1024u) / stage);
+  if (stages < 3) stages = (int)((200u * 1024u) / stage);
   g.stages = stages > 8 ? 8 : stages;
   if (g.stages < 2) return cudaErrorInvalidValue;
   g.status = status;
+  // split K when the tiles alone cannot cover the SMs (single-segment launches)
+  const int nk = (a.k + UM_K - 1) / UM_K;
+  const int mchunks = (a.M + nbox - 1) / nbox;
+  const long ctas = (long)mchunks * a.tile_off[a.nseg];
+  int ksplit = 1;
+  const bool splittable = a.nseg == 1 || (a.epi == EPI_STORE && !a.out_hi);
+  if (splittable && a.kpart && ctas < num_sms) {
+    ksplit = (int)(2L * num_sms / ctas);
+    ksplit = ksplit > 8 ? 8 : ksplit;
+    ksplit = ksplit > nk / 4 ? nk / 4 : ksplit;
+    while (ksplit > 1 && (size_t)ksplit * a.M * a.ldo * sizeof(float) > a.kpart_bytes) --ksplit;
+    ksplit = ksplit < 1 ? 1 : ksplit;
+  }
+  g.ksplit = ksplit;
+  g.kpart = a.kpart;
   for (int i = 0; i < a.nseg; ++i) {
     const MatSeg& s = a.seg[i];
     if (!make_map(&g.tw[i], s.w, a.k, s.rows, a.k, UM_R)) return cudaErrorInvalidValue;
@@ -225,8 +270,14 @@ cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st
   auto kern = has_lo ? umma_gemm_kernel<true> : umma_gemm_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.M + nbox - 1) / nbox, a.tile_off[a.nseg]);
+  dim3 grid(mchunks, a.tile_off[a.nseg], ksplit);
   kern<<<grid, 128, smem, st>>>(g);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || ksplit == 1) return e;
+  const int ncols = a.nseg == 1 ? a.seg[0].rows : (int)a.ldo;
+  const long n = (long)a.M * ncols;
+  const long blocks = (n + 255) / 256;
+  umma_splitk_reduce_kernel<<<(int)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(a, a.kpart, ksplit, ncols);
   return cudaGetLastError();
 }
 

@@ -64,11 +64,10 @@ __device__ __forceinline__ void stat_add(SoftStat& s, float y) {
   s.U += (y - s.m) * e;
 }
 
-// One 1024-thread CTA per node row (b, n).
-__global__ void __launch_bounds__(1024) verify_stats_kernel(VerifyArgs a) {
+// Statistics of one node row (b, n) by one CTA (1024 threads).
+__device__ void row_stats(const VerifyArgs& a, int row) {
   __shared__ float sv[32], sS[32], sU[32];
   __shared__ int si[32];
-  const int row = blockIdx.x;
   const int b = row / a.n1, n = row - b * a.n1;
   const float* z = a.logits + (long)row * a.V;
   const bool typ = a.typical != 0;
@@ -140,18 +139,21 @@ __global__ void __launch_bounds__(1024) verify_stats_kernel(VerifyArgs a) {
   for (int q = 0; q < 4; ++q) a.stats[(long)row * 4 + q] = out[q];
 }
 
+__global__ void __launch_bounds__(1024) verify_stats_kernel(VerifyArgs a) { row_stats(a, blockIdx.x); }
+
 cudaError_t launch_verify_stats(const VerifyArgs& a, cudaStream_t st) {
   verify_stats_kernel<<<a.B * a.n1, 1024, 0, st>>>(a);
   return cudaGetLastError();
 }
 
-// One CTA per sequence; thread c decides candidate c, thread p walks path p.
-__global__ void __launch_bounds__(256) verify_accept_kernel(VerifyArgs a) {
+// Acceptance of sequence b by one CTA; thread c decides candidate c, thread p walks path
+// p.  Statistics are read through L2 (other CTAs of the same launch may have written them).
+__device__ void accept_seq(const VerifyArgs& a, int b) {
   __shared__ int acc[MEDUSA_MAX_NODES];
   __shared__ float sv[32];
   __shared__ int si[32];
   __shared__ int s_last;
-  const int b = blockIdx.x, tid = threadIdx.x;
+  const int tid = threadIdx.x;
   const long rb = (long)b * a.n1;
   const float log_eps = logf(a.eps), log_delta = logf(a.delta);
   for (int c = tid; c < a.n1; c += blockDim.x) {
@@ -160,10 +162,10 @@ __global__ void __launch_bounds__(256) verify_accept_kernel(VerifyArgs a) {
       const int p = a.parent[c];
       if (a.typical) {
         const float* sp = a.stats + (rb + p) * 4;
-        const float lp = a.stats[(rb + c) * 4 + 3] - sp[0] - sp[1];   // log p_parent(tok_c)
-        ok = lp > fminf(log_eps, log_delta - sp[2]);
+        const float lp = __ldcg(a.stats + (rb + c) * 4 + 3) - __ldcg(sp) - __ldcg(sp + 1);
+        ok = lp > fminf(log_eps, log_delta - __ldcg(sp + 2));         // log p_parent(tok_c)
       } else {
-        ok = a.tok[rb + c] == a.am[rb + p];
+        ok = a.tok[rb + c] == __ldcg(a.am + rb + p);
       }
     }
     acc[c] = ok;
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(256) verify_accept_kernel(VerifyArgs a) {
     a.out_tok[(long)b * W + l] = node >= 0 ? a.tok[rb + node] : -1;
     if (l == m) {
       a.n_acc[b] = m + 1;
-      a.root_next[b] = a.am[rb + node];
+      a.root_next[b] = __ldcg(a.am + rb + node);
       s_last = node;
     }
   }
@@ -198,7 +200,10 @@ __global__ void __launch_bounds__(256) verify_accept_kernel(VerifyArgs a) {
   const float4* src = reinterpret_cast<const float4*>(a.hprime + (rb + s_last) * a.d);
   float4* dst = reinterpret_cast<float4*>(a.h_next + (long)b * a.d);
   for (int j = tid; j < a.d / 4; j += blockDim.x) dst[j] = src[j];
+  __syncthreads();
 }
+
+__global__ void __launch_bounds__(256) verify_accept_kernel(VerifyArgs a) { accept_seq(a, blockIdx.x); }
 
 cudaError_t launch_verify_accept(const VerifyArgs& a, cudaStream_t st) {
   verify_accept_kernel<<<a.B, 256, 0, st>>>(a);
@@ -208,10 +213,9 @@ cudaError_t launch_verify_accept(const VerifyArgs& a, cudaStream_t st) {
 // One CTA per sequence: slot len + l <- tree node path_nodes[l], l < n_acc, in 16-byte
 // pieces spread over all threads.
 template <typename T>
-__global__ void __launch_bounds__(256) kv_compact_kernel(CompactArgs a) {
+__device__ void compact_seq(const CompactArgs& a, int b) {
   __shared__ int s_len, s_n;
   __shared__ long s_dst[MEDUSA_MAX_HEADS + 1], s_src[MEDUSA_MAX_HEADS + 1];
-  const int b = blockIdx.x;
   const long row = (long)a.Hkv * a.dh;                // elements per cached token
   if (threadIdx.x == 0) {
     int L = a.len[b];
@@ -222,7 +226,6 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(CompactArgs a) {
       set_flag(a.status, MEDUSA_FLAG_KV_CAPACITY);
       n = a.capacity > L ? a.capacity - L : 0;
     }
-    int kept = 0;
     for (int l = 0; l < n; ++l) {
       const int node = a.path_nodes[(long)b * (a.K + 1) + l];
       const int t = L + l;
@@ -240,9 +243,7 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(CompactArgs a) {
       }
       s_dst[l] = slot * row;
       s_src[l] = ((long)b * a.n1 + (node < 0 ? 0 : node)) * row;
-      kept += slot >= 0;
     }
-    (void)kept;
     s_len = L;
     s_n = n;
   }
@@ -264,6 +265,37 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(CompactArgs a) {
   }
   __syncthreads();
   if (threadIdx.x == 0) a.len_out[b] = s_len + n;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) kv_compact_kernel(CompactArgs a) { compact_seq<T>(a, blockIdx.x); }
+
+// Fused verification for the whole step: one CTA per node row computes its statistics; the
+// last CTA to finish for a sequence (atomic counter, nothing waits) runs that sequence's
+// acceptance and KV compaction, then resets the counter.
+template <typename T>
+__global__ void __launch_bounds__(1024) verify_commit_kernel(VerifyArgs v, CompactArgs c, int32_t* counter) {
+  __shared__ int s_last;
+  const int row = blockIdx.x, b = row / v.n1;
+  row_stats(v, row);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(counter + b, 1) == v.n1 - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  accept_seq(v, b);
+  compact_seq<T>(c, b);
+  if (threadIdx.x == 0) counter[b] = 0;
+}
+
+cudaError_t launch_verify_commit(const VerifyArgs& v, const CompactArgs& c, int32_t* counter,
+                                 cudaStream_t st) {
+  if (c.dtype == 0)
+    verify_commit_kernel<float><<<v.B * v.n1, 1024, 0, st>>>(v, c, counter);
+  else
+    verify_commit_kernel<bf16><<<v.B * v.n1, 1024, 0, st>>>(v, c, counter);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_kv_compact(const CompactArgs& a, cudaStream_t st) {

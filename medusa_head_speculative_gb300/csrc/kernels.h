@@ -41,6 +41,8 @@ struct MatArgs {
   long ldr;
   __nv_bfloat16* out_hi;         // optional bf16 hi/lo copies of out (same indexing)
   __nv_bfloat16* out_lo;
+  float* kpart;                  // tensor-core path: scratch for split-K partials, or null
+  size_t kpart_bytes;
 };
 
 // CUDA-core row-dot projection: dtype 0 = f32 weights, 1 = bf16.
@@ -83,12 +85,19 @@ struct TreeArgs {
   uint32_t* status;
 };
 cudaError_t launch_tree_build(const TreeArgs& a, cudaStream_t st);
+// Fused slice top-k + head merge + node tokens/positions (tr.mask/retrieve unused).
+// counter: [B] zeros on entry; left at zero on exit.
+cudaError_t launch_heads_select(const TopkArgs& t, const MergeArgs& m, const TreeArgs& tr,
+                                int32_t* counter, cudaStream_t st);
 
 // qkv [M][(Hq+2Hkv)*dh] fp32 -> q [M][Hq][dh] fp32 (RoPE; also as bf16 into qb when
 // non-null), tree k (RoPE) / v in dtype.
+// table: [rows][dh] = cos(p theta_i) for i < dh/2, then sin(p theta_i); built by rope_table.
 cudaError_t launch_rope_split(const float* qkv, const int32_t* pos, int M, int Hq, int Hkv, int dh,
-                              float base, int dtype, float* q, __nv_bfloat16* qb, void* tk, void* tv,
-                              cudaStream_t st);
+                              const float* table, int rows, uint32_t* status, int dtype, float* q,
+                              __nv_bfloat16* qb, void* tk, void* tv, cudaStream_t st);
+// Host: cos/sin of p * base^(-2i/dh) for p < rows, computed in double.
+void rope_table(float base, int dh, int rows, float* out);
 
 // ---- attention
 struct AttnArgs {
@@ -139,6 +148,9 @@ struct CompactArgs {
   uint32_t* status;
 };
 cudaError_t launch_kv_compact(const CompactArgs& a, cudaStream_t st);
+// Fused per-row statistics + acceptance + KV compaction.  counter: [B] zeros on entry.
+cudaError_t launch_verify_commit(const VerifyArgs& v, const CompactArgs& c, int32_t* counter,
+                                 cudaStream_t st);
 
 // Plan fields used by the workspace-free heads entry point (defined in capi.cu).
 struct HeadsPlanView {
