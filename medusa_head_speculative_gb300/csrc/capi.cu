@@ -57,13 +57,15 @@ struct medusa_plan {
   medusa_dims d;
   int K, N, n1, P, smax;
   int s[MEDUSA_MAX_HEADS];
+  int need[MEDUSA_MAX_HEADS + 1];   // ranks the tree uses per head (LM head: the root only)
   std::vector<int32_t> parent, rank, depth;
   int32_t* d_spec = nullptr;        // device [3][n1]: parent, depth, rank
   uint32_t* d_status = nullptr;
   float* d_rope = nullptr;          // device [rope_rows][dh]: cos | sin of p * theta_i
   int rope_rows = 0;
   size_t o_kpart = 0, kpart_bytes = 0;   // split-K partials of the node projections
-  size_t o_cnt = 0;                      // per-sequence completion counters of fused kernels
+  size_t o_cnt = 0;                      // completion counters of the fused kernels
+  size_t o_vparts = 0;                   // per-row partial statistics of the fused commit
   uint32_t* d_mask = nullptr;            // device [n1][8] ancestor bitmask of the tree
   int32_t* d_retr = nullptr;             // device [n1][K+1] root->leaf paths
   int device = 0, num_sms = 148;
@@ -198,7 +200,9 @@ void layout(medusa_plan* p) {
   const size_t widest = std::max(std::max(D, qd), std::min<size_t>(V, 128 * 148));
   p->kpart_bytes = p->tc_nodes ? std::min<size_t>(8 * M * widest * 4, (size_t)64 << 20) : 0;
   p->o_kpart = take(p->kpart_bytes);
-  p->o_cnt = take(2 * B * 4);
+  // counters: [0,B) selection, [B,2B) commit per sequence, then one per node row
+  p->o_cnt = take((2 * B + M) * 4);
+  p->o_vparts = take(M * 4 * 6 * 4);
   p->ws_bytes = off;
 }
 
@@ -637,6 +641,8 @@ medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec
   p->nsplit = (dims->capacity + p->chunk - 1) / p->chunk;
   layout(p);
 
+  for (int k = 0; k <= MEDUSA_MAX_HEADS; ++k) p->need[k] = 1;
+  for (int n = 1; n < p->n1; ++n) p->need[p->depth[n]] = std::max(p->need[p->depth[n]], p->rank[n] + 1);
   std::vector<int32_t> spec(3 * p->n1);
   for (int n = 0; n < p->n1; ++n) {
     spec[n] = p->parent[n];
@@ -859,12 +865,13 @@ medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* r
   int32_t* cnt = at<int32_t>(ws, p->o_cnt);
   (void)mask;
   (void)retr;
-  MEDUSA_TRY(cudaMemsetAsync(cnt, 0, 2 * sizeof(int32_t) * p->d.B, st));
+  MEDUSA_TRY(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * (2 * p->d.B + p->M), st));
   if ((s = heads_impl(p, h, root_in, w, logits, ttok, at<float>(ws, p->o_tval), root, ws, st)) != MEDUSA_OK)
     return s;
   {   // fused: slice top-k, head merge and node tokens / positions
-    const TopkArgs t = topk_args(p, logits, ws);
-    const MergeArgs mg = merge_args(p, root_in, ttok, at<float>(ws, p->o_tval), root, ws);
+    TopkArgs t = topk_args(p, logits, ws);
+    MergeArgs mg = merge_args(p, root_in, ttok, at<float>(ws, p->o_tval), root, ws);
+    for (int k = 0; k <= p->K; ++k) t.rounds[k] = mg.rounds[k] = p->need[k];
     TreeArgs tr{ttok, root, kv->len, p->d.B, p->K, p->d.V, p->n1, p->dparent(), p->ddepth(), p->drank(),
                 tok, pos, nullptr, nullptr, p->d_status};
     LAUNCH(p, KN_SELECT, st, launch_heads_select(t, mg, tr, cnt, st));
@@ -888,7 +895,9 @@ medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* r
     v.h_next = out->h_next;
     v.root_next = out->root_next;
     const CompactArgs c = compact_args(p, kv, tk, tv, path, out->n_acc);
-    LAUNCH(p, KN_COMMIT, st, launch_verify_commit(v, c, cnt + p->d.B, st));
+    LAUNCH(p, KN_COMMIT, st,
+           launch_verify_commit(v, c, cnt + 2 * p->d.B, cnt + p->d.B,
+                                at<float>(ws, p->o_vparts), st));
   }
   return MEDUSA_OK;
 }

@@ -45,16 +45,35 @@ struct TopList {
   }
 };
 
-// Merge the 32 lanes' sorted lists: kTops rounds of a warp argmax over the list heads;
+// Order-preserving 32-bit key of a float (larger float -> larger key; -0 as +0; NaN lowest).
+__device__ __forceinline__ uint32_t float_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0u;
+  if (v != v) return 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Merge the 32 lanes' sorted lists: kTops rounds of a warp reduction over the list heads
+// (max of the value keys, then min of the token ids among the lanes holding that value);
 // the winning lane pops.  Token ids are distinct across lanes (sentinels aside).
-__device__ __forceinline__ void warp_merge(TopList& L, float* ov, int* oi) {
+__device__ __forceinline__ void warp_merge(TopList& L, float* ov, int* oi, int rounds = kTops) {
   const int lane = threadIdx.x & 31;
-  for (int t = 0; t < kTops; ++t) {
-    float v = L.v[0];
-    int i = L.i[0];
-    warp_argmax(v, i);
-    if (L.i[0] == i && L.v[0] == v) L.pop();
-    if (lane == 0) { ov[t] = v; oi[t] = i; }
+  rounds = rounds < 1 || rounds > kTops ? kTops : rounds;
+  if (lane == 0)                                   // ranks past `rounds` are not needed
+    for (int t = rounds; t < kTops; ++t) { ov[t] = NEG_INF; oi[t] = NO_IDX; }
+#pragma unroll 1
+  for (int t = 0; t < rounds; ++t) {
+    const uint32_t key = float_key(L.v[0]);
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+    const uint32_t imin = __reduce_min_sync(0xffffffffu, key == kmax ? (uint32_t)L.i[0] : 0x7fffffffu);
+    if (key == kmax && (uint32_t)L.i[0] == imin) L.pop();
+    if (lane == 0) {
+      ov[t] = kmax != 0u ? key_float(kmax) : NEG_INF;
+      oi[t] = (int)imin;
+    }
   }
 }
 
@@ -68,7 +87,7 @@ __device__ void slice_topk(const TopkArgs& a, int sp, int k, int b) {
   L.init();
   for (int v = lo + threadIdx.x; v < hi; v += blockDim.x) L.insert(z[v], v);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  warp_merge(L, sv[warp], si[warp]);
+  warp_merge(L, sv[warp], si[warp], a.rounds[k]);
   __syncthreads();
   if (warp == 0) {
     L.init();
@@ -77,7 +96,7 @@ __device__ void slice_topk(const TopkArgs& a, int sp, int k, int b) {
       for (int t = 0; t < kTops; ++t) { L.v[t] = sv[lane][t]; L.i[t] = si[lane][t]; }
     }
     const long o = (((long)b * a.nh + k) * a.splits + sp) * kTops;
-    warp_merge(L, a.cand_val + o, a.cand_idx + o);
+    warp_merge(L, a.cand_val + o, a.cand_idx + o, a.rounds[k]);
   }
 }
 
@@ -106,7 +125,7 @@ __device__ void merge_heads(const MergeArgs& a, int b, float (*tv)[kTops], int (
 #pragma unroll
       for (int t = 0; t < kTops; ++t) { L.v[t] = __ldcg(a.cand_val + o + t); L.i[t] = __ldcg(a.cand_idx + o + t); }
     }
-    warp_merge(L, tv[k], ti[k]);
+    warp_merge(L, tv[k], ti[k], a.rounds[k]);
   }
   __syncthreads();
   if (tid == 0) {

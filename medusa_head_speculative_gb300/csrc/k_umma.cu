@@ -170,16 +170,33 @@ __global__ void __launch_bounds__(128, 2) umma_gemm_kernel(const __grid_constant
   if (warp == 1) tmem_dealloc(tmem, g.tmem_cols);
 }
 
-// Sum of the K-range partials over output columns [0, cols), then the epilogue
-// (single-segment launches) or a plain store (multi-segment EPI_STORE launches).
-__global__ void umma_splitk_reduce_kernel(const MatArgs a, const float* kpart, int ksplit, int cols) {
-  const long n = (long)a.M * cols;
+// Sum of the K-range partials for 4 consecutive output columns per thread (all loads issued
+// before the epilogue's stores), then the epilogue (single-segment launches) or a plain
+// store (multi-segment EPI_STORE launches).  cols % 4 == 0.
+__global__ void splitk_reduce_kernel(const MatArgs a, const float* __restrict__ kpart, int ksplit, int cols) {
+  constexpr int ZMAX = 8;
+  const int c4 = cols / 4;
+  const long n = (long)a.M * c4;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
-    const int m = (int)(i / cols), c = (int)(i - (long)m * cols);
-    float acc = 0.f;
-    for (int z = 0; z < ksplit; ++z) acc += kpart[((long)z * a.M + m) * a.ldo + c];
-    if (a.nseg == 1) umma_epilogue(a, a.seg[0], m, c, acc);
-    else a.out[(long)m * a.ldo + c] = acc;
+    const int m = (int)(i / c4), c = (int)(i - (long)m * c4) * 4;
+    float4 v[ZMAX];
+#pragma unroll
+    for (int z = 0; z < ZMAX; ++z)
+      v[z] = z < ksplit ? __ldcg(reinterpret_cast<const float4*>(kpart + ((long)z * a.M + m) * a.ldo + c))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int z = 0; z < ZMAX; ++z) {
+      acc[0] += v[z].x;
+      acc[1] += v[z].y;
+      acc[2] += v[z].z;
+      acc[3] += v[z].w;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (a.nseg == 1) umma_epilogue(a, a.seg[0], m, c + e, acc[e]);
+      else a.out[(long)m * a.ldo + c + e] = acc[e];
+    }
   }
 }
 
@@ -251,7 +268,7 @@ cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st
   const long ctas = (long)mchunks * a.tile_off[a.nseg];
   int ksplit = 1;
   const bool splittable = a.nseg == 1 || (a.epi == EPI_STORE && !a.out_hi);
-  if (splittable && a.kpart && ctas < num_sms) {
+  if (splittable && a.kpart && ctas < num_sms && (a.nseg == 1 ? a.seg[0].rows : a.ldo) % 4 == 0) {
     ksplit = (int)(2L * num_sms / ctas);
     ksplit = ksplit > 8 ? 8 : ksplit;
     ksplit = ksplit > nk / 4 ? nk / 4 : ksplit;
@@ -275,9 +292,9 @@ cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st
   e = cudaGetLastError();
   if (e != cudaSuccess || ksplit == 1) return e;
   const int ncols = a.nseg == 1 ? a.seg[0].rows : (int)a.ldo;
-  const long n = (long)a.M * ncols;
-  const long blocks = (n + 255) / 256;
-  umma_splitk_reduce_kernel<<<(int)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(a, a.kpart, ksplit, ncols);
+  const long n4 = (long)a.M * (ncols / 4);
+  const long blocks = (n4 + 255) / 256;
+  splitk_reduce_kernel<<<(int)(blocks < 8192 ? blocks : 8192), 256, 0, st>>>(a, a.kpart, ksplit, ncols);
   return cudaGetLastError();
 }
 

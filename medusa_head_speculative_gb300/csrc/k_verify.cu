@@ -64,79 +64,93 @@ __device__ __forceinline__ void stat_add(SoftStat& s, float y) {
   s.U += (y - s.m) * e;
 }
 
-// Statistics of one node row (b, n) by one CTA (1024 threads).
-__device__ void row_stats(const VerifyArgs& a, int row) {
+// Partial statistics of logits [v0, v1) of one node row: max/argmax and, for typical
+// acceptance, the running-max softmax sums of z/T.  Result valid in thread 0.
+struct RowPart {
+  float bv;
+  int bi;
+  SoftStat st;
+  bool nonfinite;
+};
+__device__ RowPart row_part(const VerifyArgs& a, int row, int v0, int v1) {
   __shared__ float sv[32], sS[32], sU[32];
   __shared__ int si[32];
-  const int b = row / a.n1, n = row - b * a.n1;
   const float* z = a.logits + (long)row * a.V;
   const bool typ = a.typical != 0;
   const float T = a.temperature;
-  float bv = -INFINITY;
-  int bi = 0x7fffffff;
-  bool nonfinite = false;
-  SoftStat st{-INFINITY, 0.f, 0.f};
+  RowPart r{-INFINITY, 0x7fffffff, SoftStat{-INFINITY, 0.f, 0.f}, false};
   auto take = [&](float x, int v) {
-    nonfinite |= !isfinite(x);
-    if (better(x, v, bv, bi)) { bv = x; bi = v; }
-    if (typ) stat_add(st, x / T);
+    r.nonfinite |= !isfinite(x);
+    if (better(x, v, r.bv, r.bi)) { r.bv = x; r.bi = v; }
+    if (typ) stat_add(r.st, x / T);
   };
-  if ((a.V & 3) == 0) {
+  if ((a.V & 3) == 0 && (v0 & 3) == 0) {
     const float4* z4 = reinterpret_cast<const float4*>(z);
-    for (int q = threadIdx.x; q < a.V / 4; q += blockDim.x) {
+    const int q1 = v1 / 4;
+    for (int q = v0 / 4 + threadIdx.x; q < q1; q += blockDim.x) {
       const float4 x = z4[q];
       take(x.x, 4 * q);
       take(x.y, 4 * q + 1);
       take(x.z, 4 * q + 2);
       take(x.w, 4 * q + 3);
     }
+    for (int v = q1 * 4 + threadIdx.x; v < v1; v += blockDim.x) take(z[v], v);
   } else {
-    for (int v = threadIdx.x; v < a.V; v += blockDim.x) take(z[v], v);
+    for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) take(z[v], v);
   }
-  if (nonfinite) set_flag(a.status, MEDUSA_FLAG_NONFINITE);
-  if (typ) {                                   // merge the rows' statistics across the CTA
+  if (typ) {                                   // merge the statistics across the CTA
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      SoftStat other{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.S, o),
-                     __shfl_xor_sync(0xffffffffu, st.U, o)};
-      st = stat_merge(st, other);
+      SoftStat other{__shfl_xor_sync(0xffffffffu, r.st.m, o), __shfl_xor_sync(0xffffffffu, r.st.S, o),
+                     __shfl_xor_sync(0xffffffffu, r.st.U, o)};
+      r.st = stat_merge(r.st, other);
     }
-    if (lane == 0) { sv[warp] = st.m; sS[warp] = st.S; sU[warp] = st.U; }
+    __syncthreads();
+    if (lane == 0) { sv[warp] = r.st.m; sS[warp] = r.st.S; sU[warp] = r.st.U; }
     __syncthreads();
     if (warp == 0) {
-      st = lane < nw ? SoftStat{sv[lane], sS[lane], sU[lane]} : SoftStat{-INFINITY, 0.f, 0.f};
+      r.st = lane < nw ? SoftStat{sv[lane], sS[lane], sU[lane]} : SoftStat{-INFINITY, 0.f, 0.f};
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        SoftStat other{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.S, o),
-                       __shfl_xor_sync(0xffffffffu, st.U, o)};
-        st = stat_merge(st, other);
+        SoftStat other{__shfl_xor_sync(0xffffffffu, r.st.m, o), __shfl_xor_sync(0xffffffffu, r.st.S, o),
+                       __shfl_xor_sync(0xffffffffu, r.st.U, o)};
+        r.st = stat_merge(r.st, other);
       }
-      if (lane == 0) { sv[0] = st.m; sS[0] = st.S; sU[0] = st.U; }
     }
     __syncthreads();
-    st = SoftStat{sv[0], sS[0], sU[0]};
-    __syncthreads();
   }
-  block_argmax(bv, bi, sv, si);
-  if (threadIdx.x != 0) return;
-  if (bi < 0 || bi >= a.V) { set_flag(a.status, MEDUSA_FLAG_TOKEN_RANGE); bi = 0; }
-  float out[4] = {bv, 0.f, 0.f, 0.f};
-  if (typ) {
-    const float logS = logf(st.S);
-    out[0] = st.m;
+  block_argmax(r.bv, r.bi, sv, si);
+  return r;
+}
+
+// Thread 0: final am / stats of a row from its (merged) partial.
+__device__ void row_finish(const VerifyArgs& a, int row, RowPart r) {
+  const int b = row / a.n1, n = row - b * a.n1;
+  if (r.nonfinite) set_flag(a.status, MEDUSA_FLAG_NONFINITE);
+  if (r.bi < 0 || r.bi >= a.V) { set_flag(a.status, MEDUSA_FLAG_TOKEN_RANGE); r.bi = 0; }
+  float out[4] = {r.bv, 0.f, 0.f, 0.f};
+  if (a.typical) {
+    const float logS = logf(r.st.S);
+    out[0] = r.st.m;
     out[1] = logS;
-    out[2] = logS - st.U / st.S;               // H = log S - sum(y e^y) / S
+    out[2] = logS - r.st.U / r.st.S;           // H = log S - sum(y e^y) / S
     if (n > 0) {
       const int p = a.parent[n];
       const int t = a.tok[(long)b * a.n1 + n];
-      out[3] = a.logits[((long)b * a.n1 + p) * a.V + t] / T;
+      out[3] = a.logits[((long)b * a.n1 + p) * a.V + t] / a.temperature;
     }
     if (!isfinite(out[1]) || !isfinite(out[2])) set_flag(a.status, MEDUSA_FLAG_NONFINITE);
   }
-  a.am[row] = bi;
+  a.am[row] = r.bi;
 #pragma unroll
   for (int q = 0; q < 4; ++q) a.stats[(long)row * 4 + q] = out[q];
+}
+
+// Statistics of one node row (b, n) by one CTA.
+__device__ void row_stats(const VerifyArgs& a, int row) {
+  RowPart r = row_part(a, row, 0, a.V);
+  if (threadIdx.x == 0) row_finish(a, row, r);
 }
 
 __global__ void __launch_bounds__(1024) verify_stats_kernel(VerifyArgs a) { row_stats(a, blockIdx.x); }
@@ -150,11 +164,14 @@ cudaError_t launch_verify_stats(const VerifyArgs& a, cudaStream_t st) {
 // p.  Statistics are read through L2 (other CTAs of the same launch may have written them).
 __device__ void accept_seq(const VerifyArgs& a, int b) {
   __shared__ int acc[MEDUSA_MAX_NODES];
+  __shared__ int sret[MEDUSA_MAX_NODES * (MEDUSA_MAX_HEADS + 1)];
   __shared__ float sv[32];
   __shared__ int si[32];
   __shared__ int s_last;
   const int tid = threadIdx.x;
   const long rb = (long)b * a.n1;
+  const int W = a.K + 1;
+  for (int e = tid; e < a.P * W; e += blockDim.x) sret[e] = a.retrieve[e];
   const float log_eps = logf(a.eps), log_delta = logf(a.delta);
   for (int c = tid; c < a.n1; c += blockDim.x) {
     int ok = 1;                                     // the root is always kept
@@ -172,13 +189,12 @@ __device__ void accept_seq(const VerifyArgs& a, int b) {
   }
   __syncthreads();
   // longest run of accepted nodes after the root, per path; best = max, lowest index
-  const int W = a.K + 1;
   float bv = -INFINITY;
   int bi = 0x7fffffff;
   for (int p = tid; p < a.P; p += blockDim.x) {
     int m = 0;
     while (m + 1 < W) {
-      const int node = a.retrieve[(long)p * W + m + 1];
+      const int node = sret[p * W + m + 1];
       if (node < 0 || !acc[node]) break;
       ++m;
     }
@@ -187,7 +203,7 @@ __device__ void accept_seq(const VerifyArgs& a, int b) {
   block_argmax(bv, bi, sv, si);
   if (tid < W) {
     const int m = (int)bv, best = bi, l = tid;
-    const int node = l <= m ? a.retrieve[(long)best * W + l] : -1;
+    const int node = l <= m ? sret[best * W + l] : -1;
     if (a.path_nodes) a.path_nodes[(long)b * W + l] = node;
     a.out_tok[(long)b * W + l] = node >= 0 ? a.tok[rb + node] : -1;
     if (l == m) {
@@ -197,9 +213,18 @@ __device__ void accept_seq(const VerifyArgs& a, int b) {
     }
   }
   __syncthreads();
-  const float4* src = reinterpret_cast<const float4*>(a.hprime + (rb + s_last) * a.d);
-  float4* dst = reinterpret_cast<float4*>(a.h_next + (long)b * a.d);
-  for (int j = tid; j < a.d / 4; j += blockDim.x) dst[j] = src[j];
+  const float4* __restrict__ src = reinterpret_cast<const float4*>(a.hprime + (rb + s_last) * a.d);
+  float4* __restrict__ dst = reinterpret_cast<float4*>(a.h_next + (long)b * a.d);
+  const int nv = a.d / 4;
+  for (int j0 = tid; j0 < nv; j0 += blockDim.x * 4) {   // four loads in flight per thread
+    float4 t[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (j0 + u * (int)blockDim.x < nv) t[u] = src[j0 + u * blockDim.x];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (j0 + u * (int)blockDim.x < nv) dst[j0 + u * blockDim.x] = t[u];
+  }
   __syncthreads();
 }
 
@@ -226,26 +251,28 @@ __device__ void compact_seq(const CompactArgs& a, int b) {
       set_flag(a.status, MEDUSA_FLAG_KV_CAPACITY);
       n = a.capacity > L ? a.capacity - L : 0;
     }
-    for (int l = 0; l < n; ++l) {
-      const int node = a.path_nodes[(long)b * (a.K + 1) + l];
-      const int t = L + l;
-      long slot = -1;
-      if (node >= 0 && node < a.n1) {
-        if (a.page_table) {
-          const int page = a.page_table[(long)b * a.pages_per_seq + t / a.page_size];
-          if (page < 0 || page >= a.num_pages)
-            set_flag(a.status, MEDUSA_FLAG_PAGE_RANGE);
-          else
-            slot = (long)page * a.page_size + t % a.page_size;
-        } else {
-          slot = (long)b * a.capacity + t;
-        }
-      }
-      s_dst[l] = slot * row;
-      s_src[l] = ((long)b * a.n1 + (node < 0 ? 0 : node)) * row;
-    }
     s_len = L;
     s_n = n;
+  }
+  __syncthreads();
+  if (threadIdx.x < s_n) {                            // one thread per kept token
+    const int l = threadIdx.x;
+    const int node = a.path_nodes[(long)b * (a.K + 1) + l];
+    const int t = s_len + l;
+    long slot = -1;
+    if (node >= 0 && node < a.n1) {
+      if (a.page_table) {
+        const int page = a.page_table[(long)b * a.pages_per_seq + t / a.page_size];
+        if (page < 0 || page >= a.num_pages)
+          set_flag(a.status, MEDUSA_FLAG_PAGE_RANGE);
+        else
+          slot = (long)page * a.page_size + t % a.page_size;
+      } else {
+        slot = (long)b * a.capacity + t;
+      }
+    }
+    s_dst[l] = slot * row;
+    s_src[l] = ((long)b * a.n1 + (node < 0 ? 0 : node)) * row;
   }
   __syncthreads();
   const int n = s_n;
@@ -255,13 +282,31 @@ __device__ void compact_seq(const CompactArgs& a, int b) {
   const uint4* tk = reinterpret_cast<const uint4*>(a.tk);
   const uint4* tv = reinterpret_cast<const uint4*>(a.tv);
   constexpr int EPV = 16 / sizeof(T);                   // elements per piece
-  for (int e = threadIdx.x; e < n * per; e += blockDim.x) {
-    const int l = e / per, c = e - l * per;
-    if (s_dst[l] < 0) continue;
-    const long d = s_dst[l] / EPV + c, s = s_src[l] / EPV + c;
-    const uint4 k = tk[s], v = tv[s];
-    kc[d] = k;
-    vc[d] = v;
+  constexpr int BATCH = 8;                              // loads in flight before the stores
+  const int total = n * per, step = blockDim.x;
+  for (int e0 = threadIdx.x; e0 < total; e0 += step * BATCH) {
+    uint4 kb[BATCH], vb[BATCH];
+    long dst[BATCH];
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int e = e0 + u * step;
+      dst[u] = -1;
+      if (e < total) {
+        const int l = e / per, c = e - l * per;
+        if (s_dst[l] >= 0) {
+          const long s = s_src[l] / EPV + c;
+          kb[u] = tk[s];
+          vb[u] = tv[s];
+          dst[u] = s_dst[l] / EPV + c;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u)
+      if (dst[u] >= 0) {
+        kc[dst[u]] = kb[u];
+        vc[dst[u]] = vb[u];
+      }
   }
   __syncthreads();
   if (threadIdx.x == 0) a.len_out[b] = s_len + n;
@@ -270,31 +315,64 @@ __device__ void compact_seq(const CompactArgs& a, int b) {
 template <typename T>
 __global__ void __launch_bounds__(256) kv_compact_kernel(CompactArgs a) { compact_seq<T>(a, blockIdx.x); }
 
-// Fused verification for the whole step: one CTA per node row computes its statistics; the
-// last CTA to finish for a sequence (atomic counter, nothing waits) runs that sequence's
-// acceptance and KV compaction, then resets the counter.
+// Fused verification for the whole step.  Each node row's vocabulary is split over
+// kVerifySlices CTAs; the last slice CTA of a row (per-row counter) merges the partials and
+// finishes the row; the last row of a sequence (per-sequence counter) runs that sequence's
+// acceptance and KV compaction.  Nothing waits; every counter is reset after use.
+constexpr int kVerifySlices = 4;
+
 template <typename T>
-__global__ void __launch_bounds__(1024) verify_commit_kernel(VerifyArgs v, CompactArgs c, int32_t* counter) {
+__global__ void __launch_bounds__(256) verify_commit_kernel(VerifyArgs v, CompactArgs c, int32_t* row_cnt,
+                                                            int32_t* seq_cnt, float* parts) {
   __shared__ int s_last;
-  const int row = blockIdx.x, b = row / v.n1;
-  row_stats(v, row);
-  __threadfence();
+  const int row = blockIdx.x, sl = blockIdx.y, b = row / v.n1;
+  const int per = ((v.V + kVerifySlices - 1) / kVerifySlices + 3) / 4 * 4;
+  const int v0 = min(v.V, sl * per), v1 = min(v.V, v0 + per);
+  RowPart r = row_part(v, row, v0, v1);
+  float* pp = parts + ((long)row * kVerifySlices + sl) * 6;
+  if (threadIdx.x == 0) {
+    pp[0] = r.bv;
+    pp[1] = __int_as_float(r.bi);
+    pp[2] = r.st.m;
+    pp[3] = r.st.S;
+    pp[4] = r.st.U;
+    pp[5] = r.nonfinite ? 1.f : 0.f;
+    __threadfence();
+    s_last = atomicAdd(row_cnt + row, 1) == kVerifySlices - 1;
+  }
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(counter + b, 1) == v.n1 - 1;
+  if (!s_last) return;
+  if (threadIdx.x == 0) {                         // merge the row's slices
+    __threadfence();
+    RowPart m{-INFINITY, 0x7fffffff, SoftStat{-INFINITY, 0.f, 0.f}, false};
+    for (int q = 0; q < kVerifySlices; ++q) {
+      const float* x = parts + ((long)row * kVerifySlices + q) * 6;
+      const float bv = __ldcg(x), m0 = __ldcg(x + 2), S = __ldcg(x + 3), U = __ldcg(x + 4);
+      const int bi = __float_as_int(__ldcg(x + 1));
+      if (better(bv, bi, m.bv, m.bi)) { m.bv = bv; m.bi = bi; }
+      m.st = stat_merge(m.st, SoftStat{m0, S, U});
+      m.nonfinite |= __ldcg(x + 5) != 0.f;
+    }
+    row_finish(v, row, m);
+    row_cnt[row] = 0;
+    __threadfence();
+    s_last = atomicAdd(seq_cnt + b, 1) == v.n1 - 1;
+  }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
   accept_seq(v, b);
   compact_seq<T>(c, b);
-  if (threadIdx.x == 0) counter[b] = 0;
+  if (threadIdx.x == 0) seq_cnt[b] = 0;
 }
 
-cudaError_t launch_verify_commit(const VerifyArgs& v, const CompactArgs& c, int32_t* counter,
-                                 cudaStream_t st) {
+cudaError_t launch_verify_commit(const VerifyArgs& v, const CompactArgs& c, int32_t* row_cnt,
+                                 int32_t* seq_cnt, float* parts, cudaStream_t st) {
+  dim3 grid(v.B * v.n1, kVerifySlices);
   if (c.dtype == 0)
-    verify_commit_kernel<float><<<v.B * v.n1, 1024, 0, st>>>(v, c, counter);
+    verify_commit_kernel<float><<<grid, 256, 0, st>>>(v, c, row_cnt, seq_cnt, parts);
   else
-    verify_commit_kernel<bf16><<<v.B * v.n1, 1024, 0, st>>>(v, c, counter);
+    verify_commit_kernel<bf16><<<grid, 256, 0, st>>>(v, c, row_cnt, seq_cnt, parts);
   return cudaGetLastError();
 }
 

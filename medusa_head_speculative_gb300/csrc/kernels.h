@@ -63,6 +63,8 @@ struct TopkArgs {
   int B, nh, V, splits, chunk;
   float* cand_val;       // [B][nh][splits][kTops]
   int32_t* cand_idx;
+  int rounds[MEDUSA_MAX_HEADS + 1];   // ranks needed per head (0 = all kTops); the rest
+                                      // of each list is left as sentinels
 };
 cudaError_t launch_topk_partial(const TopkArgs& a, cudaStream_t st);
 
@@ -73,6 +75,7 @@ struct MergeArgs {
   const int32_t* root_in;
   int32_t* topk_tok; float* topk_val; int32_t* root_out;              // [B][K][kTops], [B]
   uint32_t* status;
+  int rounds[MEDUSA_MAX_HEADS + 1];   // as TopkArgs::rounds
 };
 cudaError_t launch_topk_merge(const MergeArgs& a, cudaStream_t st);
 
@@ -148,9 +151,10 @@ struct CompactArgs {
   uint32_t* status;
 };
 cudaError_t launch_kv_compact(const CompactArgs& a, cudaStream_t st);
-// Fused per-row statistics + acceptance + KV compaction.  counter: [B] zeros on entry.
-cudaError_t launch_verify_commit(const VerifyArgs& v, const CompactArgs& c, int32_t* counter,
-                                 cudaStream_t st);
+// Fused per-row statistics + acceptance + KV compaction.  row_cnt [B*n1] and seq_cnt [B]
+// zero on entry (left zero); parts: [B*n1][4][6] float scratch.
+cudaError_t launch_verify_commit(const VerifyArgs& v, const CompactArgs& c, int32_t* row_cnt,
+                                 int32_t* seq_cnt, float* parts, cudaStream_t st);
 
 // Plan fields used by the workspace-free heads entry point (defined in capi.cu).
 struct HeadsPlanView {
