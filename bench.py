@@ -88,6 +88,59 @@ def step_bytes(w: S.Workload, n1: int):
     return heads + lm + kv + layer
 
 
+def steady_bytes(w: S.Workload, n1: int):
+    """step_bytes of a decode-loop step whose root comes from the previous step: the LM
+    head is read once (for verification)."""
+    es = 4 if w.dtype == "f32" else 2
+    return step_bytes(w, n1) - w.V * w.d * es
+
+
+def steady_state(args, w: S.Workload, st, stream, barrier):
+    """The decode loop's steady state: each step takes the previous step's root_next and
+    h_next (so the LM head is not applied to h_t), as a CUDA graph of two ping-ponged
+    steps.  The prefix length is held at the workload's (len_out goes to a side buffer),
+    so every step sees the same context size."""
+    from medusa_head_speculative_gb300 import binding as Bnd
+    plan, o = st["plan"], st["out"]
+    h_a = st["h"].clone()
+    h_b = torch.empty_like(h_a)
+    r_a = o["root_next"].clone()
+    r_b = torch.empty_like(r_a)
+    outs_a = Bnd.outputs_struct(o["out_tok"], o["n_acc"], o["path"], h_b, r_b)
+    outs_b = Bnd.outputs_struct(o["out_tok"], o["n_acc"], o["path"], h_a, r_a)
+
+    def pair():
+        Bnd.step(plan, h_a, r_a, st["wstruct"], st["kv"], st["acc"], outs_a, st["ws"])
+        Bnd.step(plan, h_b, r_b, st["wstruct"], st["kv"], st["acc"], outs_b, st["ws"])
+
+    for _ in range(3):
+        pair()
+    run, mode = pair, "direct"
+    if not args.no_graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                pair()
+            g.replay()
+            run, mode = g.replay, "cuda_graph"
+        except Exception as exc:                        # noqa: BLE001
+            mode = f"direct (graph capture failed: {exc})"[:160]
+    reps = max(1, args.steps // 2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(reps):
+        run()
+    e1.record(stream)
+    barrier()
+    ms = e0.elapsed_time(e1) / (2 * reps)
+    assert plan.status() == 0, "device status word set during the steady-state region"
+    return {"value": round(1e3 / ms, 2), "unit": "steps/s", "ms_per_step": round(ms, 5),
+            "steps": 2 * reps, "launch": mode,
+            "note": "root_in = previous root_next, h = previous h_next: the LM head is read "
+                    "once per step; prefix length held fixed"}
+
+
 # ----------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -253,6 +306,7 @@ def run_ours(args, w: S.Workload):
     ms_max = float(t.item())
     assert plan.status() == 0, "device status word set during the timed region"
     n_acc_mean = float(st["out"]["n_acc"].float().mean())
+    steady = steady_state(args, w, st, stream, barrier)
 
     # end to end: h_t from pinned host memory, result (tokens, counts) back, every step
     ke = min(K, 500)
@@ -321,6 +375,9 @@ def run_ours(args, w: S.Workload):
                 "h2d_bytes_per_step": int(h_host.numel() * 4),
                 "d2h_bytes_per_step": int(tok_host.numel() * 4 + nacc_host.numel() * 4)},
         "clocks": clk,
+        "steady_state": dict(steady, step_hbm_frac=round(
+            steady_bytes(w, n1) / (steady["ms_per_step"] * 1e-3) / 1e9 / hbm, 4),
+            step_bytes=steady_bytes(w, n1)),
         "gpu_launches": int(launches),
         "launch": launch_mode,
     }
@@ -414,6 +471,114 @@ def run_reference(args, w: S.Workload):
                     "d2h_bytes_per_step": 0}}
 
 
+# ----------------------------------------------------------------------- 33B sweep
+def device_inputs(w: S.Workload, device):
+    """Seeded synthetic weights, h_t and KV cache drawn on the device (torch's CUDA
+    generator), with the same shapes and distributions as synthetic.inputs.  Used only for
+    timing the large sweep points, where drawing tens of GB on the host would dominate."""
+    gen = torch.Generator(device=device)
+    dt = w.torch_dtype
+
+    def normal(shape, std, tag):
+        gen.manual_seed(w.seed * 1000003 + tag)
+        return (torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+                * std).to(dt)
+
+    d, V, K = w.d, w.V, w.K
+    qd, kd = w.Hq * w.dh, w.Hkv * w.dh
+    sd = 1.0 / math.sqrt(d)
+    wts = {"w1": normal((K, d, d), sd, 1), "w2": normal((K, V, d), sd, 2),
+           "lm": normal((V, d), sd, 3), "emb": normal((V, d), 1.0, 4),
+           "wq": normal((qd, d), sd, 5), "wk": normal((kd, d), sd, 6),
+           "wv": normal((kd, d), sd, 7), "wo": normal((d, qd), 1.0 / math.sqrt(qd), 8)}
+    h = normal((w.B, d), 1.0, 9).float()
+    kc = torch.zeros((w.B, w.capacity, w.Hkv, w.dh), dtype=dt, device=device)
+    vc = torch.zeros_like(kc)
+    for b in range(w.B):
+        L = w.lengths[b]
+        kc[b, :L] = normal((L, w.Hkv, w.dh), 1.0, 100 + 2 * b)
+        vc[b, :L] = normal((L, w.Hkv, w.dh), 1.0, 101 + 2 * b)
+    return wts, h, kc, vc
+
+
+def run_sweep(args):
+    """The Vicuna-33B-shaped grid: batch x prefix x tree size, one JSON line per point with
+    steps/s and the heads' and tree attention's HBM GB/s (separately)."""
+    from medusa_head_speculative_gb300 import binding as Bnd
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    hbm, _ = peaks()
+    Bs = [int(x) for x in args.sweep_b.split(",")]
+    Ls = [int(x) for x in args.sweep_l.split(",")]
+    Ns = [int(x) for x in args.sweep_n.split(",")]
+    wts = None
+    for N in Ns:
+        for B in Bs:
+            for L in Ls:
+                w = S.vicuna33b(B, L, N)
+                parent, rank = Bnd.tree_greedy(w.s, S.score_table(w.K, max(w.s)), w.N)
+                plan = Bnd.Plan(w.B, w.d, w.V, w.K, w.Hq, w.Hkv, w.dh, Bnd.BF16, w.capacity,
+                                w.s, parent, rank, rope_base=w.rope_base)
+                wp, h, kc, vc = device_inputs(w, device)
+                if wts is None:
+                    wts = wp
+                else:
+                    del wp
+                length = torch.tensor(w.lengths, dtype=torch.int32, device=device)
+                len_out = torch.empty_like(length)
+                ws = torch.empty(plan.workspace_size, dtype=torch.uint8, device=device)
+                i32 = dict(dtype=torch.int32, device=device)
+                outs = Bnd.outputs_struct(torch.empty(B, w.K + 1, **i32), torch.empty(B, **i32),
+                                          torch.empty(B, w.K + 1, **i32),
+                                          torch.empty(B, w.d, dtype=torch.float32, device=device),
+                                          torch.empty(B, **i32))
+                wst = Bnd.weights_struct(wts)
+                kv = Bnd.kv_struct(kc, vc, length, len_out, None)
+                acc = Bnd.accept_struct("greedy", 0.0, 0.09, 0.3)
+
+                def one():
+                    Bnd.step(plan, h, None, wst, kv, acc, outs, ws)
+
+                for _ in range(3):
+                    one()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    one()
+                g.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(args.steps):
+                    g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / args.steps
+                plan.profile_start(8 * 32)
+                for _ in range(8):
+                    one()
+                kern, _ = plan.profile_stop()
+                status = plan.status()
+                n1 = plan.n1
+                kb = kernel_bytes(w, n1, plan_tc_heads(w))
+                t = {k: v[1] / v[0] for k, v in kern.items()}          # ms per launch
+                heads_ms = t.get("heads_w1", 0) + t.get("heads_vocab", 0) + t.get("split_h", 0)
+                attn_ms = t.get("tree_attention", 0) + t.get("attn_combine", 0) + t.get("cast_q", 0)
+                sb = step_bytes(w, n1)
+                row = {"sweep": "vicuna33b", "B": B, "prefix": L, "tree_nodes": n1,
+                       "steps_per_s": round(1e3 / ms, 2), "ms_per_step": round(ms, 4),
+                       "tree_nodes_per_s": round(1e3 / ms * B * n1, 1),
+                       "step_hbm_gbs": round(sb / (ms * 1e-3) / 1e9, 1),
+                       "step_hbm_frac": round(sb / (ms * 1e-3) / 1e9 / hbm, 4),
+                       "medusa_heads_gbs": round((kb["heads_w1"] + kb["heads_vocab"])
+                                                 / (heads_ms * 1e-3) / 1e9, 1),
+                       "tree_attention_gbs": round(kb["tree_attention"] / (attn_ms * 1e-3) / 1e9, 1),
+                       "kernels_us": {k: round(v * 1e3, 1) for k, v in t.items()},
+                       "status": status}
+                print(json.dumps(row), flush=True)
+                del g, plan, ws, kc, vc, h, kv
+                torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -423,7 +588,15 @@ def main():
     ap.add_argument("--workload", default="vicuna7b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct calls, not a CUDA graph")
+    ap.add_argument("--sweep", action="store_true",
+                    help="Vicuna-33B-shaped grid instead of the default workload")
+    ap.add_argument("--sweep-b", default="1,4,16,64")
+    ap.add_argument("--sweep-l", default="1024,4096,16384")
+    ap.add_argument("--sweep-n", default="16,64,128")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     w = S.workload(args.workload)
     res = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if res is not None:

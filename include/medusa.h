@@ -153,7 +153,9 @@ medusa_status medusa_get_status(const medusa_plan* plan, void* stream, uint32_t*
 /* ------------------------------------------------------------------ full step */
 /* One decode step ([MEDUSA] §3.2 information flow, steps (2)-(6); [READING] section 3).
  * h: device [B][d] last hidden state.  root_in: device [B] first token carried from the
- * previous step's root_next, or NULL to take the LM head's greedy token on h. */
+ * previous step's root_next, or NULL to take the LM head's greedy token on h.  With
+ * root_in given the LM head is not applied to h (it would only yield the root), so a
+ * step of the steady-state decode loop reads the LM head once, for verification. */
 medusa_status medusa_step(const medusa_plan* plan, const float* h, const int32_t* root_in,
                           const medusa_weights* w, const medusa_kv* kv, medusa_accept acc,
                           const medusa_outputs* out, void* workspace, size_t ws_bytes,
@@ -162,7 +164,8 @@ medusa_status medusa_step(const medusa_plan* plan, const float* h, const int32_t
 /* ------------------------------------------------------------------ stages */
 /* (a) Heads ([MEDUSA] §3.4 MEDUSA Heads eq.; Tree Attention Step 1).  Writes the
  * logits [B][K+1][V] (row 0: LM head, row k: head k) to `logits` (device, may be NULL to
- * keep them in the workspace), topk_tok/topk_val [B][K][16] (ranks past s_k unspecified)
+ * keep them in the workspace; row 0 is left unwritten when root_in is given, as the LM
+ * head pass is then skipped), topk_tok/topk_val [B][K][16] (ranks past s_k unspecified)
  * and root [B] (root_in's value when given, else the LM head's greedy token; ties to the
  * lowest token id). */
 medusa_status medusa_heads(const medusa_plan* plan, const float* h, const int32_t* root_in,

@@ -248,20 +248,23 @@ medusa_status heads_impl(const medusa_plan* p, const float* h, const int32_t* ro
     s.out_off = k * D;
   }
   LAUNCH(p, KN_H_W1, st, p->tc_heads ? launch_umma_gemm(a, p->d_status, st) : launch_rowdot(a, d.dtype, st));
-  // z_0 = LM h, z_k = W2_k u_k
+  // z_0 = LM h (only when the root is not given), z_k = W2_k u_k
+  const int k0 = root_in ? 1 : 0;
   MatArgs b{};
-  b.nseg = K + 1;
+  b.nseg = K + 1 - k0;
   b.M = B;
   b.k = D;
   b.out = logits;
   b.ldo = (long)(K + 1) * V;
   b.epi = EPI_STORE;
-  b.seg[0].w = w->lm;
-  b.seg[0].x = h; b.seg[0].a_hi = hhi; b.seg[0].a_lo = hlo; b.seg[0].ldx = D;
-  b.seg[0].rows = V;
-  b.seg[0].out_off = 0;
+  if (!root_in) {
+    b.seg[0].w = w->lm;
+    b.seg[0].x = h; b.seg[0].a_hi = hhi; b.seg[0].a_lo = hlo; b.seg[0].ldx = D;
+    b.seg[0].rows = V;
+    b.seg[0].out_off = 0;
+  }
   for (int k = 1; k <= K; ++k) {
-    MatSeg& s = b.seg[k];
+    MatSeg& s = b.seg[k - k0];
     s.w = static_cast<const char*>(w->w2) + (size_t)(k - 1) * V * D * es;
     s.x = u + (size_t)(k - 1) * D;
     s.a_hi = p->tc_heads ? at<bf16>(ws, p->o_uhi) + (size_t)(k - 1) * D : nullptr;
@@ -275,20 +278,25 @@ medusa_status heads_impl(const medusa_plan* p, const float* h, const int32_t* ro
   return MEDUSA_OK;
 }
 
-TopkArgs topk_args(const medusa_plan* p, const float* logits, void* ws) {
-  return TopkArgs{logits, p->d.B, p->K + 1, p->d.V, p->topk_splits, p->topk_chunk,
-                  at<float>(ws, p->o_cv), at<int32_t>(ws, p->o_ci)};
+// Head 0 (the LM head) is selected only when the root is not given.
+TopkArgs topk_args(const medusa_plan* p, const float* logits, const int32_t* root_in, void* ws) {
+  TopkArgs t{logits, p->d.B, p->K + 1, p->d.V, p->topk_splits, p->topk_chunk,
+             at<float>(ws, p->o_cv), at<int32_t>(ws, p->o_ci)};
+  t.k0 = root_in ? 1 : 0;
+  return t;
 }
 MergeArgs merge_args(const medusa_plan* p, const int32_t* root_in, int32_t* ttok, float* tval,
                      int32_t* root, void* ws) {
-  return MergeArgs{at<float>(ws, p->o_cv), at<int32_t>(ws, p->o_ci), p->d.B, p->K, p->d.V,
-                   p->topk_splits, root_in, ttok, tval, root, p->d_status};
+  MergeArgs m{at<float>(ws, p->o_cv), at<int32_t>(ws, p->o_ci), p->d.B, p->K, p->d.V,
+              p->topk_splits, root_in, ttok, tval, root, p->d_status};
+  m.k0 = root_in ? 1 : 0;
+  return m;
 }
 
 // per-head top-16 and root from the head logits (the heads stage's selection)
 medusa_status heads_topk(const medusa_plan* p, const float* logits, const int32_t* root_in,
                          int32_t* ttok, float* tval, int32_t* root, void* ws, cudaStream_t st) {
-  const TopkArgs t = topk_args(p, logits, ws);
+  const TopkArgs t = topk_args(p, logits, root_in, ws);
   LAUNCH(p, KN_TOPK_PARTIAL, st, launch_topk_partial(t, st));
   const MergeArgs mg = merge_args(p, root_in, ttok, tval, root, ws);
   LAUNCH(p, KN_TOPK_MERGE, st, launch_topk_merge(mg, st));
@@ -869,7 +877,7 @@ medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* r
   if ((s = heads_impl(p, h, root_in, w, logits, ttok, at<float>(ws, p->o_tval), root, ws, st)) != MEDUSA_OK)
     return s;
   {   // fused: slice top-k, head merge and node tokens / positions
-    TopkArgs t = topk_args(p, logits, ws);
+    TopkArgs t = topk_args(p, logits, root_in, ws);
     MergeArgs mg = merge_args(p, root_in, ttok, at<float>(ws, p->o_tval), root, ws);
     for (int k = 0; k <= p->K; ++k) t.rounds[k] = mg.rounds[k] = p->need[k];
     TreeArgs tr{ttok, root, kv->len, p->d.B, p->K, p->d.V, p->n1, p->dparent(), p->ddepth(), p->drank(),

@@ -101,11 +101,11 @@ __device__ void slice_topk(const TopkArgs& a, int sp, int k, int b) {
 }
 
 __global__ void __launch_bounds__(256) topk_partial_kernel(TopkArgs a) {
-  slice_topk(a, blockIdx.x, blockIdx.y, blockIdx.z);
+  slice_topk(a, blockIdx.x, blockIdx.y + a.k0, blockIdx.z);
 }
 
 cudaError_t launch_topk_partial(const TopkArgs& a, cudaStream_t st) {
-  dim3 grid(a.splits, a.nh, a.B);
+  dim3 grid(a.splits, a.nh - a.k0, a.B);
   topk_partial_kernel<<<grid, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
@@ -117,7 +117,7 @@ __device__ void merge_heads(const MergeArgs& a, int b, float (*tv)[kTops], int (
                             int* s_root) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
   const int nh = a.K + 1;
-  for (int k = warp; k < nh; k += nw) {
+  for (int k = warp + a.k0; k < nh; k += nw) {
     TopList L;
     L.init();
     if (lane < a.splits) {
@@ -129,7 +129,7 @@ __device__ void merge_heads(const MergeArgs& a, int b, float (*tv)[kTops], int (
   }
   __syncthreads();
   if (tid == 0) {
-    int r = a.root_in ? a.root_in[b] : ti[0][0];
+    int r = a.root_in ? a.root_in[b] : (a.k0 == 0 ? ti[0][0] : -1);
     if (r < 0 || r >= a.V) { set_flag(a.status, MEDUSA_FLAG_TOKEN_RANGE); r = 0; }
     a.root_out[b] = r;
     *s_root = r;
@@ -177,10 +177,10 @@ __global__ void __launch_bounds__(256) heads_select_kernel(TopkArgs t, MergeArgs
   __shared__ int ti[MEDUSA_MAX_HEADS + 1][kTops];
   __shared__ int s_root, s_last;
   const int b = blockIdx.z;
-  slice_topk(t, blockIdx.x, blockIdx.y, b);
+  slice_topk(t, blockIdx.x, blockIdx.y + t.k0, b);
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(counter + b, 1) == t.splits * t.nh - 1;
+  if (threadIdx.x == 0) s_last = atomicAdd(counter + b, 1) == t.splits * (t.nh - t.k0) - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(256) heads_select_kernel(TopkArgs t, MergeArgs
 
 cudaError_t launch_heads_select(const TopkArgs& t, const MergeArgs& m, const TreeArgs& tr,
                                 int32_t* counter, cudaStream_t st) {
-  dim3 grid(t.splits, t.nh, t.B);
+  dim3 grid(t.splits, t.nh - t.k0, t.B);
   heads_select_kernel<<<grid, 256, 0, st>>>(t, m, tr, counter);
   return cudaGetLastError();
 }

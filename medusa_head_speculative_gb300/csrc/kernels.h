@@ -65,6 +65,8 @@ struct TopkArgs {
   int32_t* cand_idx;
   int rounds[MEDUSA_MAX_HEADS + 1];   // ranks needed per head (0 = all kTops); the rest
                                       // of each list is left as sentinels
+  int k0;                             // first head to select (1: the root is given and
+                                      // the LM head's logits were not computed)
 };
 cudaError_t launch_topk_partial(const TopkArgs& a, cudaStream_t st);
 
@@ -76,6 +78,7 @@ struct MergeArgs {
   int32_t* topk_tok; float* topk_val; int32_t* root_out;              // [B][K][kTops], [B]
   uint32_t* status;
   int rounds[MEDUSA_MAX_HEADS + 1];   // as TopkArgs::rounds
+  int k0;                             // as TopkArgs::k0 (requires root_in when 1)
 };
 cudaError_t launch_topk_merge(const MergeArgs& a, cudaStream_t st);
 

@@ -34,6 +34,9 @@ CASES = {
                             mode="typical", temperature=1.3, s=(4, 3, 2, 2), tree="cartesian",
                             N=4 + 12 + 24 + 48), None),
     "mid_fp32_gqa": (_mid(dtype="f32", d=96, V=700, lengths=(5, 70, 33)), None),
+    # 151 nodes of one query head per KV head: two 128-row attention tiles, three tree-key
+    # chunks, ancestors across the tile boundary
+    "mid_n150_mha": (_mid(B=2, Hq=4, Hkv=4, N=150, lengths=(70, 200)), None),
     "vicuna7b": (S.workload("vicuna7b"), None),
     "vicuna7b_typical": (S.workload("vicuna7b_typical"), None),
     "vicuna13b": (S.workload("vicuna13b"), (0, 5)),
@@ -93,6 +96,34 @@ def _logical_cache(dev, t):
 @pytest.mark.parametrize("name", list(CASES))
 def test_step_matches_oracle(name):
     _check(name)
+
+
+@pytest.mark.parametrize("name", ["mid_greedy", "mid_b6_typical", "vicuna7b"])
+def test_step_with_given_root(name):
+    """A root carried in from the previous step (the LM head pass on h_t is skipped): the
+    stages and the fused step both match the oracle's step with that root."""
+    w, sample = CASES[name]
+    dev = setup(w)
+    rng = np.random.default_rng(11)
+    roots = rng.integers(0, w.V, size=w.B).astype(np.int32)
+    root_in = torch.from_numpy(roots).cuda()
+    g = run_stages(dev, root_in=root_in)
+    np.testing.assert_array_equal(g["root"], roots)
+    ow = O.oracle_weights(dev.cpu["wts"])
+    seqs = list(sample) if sample else list(range(w.B))
+    report, flagged = {}, []
+    for b in seqs:
+        r = oracle_step(dev, b, ow, root=int(roots[b]))
+        try:
+            compare_sequence(g, r, b, dev.spec, w, report, root_given=True)
+        except Flagged as e:
+            flagged.append((b, str(e)))
+    assert len(flagged) <= max(1, len(seqs) // 2), flagged
+    s = run_step(dev, root_in=root_in, len_out=torch.empty_like(dev.length))
+    np.testing.assert_array_equal(s["out_tok"], g["out_tok"])
+    np.testing.assert_array_equal(s["path"], g["path"])
+    np.testing.assert_array_equal(s["h_next"].cpu().numpy(), g["h_next"])
+    assert dev.plan.status() == 0
 
 
 def test_fp32_tiny_tight_tolerance():
