@@ -389,7 +389,7 @@ def run_ours(args, w: S.Workload):
 
 
 def plan_tc_heads(w: S.Workload):
-    return w.dtype == "bf16" and w.B > 4
+    return w.dtype == "bf16" and w.B >= 2
 
 
 def load_traffic(workload: str, kernel: str):

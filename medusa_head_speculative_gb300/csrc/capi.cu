@@ -612,7 +612,9 @@ medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec
   for (int n = 1; n < p->n1; ++n) haschild[p->parent[n]] = 1;
   p->P = (int)std::count(haschild.begin(), haschild.end(), 0);
   p->M = dims->B * p->n1;
-  p->tc_heads = dims->dtype == MEDUSA_BF16 && dims->B > 4;
+  // Row-dot re-reads the staged activations from shared memory once per batch row for
+  // every 16 bytes of weights; from two rows on, the tensor-core path streams faster.
+  p->tc_heads = dims->dtype == MEDUSA_BF16 && dims->B >= 2;
   p->tc_nodes = dims->dtype == MEDUSA_BF16;
 
   cudaGetDevice(&p->device);
@@ -627,7 +629,7 @@ medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec
   const int R = p->n1 * G;
   p->tc_attn = tree_attention_tc_supported(dims->dtype, dims->dh, G, dims->page_size);
   p->rpw = R <= 32 ? 4 : (R <= 72 ? 9 : 12);
-  p->rows_per_block = p->tc_attn ? 128 : 8 * p->rpw;
+  p->rows_per_block = p->tc_attn ? (R > 128 ? 256 : 128) : 8 * p->rpw;
   p->nrb = (R + p->rows_per_block - 1) / p->rows_per_block;
   const int base = dims->B * dims->Hkv * p->nrb;
   const int want = std::max(1, (2 * p->num_sms + base - 1) / base);
@@ -635,13 +637,19 @@ medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec
   const int max_splits = std::max(1, (dims->capacity + gran - 1) / gran);
   p->nsplit = std::min(want, max_splits);
   if (p->tc_attn) {
-    // one resident CTA per SM: minimise rounds x (keys per CTA + fixed per-CTA cost)
-    long best = -1;
+    // One resident CTA per SM.  Cost in key-loads of one SM: the busiest SM's keys (the
+    // work spread over the SMs, but no less than one CTA's chunk; each CTA also pays a
+    // fixed start-up of about three chunks), plus the partials that the splits write and
+    // the combine reads back, in the same units.
+    const double key_bytes = 2.0 * dims->dh * 2;                 // one key's K and V
+    const double part_bytes = 2.0 * dims->B * dims->Hq * p->n1 * (dims->dh * 4 + 8);
+    const long tree_keys = ((p->n1 + gran - 1) / gran + 3) * (long)gran;
+    double best = -1;
     for (int ns = 1; ns <= std::min(max_splits, 64); ++ns) {
-      const long ctas = (long)base * (ns + 1);
-      const long rounds = (ctas + p->num_sms - 1) / p->num_sms;
-      const long keys = ((dims->capacity + ns - 1) / ns + gran - 1) / gran * gran;
-      const long cost = rounds * (keys + 3 * gran);
+      const long keys = ((dims->capacity + ns - 1) / ns + gran - 1) / gran * gran + 3 * gran;
+      const double work = ((double)base * ns * keys + (double)base * tree_keys) / p->num_sms;
+      const double cost = std::max(work, (double)keys) +
+                          (ns + 1) * part_bytes / (p->num_sms * key_bytes);
       if (best < 0 || cost < best) { best = cost; p->nsplit = ns; }
     }
   }

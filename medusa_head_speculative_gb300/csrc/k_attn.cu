@@ -146,29 +146,56 @@ __global__ void __launch_bounds__(256) tree_attn_kernel(AttnArgs a) {
   }
 }
 
-// One CTA per (query row, kv head, sequence): o = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s
-__global__ void attn_combine_kernel(AttnArgs a) {
-  const int r = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+// One warp per (sequence, kv head, query row): o = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s
+// over the prefix splits and the tree split, M = max_s m_s.  Lane j holds the VPL
+// consecutive columns [j*VPL, (j+1)*VPL) of the head (dh = 32 * VPL); the splits' (m, l)
+// pairs are read once per lane and reduced across the warp.
+template <int VPL>
+__global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
   const int R = a.n1 * a.G, S = a.nsplit + 1;
-  const long base = ((long)b * a.Hkv + g) * S * R;
+  const long wg = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (wg >= (long)a.B * a.Hkv * R) return;
+  const int lane = threadIdx.x & 31;
+  const int r = (int)(wg % R);
+  const long bg = wg / R;                            // b * Hkv + g
+  const int g = (int)(bg % a.Hkv), b = (int)(bg / a.Hkv);
+  const long base = bg * S * R + r;                  // partial row of split s: base + s * R
   float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, a.part_ml[(base + (long)s * R + r) * 2]);
+  for (int s = lane; s < S; s += 32) M = fmaxf(M, a.part_ml[(base + (long)s * R) * 2]);
+  M = warp_max(M);
   float Lsum = 0.f;
-  for (int s = 0; s < S; ++s) {
-    const float m = a.part_ml[(base + (long)s * R + r) * 2];
-    if (m != -INFINITY) Lsum += __expf(m - M) * a.part_ml[(base + (long)s * R + r) * 2 + 1];
+  for (int s = lane; s < S; s += 32) {
+    const float m = a.part_ml[(base + (long)s * R) * 2];
+    if (m != -INFINITY) Lsum += __expf(m - M) * a.part_ml[(base + (long)s * R) * 2 + 1];
   }
-  const int n = r / a.G, hq = g * a.G + r % a.G;
-  const long orow = ((long)b * a.n1 + n) * a.Hq + hq;
-  for (int i = threadIdx.x; i < a.dh; i += blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float m = a.part_ml[(base + (long)s * R + r) * 2];
-      if (m != -INFINITY) acc += __expf(m - M) * a.part_o[(base + (long)s * R + r) * a.dh + i];
+  Lsum = warp_sum(Lsum);
+  float acc[VPL];
+#pragma unroll
+  for (int c = 0; c < VPL; ++c) acc[c] = 0.f;
+#pragma unroll 4
+  for (int s = 0; s < S; ++s) {
+    const float m = a.part_ml[(base + (long)s * R) * 2];
+    const float w = m == -INFINITY ? 0.f : __expf(m - M);
+    const float* src = a.part_o + (base + (long)s * R) * a.dh + lane * VPL;
+    if (VPL == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] += w * v.x; acc[VPL > 1 ? 1 : 0] += w * v.y;
+      acc[VPL > 2 ? 2 : 0] += w * v.z; acc[VPL > 3 ? 3 : 0] += w * v.w;
+    } else if (VPL == 2) {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] += w * v.x; acc[VPL > 1 ? 1 : 0] += w * v.y;
+    } else {
+      acc[0] += w * src[0];
     }
-    const float y = Lsum > 0.f ? acc / Lsum : 0.f;
-    a.o[orow * a.dh + i] = y;
-    if (a.o_hi) split_hi_lo(y, a.o_hi[orow * a.dh + i], a.o_lo[orow * a.dh + i]);
+  }
+  const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+  const int n = r / a.G, hq = g * a.G + r % a.G;
+  const long o0 = (((long)b * a.n1 + n) * a.Hq + hq) * a.dh + lane * VPL;
+#pragma unroll
+  for (int c = 0; c < VPL; ++c) {
+    const float y = Lsum > 0.f ? acc[c] * inv : 0.f;
+    a.o[o0 + c] = y;
+    if (a.o_hi) split_hi_lo(y, a.o_hi[o0 + c], a.o_lo[o0 + c]);
   }
 }
 
@@ -184,8 +211,13 @@ static cudaError_t attn_go(const AttnArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st) {
-  dim3 g2(a.n1 * a.G, a.Hkv, a.B);
-  attn_combine_kernel<<<g2, a.dh, 0, st>>>(a);
+  const long rows = (long)a.B * a.Hkv * a.n1 * a.G;
+  const int blocks = (int)((rows + 7) / 8);           // 8 warps per CTA, one row each
+  switch (a.dh) {
+    case 32: attn_combine_kernel<1><<<blocks, 256, 0, st>>>(a); break;
+    case 64: attn_combine_kernel<2><<<blocks, 256, 0, st>>>(a); break;
+    default: attn_combine_kernel<4><<<blocks, 256, 0, st>>>(a); break;
+  }
   return cudaGetLastError();
 }
 

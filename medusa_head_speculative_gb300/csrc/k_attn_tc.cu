@@ -4,16 +4,23 @@
 // ("Medusa: Simple LLM Inference Acceleration Framework with Multiple Decoding Heads"
 // §3.4 Tree Attention, Steps 3 and 5): CTA (split, kv head g, sequence b, row block) covers
 // one chunk of the prefix, or (split == nsplit) the tree keys under the ancestor bitmask,
-// for 128 query rows (node, query head of the group).  Inside the CTA the keys are walked
-// in 64-key chunks:
-//   warp 4 (one lane)  TMA: Q once, then K and V chunks through a 3-stage mbarrier ring
+// for up to two 128-row query tiles (row = node x query head of the group) that share every
+// K/V tile, so up to 256 rows read the prefix once.  Inside the CTA the keys are walked in
+// 64-key chunks:
+//   warp 8 (one lane)  TMA: Q once, then K and V chunks through a 3-stage mbarrier ring
 //                      (paged caches: one box per page)
-//   warp 5 (one lane)  MMAs: S = Q K^T into one of two TMEM buffers (issued one chunk
-//                      ahead), then O = P V with V as an MN-major operand
-//   warps 0-3          one query row per thread: masked online softmax of S, P written as
-//                      bf16 into swizzled shared memory, O accumulated in registers
-// Each CTA writes one unnormalised partial (o, max, sum) per row, merged by
-// attn_combine_kernel.  Every wait is bounded; on expiry MEDUSA_FLAG_TIMEOUT is set.
+//   warp 9 (one lane)  MMAs: S = Q K^T into one of two TMEM buffers per tile (issued one
+//                      chunk ahead), then O += P V into the tile's TMEM accumulator, V as
+//                      an MN-major operand
+//   warps 0-7          one query row per thread (warps 4t..4t+3 for tile t): masked online
+//                      softmax of S in base 2, P written as bf16 into one of two swizzled
+//                      shared-memory buffers
+// The running maximum is raised lazily: only when a row's new maximum exceeds the one its
+// P values are taken against by more than 2^8 does the warp wait for the previous P V and
+// rescale O in TMEM; otherwise P is formed against the old maximum (values <= 256) and O
+// keeps accumulating in the tensor cores.  Each CTA writes one unnormalised partial
+// (o, max, sum) per row, merged by attn_combine_kernel.  Every wait is bounded; on expiry
+// MEDUSA_FLAG_TIMEOUT is set.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -26,10 +33,13 @@
 
 namespace medusa {
 
-constexpr int AT_ROWS = 128;      // query rows per CTA (MMA M, TMEM lanes)
+constexpr int AT_ROWS = 128;      // query rows per tile (MMA M, TMEM lanes)
+constexpr int AT_TILES = 2;       // query tiles per CTA at most
 constexpr int AT_KEYS = 64;       // keys per chunk (S columns, PV reduction)
 constexpr int AT_STAGES = 3;      // K/V ring depth
-constexpr uint32_t AT_TMEM_COLS = 256;   // S0 [0,64), S1 [64,128), O [128, 128+dh)
+constexpr int AT_WARPS = 4 * AT_TILES + 2;
+constexpr uint32_t AT_TILE_COLS = 256;   // per tile: S0 [0,64), S1 [64,128), O [128, 128+dh)
+constexpr float AT_LAZY = 8.f;           // log2 headroom before O is rescaled
 
 struct AttnTcArgs {
   CUtensorMap tq;        // q bf16:    dims {dh, Hq, B*n1},   box {64, G, 128/G}
@@ -37,17 +47,32 @@ struct AttnTcArgs {
   CUtensorMap ttk, ttv;  // tree K/V:  dims {dh, Hkv, B*n1},  box {64, 1, 64}
   AttnArgs a;
   int kbox;              // cache rows per TMA box: 64 (contiguous) or the page size
+  int nt;                // query tiles per CTA: rows_per_block / 128
 };
 
-enum { BQ = 0, BKVF = 1, BKVE = BKVF + AT_STAGES, BSF = BKVE + AT_STAGES, BOF = BSF + 2, BPR = BOF + 1,
-       BCOUNT = BPR + 1 };
+// Barriers: Q loaded; K/V stage full / empty; per tile and buffer: S written (BSF), P V
+// done (BOF), P written (BPR).  One P-written barrier per P buffer: the softmax warps can
+// finish chunk i + 1 before the MMA thread has waited for chunk i, but never chunk i + 2
+// (that needs the P V of chunk i), so no barrier runs two phases ahead of its waiter.
+enum {
+  BQ = 0, BKVF = 1, BKVE = BKVF + AT_STAGES, BSF = BKVE + AT_STAGES,
+  BOF = BSF + 2 * AT_TILES, BPR = BOF + 2 * AT_TILES, BCOUNT = BPR + 2 * AT_TILES
+};
+
+// A bounded wait whose outcome is the same in every lane (the TMEM accesses that follow
+// are warp-collective).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, TC_TIMEOUT_NS));
+}
 
 template <int DH>
-__global__ void __launch_bounds__(192, 1) tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
+__global__ void __launch_bounds__(AT_WARPS * 32, 1)
+tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
   constexpr int H = DH / 64;                        // 64-column halves of a head
-  constexpr uint32_t QH = AT_ROWS * 128;            // one half of Q: 16 KB
+  constexpr uint32_t QH = AT_ROWS * 128;            // one half of a Q tile: 16 KB
   constexpr uint32_t KVH = AT_KEYS * 128;           // one half of a 64-key K or V tile: 8 KB
   constexpr uint32_t KV_STAGE = 2 * H * KVH;
+  constexpr uint32_t PT = AT_ROWS * 128;            // one P buffer: 128 rows x 64 keys bf16
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[BCOUNT];
   __shared__ uint32_t tmem_slot;
@@ -56,8 +81,9 @@ __global__ void __launch_bounds__(192, 1) tree_attn_tc_kernel(const __grid_const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, gk = blockIdx.y;
   const int b = blockIdx.z / a.nrb, rb = blockIdx.z % a.nrb;
-  const int G = a.G, R = a.n1 * G;
-  const int row0 = rb * AT_ROWS, node0 = row0 / G;
+  const int G = a.G, R = a.n1 * G, nt = g.nt;
+  const int row0 = rb * AT_ROWS * nt;
+  const int nta = min(nt, (R - row0 + AT_ROWS - 1) / AT_ROWS);   // tiles with rows
   const bool tree = split == a.nsplit;
   int L = a.len[b];
   L = L < 0 ? 0 : (L > a.capacity ? a.capacity : L);
@@ -66,8 +92,9 @@ __global__ void __launch_bounds__(192, 1) tree_attn_tc_kernel(const __grid_const
   const int nch = kend > kbeg ? (kend - kbeg + AT_KEYS - 1) / AT_KEYS : 0;
   const uint32_t sraw = smem_u32(smem_raw);
   const uint32_t base = (sraw + 1023u) & ~1023u;
-  const uint32_t qs = base, kv0 = base + H * QH, ps = kv0 + AT_STAGES * KV_STAGE;
+  const uint32_t qs = base, kv0 = base + nt * H * QH, ps = kv0 + AT_STAGES * KV_STAGE;
   const uint32_t bar0 = smem_u32(bars);
+  const uint32_t tmem_cols = AT_TILE_COLS * nt;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
   if (tid == 0) {
@@ -76,30 +103,34 @@ __global__ void __launch_bounds__(192, 1) tree_attn_tc_kernel(const __grid_const
       mbar_init(bar(BKVF + i), 1);
       mbar_init(bar(BKVE + i), 1);
     }
-    mbar_init(bar(BSF), 1);
-    mbar_init(bar(BSF + 1), 1);
-    mbar_init(bar(BOF), 1);
-    mbar_init(bar(BPR), AT_ROWS);
+    for (int i = 0; i < 2 * AT_TILES; ++i) {
+      mbar_init(bar(BSF + i), 1);
+      mbar_init(bar(BOF + i), 1);
+      mbar_init(bar(BPR + i), AT_ROWS);
+    }
     s_issued = 0;
     s_waited = 0;
     s_qok = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 5) tmem_alloc(smem_u32(&tmem_slot), AT_TMEM_COLS);
+  if (warp == 9) tmem_alloc(smem_u32(&tmem_slot), tmem_cols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   bool timed_out = false;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && nch > 0) {
       const uint64_t pol_kv = policy_evict_first(), pol_q = policy_evict_last();
-      mbar_expect_tx(bar(BQ), H * QH);
+      mbar_expect_tx(bar(BQ), nta * H * QH);
+      for (int t = 0; t < nta; ++t) {
+        const int node0 = (row0 + t * AT_ROWS) / G;
 #pragma unroll
-      for (int h = 0; h < H; ++h)
-        tma_load_3d(qs + h * QH, &g.tq, h * 64, gk * G, b * a.n1 + node0, bar(BQ), pol_q);
+        for (int h = 0; h < H; ++h)
+          tma_load_3d(qs + (t * H + h) * QH, &g.tq, h * 64, gk * G, b * a.n1 + node0, bar(BQ), pol_q);
+      }
       int i = 0;
       for (; i < nch; ++i) {
         const int st = i % AT_STAGES;
@@ -143,7 +174,7 @@ __global__ void __launch_bounds__(192, 1) tree_attn_tc_kernel(const __grid_const
       }
       s_issued = i;
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && nch > 0) {
       int waited = 0;
@@ -158,65 +189,54 @@ __global__ void __launch_bounds__(192, 1) tree_attn_tc_kernel(const __grid_const
           if (!mbar_wait(bar(BKVF + st), (i / AT_STAGES) & 1, TC_TIMEOUT_NS)) return false;
           waited = i + 1;
           tc_fence_after();
-          const uint32_t ks = kv0 + st * KV_STAGE, d = tmem + (uint32_t)(i & 1) * AT_KEYS;
+          const uint32_t ks = kv0 + st * KV_STAGE;
+          for (int t = 0; t < nta; ++t) {
+            const uint32_t d = tmem + t * AT_TILE_COLS + (uint32_t)(i & 1) * AT_KEYS;
 #pragma unroll
-          for (int h = 0; h < H; ++h)
+            for (int h = 0; h < H; ++h)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(d, sw128_desc(qs + h * QH) + 2 * kk, sw128_desc(ks + h * KVH) + 2 * kk, id_qk,
-                        (h | kk) != 0);
-          umma_commit(bar(BSF + (i & 1)));
+              for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(d, sw128_desc(qs + (t * H + h) * QH) + 2 * kk,
+                          sw128_desc(ks + h * KVH) + 2 * kk, id_qk, (h | kk) != 0);
+            umma_commit(bar(BSF + 2 * t + (i & 1)));
+          }
           return true;
         };
         if (!issue_qk(0)) timed_out = true;
         for (int i = 0; i < nch && !timed_out; ++i) {
           if (i + 1 < nch && !issue_qk(i + 1)) { timed_out = true; break; }
-          if (!mbar_wait(bar(BPR), i & 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
-          tc_fence_after();
           const uint32_t vs = kv0 + (i % AT_STAGES) * KV_STAGE + H * KVH;
+          for (int t = 0; t < nta && !timed_out; ++t) {
+            if (!mbar_wait(bar(BPR + 2 * t + (i & 1)), (i >> 1) & 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+            tc_fence_after();
+            const uint32_t pt = ps + (uint32_t)(2 * t + (i & 1)) * PT;
 #pragma unroll
-          for (int kk = 0; kk < AT_KEYS / 16; ++kk)
-            umma_bf16(tmem + 128, sw128_desc(ps) + 2 * kk, sw128_desc_mn(vs + kk * 2048, KVH), id_pv,
-                      kk != 0);
-          umma_commit(bar(BOF));
+            for (int kk = 0; kk < AT_KEYS / 16; ++kk)
+              umma_bf16(tmem + t * AT_TILE_COLS + 128, sw128_desc(pt) + 2 * kk,
+                        sw128_desc_mn(vs + kk * 2048, KVH), id_pv, (i | kk) != 0);
+            umma_commit(bar(BOF + 2 * t + (i & 1)));
+          }
+          if (timed_out) break;
           umma_commit(bar(BKVE + i % AT_STAGES));
         }
       }
       s_waited = waited;
     }
-  } else {
+  } else if (warp < 4 * nta) {
     // ------------------------------------------------------------ softmax rows
-    const int gr = row0 + tid;
+    const int t = warp >> 2, wl = warp & 3;
+    const int r = wl * 32 + lane;                   // row within the tile = TMEM lane
+    const int gr = row0 + t * AT_ROWS + r;
     const int node = gr / G;
     const bool row_ok = gr < R;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    uint8_t* pgen = smem_raw + (ps - sraw);
-    float o_acc[DH];
-#pragma unroll
-    for (int c = 0; c < DH; ++c) o_acc[c] = 0.f;
-    float m_acc = -INFINITY, l_acc = 0.f, m_run = -INFINITY, m_prev = -INFINITY, l_prev = 0.f;
-
-    auto accumulate = [&](int j) -> bool {     // fold chunk j's P V into o_acc
-      if (!mbar_wait(bar(BOF), j & 1, TC_TIMEOUT_NS)) return false;
-      tc_fence_after();
-      __syncwarp();
-      const float sc = m_acc == -INFINITY ? 0.f : __expf(m_acc - m_prev);
-#pragma unroll
-      for (int c = 0; c < DH; c += 16) {
-        float v[16];
-        tmem_ld16(lane_base + 128 + c, v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) o_acc[c + e] = o_acc[c + e] * sc + v[e];
-      }
-      l_acc = l_acc * sc + l_prev;
-      m_acc = m_prev;
-      return true;
-    };
+    const uint32_t lane_base = tmem + t * AT_TILE_COLS + ((uint32_t)(wl * 32) << 16);
+    uint8_t* pgen = smem_raw + (ps - sraw) + (size_t)(2 * t) * PT;
+    const float sl2 = a.scale * 1.4426950408889634f;      // scores in base-2 units
+    float m_use = -INFINITY, l_acc = 0.f;
 
     for (int i = 0; i < nch; ++i) {
-      if (!mbar_wait(bar(BSF + (i & 1)), (i >> 1) & 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+      if (!warp_wait(bar(BSF + 2 * t + (i & 1)), (i >> 1) & 1)) { timed_out = true; break; }
       tc_fence_after();
-      __syncwarp();
       float s[AT_KEYS];
 #pragma unroll
       for (int c = 0; c < AT_KEYS; c += 16) {
@@ -236,19 +256,41 @@ __global__ void __launch_bounds__(192, 1) tree_attn_tc_kernel(const __grid_const
       for (int j = 0; j < AT_KEYS; ++j) {
         const bool bit = ((j < 32 ? w0 : w1) >> (j & 31)) & 1u;
         const bool valid = (t0 + j < kend) && bit;
-        s[j] = valid ? s[j] * a.scale : -INFINITY;
+        s[j] = valid ? s[j] * sl2 : -INFINITY;
         mx = fmaxf(mx, s[j]);
       }
-      const float m_new = fmaxf(m_run, mx);
+      // this chunk's P buffer was last read by the P V of chunk i - 2
+      if (i >= 2 && !warp_wait(bar(BOF + 2 * t + (i & 1)), ((i - 2) >> 1) & 1)) { timed_out = true; break; }
+      const bool raise = m_use != -INFINITY && mx > m_use + AT_LAZY;
+      if (__any_sync(0xffffffffu, raise)) {
+        // O must hold the P V of chunk i - 1 before it is rescaled
+        if (!warp_wait(bar(BOF + 2 * t + ((i - 1) & 1)), ((i - 1) >> 1) & 1)) { timed_out = true; break; }
+        tc_fence_after();
+        const float f = raise ? ex2_approx(m_use - mx) : 1.f;
+#pragma unroll
+        for (int c = 0; c < DH; c += 16) {
+          float v[16];
+          tmem_ld16(lane_base + 128 + c, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] *= f;
+          tmem_st16(lane_base + 128 + c, v);
+        }
+        if (raise) {
+          l_acc *= f;
+          m_use = mx;
+        }
+      }
+      if (m_use == -INFINITY) m_use = mx;             // first keys of this row
       float lsum = 0.f;
 #pragma unroll
       for (int j = 0; j < AT_KEYS; ++j) {
-        const float p = s[j] == -INFINITY ? 0.f : __expf(s[j] - m_new);
+        const float p = s[j] == -INFINITY ? 0.f : ex2_approx(s[j] - m_use);
         s[j] = p;
         lsum += p;
       }
-      if (i > 0 && !accumulate(i - 1)) { timed_out = true; break; }
+      l_acc += lsum;
       // P row (bf16) into the 128-byte-swizzled K-major tile the PV MMA reads
+      uint8_t* prow = pgen + (size_t)(i & 1) * PT + r * 128;
 #pragma unroll
       for (int c = 0; c < AT_KEYS / 8; ++c) {
         uint4 u;
@@ -260,22 +302,35 @@ __global__ void __launch_bounds__(192, 1) tree_attn_tc_kernel(const __grid_const
         u.y = *reinterpret_cast<uint32_t*>(&p1);
         u.z = *reinterpret_cast<uint32_t*>(&p2);
         u.w = *reinterpret_cast<uint32_t*>(&p3);
-        *reinterpret_cast<uint4*>(pgen + tid * 128 + ((c ^ (tid & 7)) << 4)) = u;
+        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = u;
       }
       fence_proxy_async();
       tc_fence_before();
-      mbar_arrive(bar(BPR));
-      m_prev = m_new;
-      l_prev = lsum;
-      m_run = m_new;
+      mbar_arrive(bar(BPR + 2 * t + (i & 1)));
     }
-    if (!timed_out && nch > 0 && !accumulate(nch - 1)) timed_out = true;
+    float o[DH];
+#pragma unroll
+    for (int c = 0; c < DH; ++c) o[c] = 0.f;
+    if (!timed_out && nch > 0) {
+      if (!warp_wait(bar(BOF + 2 * t + ((nch - 1) & 1)), ((nch - 1) >> 1) & 1)) {
+        timed_out = true;
+      } else {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < DH; c += 16) {
+          float v[16];
+          tmem_ld16(lane_base + 128 + c, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[c + e] = v[e];
+        }
+      }
+    }
     if (row_ok) {
       const long pr = (((long)b * a.Hkv + gk) * (a.nsplit + 1) + split) * R + gr;
       float4* dst = reinterpret_cast<float4*>(a.part_o + pr * DH);
 #pragma unroll
-      for (int c = 0; c < DH; c += 4) dst[c / 4] = make_float4(o_acc[c], o_acc[c + 1], o_acc[c + 2], o_acc[c + 3]);
-      a.part_ml[pr * 2] = m_acc;
+      for (int c = 0; c < DH; c += 4) dst[c / 4] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+      a.part_ml[pr * 2] = m_use * 0.6931471805599453f;     // back to natural-log units
       a.part_ml[pr * 2 + 1] = l_acc;
     }
   }
@@ -288,7 +343,7 @@ __global__ void __launch_bounds__(192, 1) tree_attn_tc_kernel(const __grid_const
       mbar_wait(bar(BKVF + i % AT_STAGES), (i / AT_STAGES) & 1, TC_TIMEOUT_NS / 16);
   }
   __syncthreads();
-  if (warp == 5) tmem_dealloc(tmem, AT_TMEM_COLS);
+  if (warp == 9) tmem_dealloc(tmem, tmem_cols);
 }
 
 // ------------------------------------------------------------------ host side
@@ -347,14 +402,16 @@ cudaError_t launch_tree_attention_tc(const AttnArgs& a, const void* q_bf16, cuda
   }
   if (!make_map3(&g.ttk, a.tk, a.dh, a.Hkv, nodes, 1, AT_KEYS)) return cudaErrorInvalidValue;
   if (!make_map3(&g.ttv, a.tv, a.dh, a.Hkv, nodes, 1, AT_KEYS)) return cudaErrorInvalidValue;
+  if (a.rows_per_block != AT_ROWS && a.rows_per_block != AT_ROWS * AT_TILES) return cudaErrorInvalidValue;
+  g.nt = a.rows_per_block / AT_ROWS;
   const int H = a.dh / 64;
-  const size_t smem = 1024 + (size_t)H * AT_ROWS * 128 + (size_t)AT_STAGES * 2 * H * AT_KEYS * 128 +
-                      (size_t)AT_ROWS * 128;
+  const size_t smem = 1024 + (size_t)g.nt * H * AT_ROWS * 128 +
+                      (size_t)AT_STAGES * 2 * H * AT_KEYS * 128 + (size_t)g.nt * 2 * AT_ROWS * 128;
   auto kern = a.dh == 128 ? tree_attn_tc_kernel<128> : tree_attn_tc_kernel<64>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.nsplit + 1, a.Hkv, a.B * a.nrb);
-  kern<<<grid, 192, smem, st>>>(g);
+  kern<<<grid, AT_WARPS * 32, smem, st>>>(g);
   return cudaGetLastError();
 }
 
