@@ -170,6 +170,157 @@ __global__ void __launch_bounds__(128, 2) umma_gemm_kernel(const __grid_constant
   if (warp == 1) tmem_dealloc(tmem, g.tmem_cols);
 }
 
+// ------------------------------------------------------------------ wide variant
+// For hundreds to thousands of activation rows (the node projections at batch > 1) the
+// 128 x nbox tiles above re-read their operands from L2 faster than the tensor cores use
+// them.  Here a CTA owns 256 weight rows (two 128-row accumulators in TMEM) against up to
+// 256 activation rows, and the two CTAs of a cluster (consecutive weight tiles, the same
+// activation rows) split each activation tile: each loads half and multicasts it to both.
+// Per stage a CTA then reads 32 KB of weights and half of the activation bytes for twice
+// the MMA work of a 128-row tile.  The stage ring is shared across the pair: a stage is
+// refilled only after both CTAs' MMAs have read it (each MMA thread's commit arrives on
+// the empty barriers of both CTAs).
+constexpr int UW_R = 256;                    // weight rows per CTA
+constexpr uint32_t UW_W_BYTES = UW_R * 128;  // one 64-column stage of them
+constexpr uint16_t UW_PAIR = 0x3;            // both CTAs of the cluster
+
+struct UmmaWideArgs {
+  CUtensorMap tw[kMaxSeg];   // weights of each segment: dims {k, rows}, box {64, 256}
+  CUtensorMap ta, tl;        // activations (hi, lo), shared by all segments: box {64, nbox/2}
+  MatArgs m;                 // tile_off counts 256-row tiles
+  int wtiles;                // weight tiles; grid.y is this rounded up to even
+  int nbox, stages, ksplit;
+  float* kpart;
+  uint32_t tmem_cols, acc_stride;
+  uint32_t* status;
+};
+
+template <bool HAS_LO>
+__global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant__ UmmaWideArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bars[2 * 8 + 1];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int s_issued, s_consumed;
+  const MatArgs& a = g.m;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank();
+  const bool has_w = (int)blockIdx.y < g.wtiles;
+  int si = 0;
+  while (has_w && si + 1 < a.nseg && (int)blockIdx.y >= a.tile_off[si + 1]) ++si;
+  const MatSeg& s = a.seg[si];
+  const int rbase = has_w ? ((int)blockIdx.y - a.tile_off[si]) * UW_R : 0;
+  const int rows_here = has_w ? min(UW_R, s.rows - rbase) : 0;
+  const int nacc = rows_here > 128 ? 2 : (rows_here > 0 ? 1 : 0);
+  const int m0 = (int)blockIdx.x * g.nbox, half = g.nbox / 2;
+  const int nk = (a.k + UM_K - 1) / UM_K;
+  const int kt0 = (int)((long)blockIdx.z * nk / g.ksplit);
+  const int nkl = (int)((long)(blockIdx.z + 1) * nk / g.ksplit) - kt0;
+  const int S = g.stages;
+  const uint32_t A_BYTES = (uint32_t)g.nbox * 128;
+  const uint32_t STAGE = UW_W_BYTES + A_BYTES * (HAS_LO ? 2 : 1);
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int i) { return bar0 + 8u * i; };
+  auto empty = [&](int i) { return bar0 + 8u * (8 + i); };
+  const uint32_t accb = bar0 + 8u * 16;
+
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full(i), 1);
+      mbar_init(empty(i), 2);                           // one commit from each CTA's MMA
+    }
+    mbar_init(accb, 1);
+    s_issued = 0;
+    s_consumed = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), g.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();                       // the peer's barriers exist before any copy or arrive
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  bool timed_out = false;
+
+  if (warp == 0 && lane == 0) {                         // ---- TMA producer
+    const uint64_t pw = policy_evict_first(), pa = policy_evict_last();
+    int j = 0;
+    for (; j < nkl; ++j) {
+      const int st = j % S, kx = (kt0 + j) * UM_K;
+      if (!mbar_wait(empty(st), ((j / S) & 1) ^ 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+      mbar_expect_tx(full(st), (has_w ? UW_W_BYTES : 0u) + A_BYTES * (HAS_LO ? 2 : 1));
+      const uint32_t ws = base + st * STAGE;
+      if (has_w) tma_load_2d(ws, &g.tw[si], kx, rbase, full(st), pw);
+      const uint32_t off = UW_W_BYTES + rank * (uint32_t)half * 128;
+      tma_load_2d_mc(ws + off, &g.ta, kx, m0 + (int)rank * half, full(st), UW_PAIR, pa);
+      if (HAS_LO) tma_load_2d_mc(ws + off + A_BYTES, &g.tl, kx, m0 + (int)rank * half, full(st), UW_PAIR, pa);
+    }
+    s_issued = j;
+  } else if (warp == 1 && lane == 0) {                  // ---- MMA issuer
+    const uint32_t idesc = idesc_bf16(128, g.nbox);
+    int j = 0;
+    for (; j < nkl; ++j) {
+      const int st = j % S;
+      if (!mbar_wait(full(st), (j / S) & 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+      tc_fence_after();
+      const uint32_t ws = base + st * STAGE;
+      const uint64_t bd = sw128_desc(ws + UW_W_BYTES), ld = sw128_desc(ws + UW_W_BYTES + A_BYTES);
+      for (int t = 0; t < nacc; ++t) {
+        const uint64_t ad = sw128_desc(ws + t * UM_W_BYTES);
+        const uint32_t d = tmem + t * g.acc_stride;
+#pragma unroll
+        for (int ks = 0; ks < UM_K / 16; ++ks) {
+          umma_bf16(d, ad + 2 * ks, bd + 2 * ks, idesc, (j | ks) != 0);
+          if (HAS_LO) umma_bf16(d, ad + 2 * ks, ld + 2 * ks, idesc, 1);
+        }
+      }
+      umma_commit_mc(empty(st), UW_PAIR);               // frees the stage in both CTAs
+    }
+    s_consumed = j;
+    umma_commit(accb);
+  }
+  __syncwarp();
+  const bool acc_ok = mbar_wait(accb, 0, TC_TIMEOUT_NS);
+  tc_fence_after();
+  __syncwarp();
+  if (acc_ok && nkl > 0) {
+    for (int t = 0; t < nacc; ++t) {
+      const int r = rbase + t * 128 + warp * 32 + lane;
+      for (int c0 = 0; c0 < g.nbox; c0 += 16) {
+        float v[16];
+        tmem_ld16(tmem + t * g.acc_stride + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+        if (r < s.rows) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = m0 + c0 + j;
+            if (m >= a.M) continue;
+            if (g.ksplit > 1)
+              g.kpart[((long)blockIdx.z * a.M + m) * a.ldo + s.out_off + r] = v[j];
+            else
+              umma_epilogue(a, s, m, r, v[j]);
+          }
+        }
+      }
+    }
+  }
+  if (timed_out || !acc_ok) set_flag(g.status, MEDUSA_FLAG_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    // copies issued but not consumed (bounded), then the last use of every stage: both
+    // CTAs' commits must have landed on this CTA's empty barriers before it may exit
+    for (int j = s_consumed; j < s_issued; ++j)
+      mbar_wait(full(j % S), (j / S) & 1, TC_TIMEOUT_NS / 16);
+    for (int st = 0; st < S && st < nkl; ++st) {
+      const int uses = (nkl - st + S - 1) / S;
+      mbar_wait(empty(st), (uses - 1) & 1, TC_TIMEOUT_NS / 16);
+    }
+  }
+  __syncthreads();
+  cluster_sync();                       // nothing more arrives from the peer after this
+  if (warp == 1) tmem_dealloc(tmem, g.tmem_cols);
+}
+
 // Sum of the K-range partials for 4 consecutive output columns per thread (all loads issued
 // before the epilogue's stores), then the epilogue (single-segment launches) or a plain
 // store (multi-segment EPI_STORE launches).  cols % 4 == 0.
@@ -229,6 +380,87 @@ static bool make_map(CUtensorMap* map, const void* ptr, long cols, long rows, lo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+static cudaError_t launch_splitk_reduce(const MatArgs& a, int ksplit, cudaStream_t st) {
+  const int ncols = a.nseg == 1 ? a.seg[0].rows : (int)a.ldo;
+  const long n4 = (long)a.M * (ncols / 4);
+  const long blocks = (n4 + 255) / 256;
+  splitk_reduce_kernel<<<(int)(blocks < 8192 ? blocks : 8192), 256, 0, st>>>(a, a.kpart, ksplit, ncols);
+  return cudaGetLastError();
+}
+
+// K ranges for a launch of `ctas` CTAs that leaves SMs idle (single-segment launches, or
+// plain stores): about two CTAs per SM, at least 4 K blocks each, partials within kpart.
+static int choose_ksplit(const MatArgs& a, long ctas, int nk, int num_sms) {
+  const bool splittable = a.nseg == 1 || (a.epi == EPI_STORE && !a.out_hi);
+  if (!splittable || !a.kpart || ctas >= num_sms || (a.nseg == 1 ? a.seg[0].rows : a.ldo) % 4 != 0)
+    return 1;
+  int ksplit = (int)(2L * num_sms / ctas);
+  ksplit = ksplit > 8 ? 8 : ksplit;
+  ksplit = ksplit > nk / 4 ? nk / 4 : ksplit;
+  while (ksplit > 1 && (size_t)ksplit * a.M * a.ldo * sizeof(float) > a.kpart_bytes) --ksplit;
+  return ksplit < 1 ? 1 : ksplit;
+}
+
+static cudaError_t launch_umma_wide(const MatArgs& m, uint32_t* status, int num_sms, cudaStream_t st) {
+  static UmmaWideArgs g;
+  std::memset(&g, 0, sizeof(g));
+  g.m = m;
+  MatArgs& a = g.m;
+  a.tile_off[0] = 0;
+  for (int i = 0; i < a.nseg; ++i) a.tile_off[i + 1] = a.tile_off[i] + (a.seg[i].rows + UW_R - 1) / UW_R;
+  g.wtiles = a.tile_off[a.nseg];
+  const bool has_lo = a.seg[0].a_lo != nullptr;
+  // activation tiles of <= 256 rows, as even as the count allows (multiple of 16)
+  const int nct = (a.M + 255) / 256;
+  g.nbox = ((a.M + nct - 1) / nct + 15) / 16 * 16;
+  g.acc_stride = g.nbox > 128 ? 256 : 128;            // two accumulators of nbox columns
+  g.tmem_cols = 2 * g.acc_stride;
+  const uint32_t stage = UW_W_BYTES + (uint32_t)g.nbox * 128 * (has_lo ? 2 : 1);
+  int stages = (int)((220u * 1024u) / stage);
+  g.stages = stages > 6 ? 6 : stages;
+  if (g.stages < 2) return cudaErrorInvalidValue;
+  g.status = status;
+  const int nk = (a.k + UM_K - 1) / UM_K;
+  const int ytiles = (g.wtiles + 1) / 2 * 2;
+  g.ksplit = choose_ksplit(a, (long)nct * ytiles, nk, num_sms);
+  g.kpart = a.kpart;
+  for (int i = 0; i < a.nseg; ++i)
+    if (!make_map(&g.tw[i], a.seg[i].w, a.k, a.seg[i].rows, a.k, UW_R)) return cudaErrorInvalidValue;
+  if (!make_map(&g.ta, a.seg[0].a_hi, a.k, a.M, a.seg[0].ldx, g.nbox / 2)) return cudaErrorInvalidValue;
+  if (has_lo && !make_map(&g.tl, a.seg[0].a_lo, a.k, a.M, a.seg[0].ldx, g.nbox / 2)) return cudaErrorInvalidValue;
+  // at least 116 KB of shared memory keeps one CTA per SM, so the 512-column TMEM
+  // allocations of co-scheduled clusters never wait on each other
+  size_t smem = (size_t)g.stages * stage + 1024;
+  if (smem < 116u * 1024u) smem = 116u * 1024u;
+  auto kern = has_lo ? umma_wide_kernel<true> : umma_wide_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(nct, ytiles, g.ksplit);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 2;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, g);
+  if (e != cudaSuccess || g.ksplit == 1) return e;
+  return launch_splitk_reduce(a, g.ksplit, st);
+}
+
+// The wide variant needs every segment to read the same activations (one shared tile).
+static bool shared_activations(const MatArgs& a) {
+  for (int i = 1; i < a.nseg; ++i)
+    if (a.seg[i].a_hi != a.seg[0].a_hi || a.seg[i].a_lo != a.seg[0].a_lo || a.seg[i].ldx != a.seg[0].ldx)
+      return false;
+  return true;
+}
+
 cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st) {
   static UmmaArgs g;                      // ~4.5 KB: keep it off the host stack
   static std::mutex mu;
@@ -240,14 +472,19 @@ cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st
         cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       num_sms = 148;
   }
+  {
+    bool lo_ok = true;
+    for (int i = 1; i < m.nseg; ++i)
+      if ((m.seg[i].a_lo != nullptr) != (m.seg[0].a_lo != nullptr)) lo_ok = false;
+    if (!lo_ok) return cudaErrorInvalidValue;
+    if (m.M > 128 && shared_activations(m)) return launch_umma_wide(m, status, num_sms, st);
+  }
   std::memset(&g, 0, sizeof(g));
   g.m = m;
   MatArgs& a = g.m;
   a.tile_off[0] = 0;
   for (int i = 0; i < a.nseg; ++i) a.tile_off[i + 1] = a.tile_off[i] + (a.seg[i].rows + UM_R - 1) / UM_R;
   const bool has_lo = a.seg[0].a_lo != nullptr;
-  for (int i = 1; i < a.nseg; ++i)
-    if ((a.seg[i].a_lo != nullptr) != has_lo) return cudaErrorInvalidValue;
   int nbox = (a.M + 15) / 16 * 16;
   const int cap = has_lo ? 128 : 256;
   nbox = nbox > cap ? cap : nbox;
@@ -262,19 +499,10 @@ cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st
   g.stages = stages > 8 ? 8 : stages;
   if (g.stages < 2) return cudaErrorInvalidValue;
   g.status = status;
-  // split K when the tiles alone cannot cover the SMs (single-segment launches)
+  // split K when the tiles alone cannot cover the SMs
   const int nk = (a.k + UM_K - 1) / UM_K;
   const int mchunks = (a.M + nbox - 1) / nbox;
-  const long ctas = (long)mchunks * a.tile_off[a.nseg];
-  int ksplit = 1;
-  const bool splittable = a.nseg == 1 || (a.epi == EPI_STORE && !a.out_hi);
-  if (splittable && a.kpart && ctas < num_sms && (a.nseg == 1 ? a.seg[0].rows : a.ldo) % 4 == 0) {
-    ksplit = (int)(2L * num_sms / ctas);
-    ksplit = ksplit > 8 ? 8 : ksplit;
-    ksplit = ksplit > nk / 4 ? nk / 4 : ksplit;
-    while (ksplit > 1 && (size_t)ksplit * a.M * a.ldo * sizeof(float) > a.kpart_bytes) --ksplit;
-    ksplit = ksplit < 1 ? 1 : ksplit;
-  }
+  const int ksplit = choose_ksplit(a, (long)mchunks * a.tile_off[a.nseg], nk, num_sms);
   g.ksplit = ksplit;
   g.kpart = a.kpart;
   for (int i = 0; i < a.nseg; ++i) {
@@ -291,11 +519,7 @@ cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st
   kern<<<grid, 128, smem, st>>>(g);
   e = cudaGetLastError();
   if (e != cudaSuccess || ksplit == 1) return e;
-  const int ncols = a.nseg == 1 ? a.seg[0].rows : (int)a.ldo;
-  const long n4 = (long)a.M * (ncols / 4);
-  const long blocks = (n4 + 255) / 256;
-  splitk_reduce_kernel<<<(int)(blocks < 8192 ? blocks : 8192), 256, 0, st>>>(a, a.kpart, ksplit, ncols);
-  return cudaGetLastError();
+  return launch_splitk_reduce(a, ksplit, st);
 }
 
 }  // namespace medusa
