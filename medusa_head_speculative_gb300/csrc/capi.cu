@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <queue>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -637,19 +638,38 @@ medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec
   const int max_splits = std::max(1, (dims->capacity + gran - 1) / gran);
   p->nsplit = std::min(want, max_splits);
   if (p->tc_attn) {
-    // One resident CTA per SM.  Cost in key-loads of one SM: the busiest SM's keys (the
-    // work spread over the SMs, but no less than one CTA's chunk; each CTA also pays a
-    // fixed start-up of about three chunks), plus the partials that the splits write and
-    // the combine reads back, in the same units.
+    // One resident CTA per SM.  Cost in key-loads of one SM: the busiest SM's keys (each
+    // CTA also pays a fixed start-up of about three chunks), plus the partials that the
+    // splits write and the combine reads back, in the same units.  The busiest SM comes
+    // from assigning the CTAs, in launch order, to the SM that frees first; for grids of
+    // many rounds the even spread of the work is close enough.
     const double key_bytes = 2.0 * dims->dh * 2;                 // one key's K and V
     const double part_bytes = 2.0 * dims->B * dims->Hq * p->n1 * (dims->dh * 4 + 8);
     const long tree_keys = ((p->n1 + gran - 1) / gran + 3) * (long)gran;
     double best = -1;
     for (int ns = 1; ns <= std::min(max_splits, 64); ++ns) {
-      const long keys = ((dims->capacity + ns - 1) / ns + gran - 1) / gran * gran + 3 * gran;
-      const double work = ((double)base * ns * keys + (double)base * tree_keys) / p->num_sms;
-      const double cost = std::max(work, (double)keys) +
-                          (ns + 1) * part_bytes / (p->num_sms * key_bytes);
+      const long chunk = ((dims->capacity + ns - 1) / ns + gran - 1) / gran * gran;
+      const long keys = chunk + 3 * gran;
+      const long ctas = (long)base * (ns + 1);
+      double busiest;
+      if (ctas <= 16L * p->num_sms) {
+        std::priority_queue<long, std::vector<long>, std::greater<long>> free_at;
+        for (int i = 0; i < p->num_sms; ++i) free_at.push(0);
+        long end = 0;
+        for (long c = 0; c < ctas; ++c) {
+          const int split = (int)(c % (ns + 1));
+          const long start = free_at.top();
+          free_at.pop();
+          const long done = start + (split == ns ? tree_keys : keys);
+          end = std::max(end, done);
+          free_at.push(done);
+        }
+        busiest = (double)end;
+      } else {
+        busiest = std::max(((double)base * ns * keys + (double)base * tree_keys) / p->num_sms,
+                           (double)keys);
+      }
+      const double cost = busiest + (ns + 1) * part_bytes / (p->num_sms * key_bytes);
       if (best < 0 || cost < best) { best = cost; p->nsplit = ns; }
     }
   }

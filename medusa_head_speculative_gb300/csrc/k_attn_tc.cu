@@ -24,6 +24,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -36,7 +37,7 @@ namespace medusa {
 constexpr int AT_ROWS = 128;      // query rows per tile (MMA M, TMEM lanes)
 constexpr int AT_TILES = 2;       // query tiles per CTA at most
 constexpr int AT_KEYS = 64;       // keys per chunk (S columns, PV reduction)
-constexpr int AT_STAGES = 3;      // K/V ring depth
+constexpr int AT_STAGES = 4;      // K/V ring depth at most (3 when two query tiles)
 constexpr int AT_WARPS = 4 * AT_TILES + 2;
 constexpr uint32_t AT_TILE_COLS = 256;   // per tile: S0 [0,64), S1 [64,128), O [128, 128+dh)
 constexpr float AT_LAZY = 8.f;           // log2 headroom before O is rescaled
@@ -48,6 +49,7 @@ struct AttnTcArgs {
   AttnArgs a;
   int kbox;              // cache rows per TMA box: 64 (contiguous) or the page size
   int nt;                // query tiles per CTA: rows_per_block / 128
+  int stages;            // K/V ring depth (<= AT_STAGES)
 };
 
 // Barriers: Q loaded; K/V stage full / empty; per tile and buffer: S written (BSF), P V
@@ -81,7 +83,7 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, gk = blockIdx.y;
   const int b = blockIdx.z / a.nrb, rb = blockIdx.z % a.nrb;
-  const int G = a.G, R = a.n1 * G, nt = g.nt;
+  const int G = a.G, R = a.n1 * G, nt = g.nt, ST = g.stages;
   const int row0 = rb * AT_ROWS * nt;
   const int nta = min(nt, (R - row0 + AT_ROWS - 1) / AT_ROWS);   // tiles with rows
   const bool tree = split == a.nsplit;
@@ -92,14 +94,14 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
   const int nch = kend > kbeg ? (kend - kbeg + AT_KEYS - 1) / AT_KEYS : 0;
   const uint32_t sraw = smem_u32(smem_raw);
   const uint32_t base = (sraw + 1023u) & ~1023u;
-  const uint32_t qs = base, kv0 = base + nt * H * QH, ps = kv0 + AT_STAGES * KV_STAGE;
+  const uint32_t qs = base, kv0 = base + nt * H * QH, ps = kv0 + ST * KV_STAGE;
   const uint32_t bar0 = smem_u32(bars);
   const uint32_t tmem_cols = AT_TILE_COLS * nt;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
   if (tid == 0) {
     mbar_init(bar(BQ), 1);
-    for (int i = 0; i < AT_STAGES; ++i) {
+    for (int i = 0; i < ST; ++i) {
       mbar_init(bar(BKVF + i), 1);
       mbar_init(bar(BKVE + i), 1);
     }
@@ -122,46 +124,65 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && nch > 0) {
+    // Lane 0 issues the copies.  For a paged cache the whole warp first reads the page ids
+    // of the next 32 pages (lane l: page l), so a chunk's boxes never wait on a
+    // dependent page-table load.
+    if (nch > 0) {
       const uint64_t pol_kv = policy_evict_first(), pol_q = policy_evict_last();
-      mbar_expect_tx(bar(BQ), nta * H * QH);
-      for (int t = 0; t < nta; ++t) {
-        const int node0 = (row0 + t * AT_ROWS) / G;
+      if (lane == 0) {
+        mbar_expect_tx(bar(BQ), nta * H * QH);
+        for (int t = 0; t < nta; ++t) {
+          const int node0 = (row0 + t * AT_ROWS) / G;
 #pragma unroll
-        for (int h = 0; h < H; ++h)
-          tma_load_3d(qs + (t * H + h) * QH, &g.tq, h * 64, gk * G, b * a.n1 + node0, bar(BQ), pol_q);
+          for (int h = 0; h < H; ++h)
+            tma_load_3d(qs + (t * H + h) * QH, &g.tq, h * 64, gk * G, b * a.n1 + node0, bar(BQ), pol_q);
+        }
       }
+      const bool paged = !tree && a.page_table;
+      int pref0 = -1 << 30, my_page = 0;               // first key covered by the page ids held
       int i = 0;
       for (; i < nch; ++i) {
-        const int st = i % AT_STAGES;
-        if (!mbar_wait(bar(BKVE + st), ((i / AT_STAGES) & 1) ^ 1, TC_TIMEOUT_NS)) {
-          timed_out = true;
+        const int st = i % ST;
+        const int t0 = kbeg + i * AT_KEYS;
+        if (paged && (t0 < pref0 || t0 + AT_KEYS > pref0 + 32 * a.page_size)) {
+          pref0 = t0 - t0 % a.page_size;
+          const int t = pref0 + lane * a.page_size;
+          my_page = 0;
+          if (t < a.capacity) {
+            my_page = a.page_table[(long)b * a.pages_per_seq + t / a.page_size];
+            if (my_page < 0 || my_page >= a.num_pages) {
+              set_flag(a.status, MEDUSA_FLAG_PAGE_RANGE);
+              my_page = 0;
+            }
+          }
+        }
+        int pages[AT_KEYS / 8];                          // one per box of this chunk
+        if (paged) {
+          for (int j = 0, q = 0; j < AT_KEYS; j += g.kbox, ++q)
+            pages[q] = __shfl_sync(0xffffffffu, my_page, (t0 + j - pref0) / a.page_size);
+        }
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(bar(BKVE + st), ((i / ST) & 1) ^ 1, TC_TIMEOUT_NS);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          timed_out = lane == 0;
           break;
         }
+        if (lane != 0) continue;
         mbar_expect_tx(bar(BKVF + st), KV_STAGE);
         const uint32_t ks = kv0 + st * KV_STAGE, vs = ks + H * KVH;
-        const int t0 = kbeg + i * AT_KEYS;
         if (tree) {
 #pragma unroll
           for (int h = 0; h < H; ++h) {
             tma_load_3d(ks + h * KVH, &g.ttk, h * 64, gk, b * a.n1 + t0, bar(BKVF + st), pol_kv);
             tma_load_3d(vs + h * KVH, &g.ttv, h * 64, gk, b * a.n1 + t0, bar(BKVF + st), pol_kv);
           }
-        } else if (a.page_table) {
-          for (int j = 0; j < AT_KEYS; j += g.kbox) {
-            const int t = t0 + j;
-            int page = 0;
-            if (t < a.capacity) {
-              page = a.page_table[(long)b * a.pages_per_seq + t / a.page_size];
-              if (page < 0 || page >= a.num_pages) {
-                set_flag(a.status, MEDUSA_FLAG_PAGE_RANGE);
-                page = 0;
-              }
-            }
+        } else if (paged) {
+          for (int j = 0, q = 0; j < AT_KEYS; j += g.kbox, ++q) {
+            const int row = pages[q] * a.page_size;
 #pragma unroll
             for (int h = 0; h < H; ++h) {
-              tma_load_3d(ks + h * KVH + j * 128, &g.tk, h * 64, gk, page * a.page_size, bar(BKVF + st), pol_kv);
-              tma_load_3d(vs + h * KVH + j * 128, &g.tv, h * 64, gk, page * a.page_size, bar(BKVF + st), pol_kv);
+              tma_load_3d(ks + h * KVH + j * 128, &g.tk, h * 64, gk, row, bar(BKVF + st), pol_kv);
+              tma_load_3d(vs + h * KVH + j * 128, &g.tv, h * 64, gk, row, bar(BKVF + st), pol_kv);
             }
           }
         } else {
@@ -172,10 +193,14 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
           }
         }
       }
-      s_issued = i;
+      if (lane == 0) s_issued = i;
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    // Per chunk i: S = Q K^T of chunk i + 1 goes first when its K/V stage has already
+    // landed (the softmax can then move on as soon as it is done with chunk i); otherwise
+    // O += P V of chunk i is not held back by that load, and S of chunk i + 1 follows it.
+    // Waits block (no polling loop), so the softmax warps keep their issue slots.
     if (lane == 0 && nch > 0) {
       int waited = 0;
       if (!mbar_wait(bar(BQ), 0, TC_TIMEOUT_NS)) {
@@ -184,28 +209,31 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
         s_qok = 1;
         const uint32_t id_qk = idesc_bf16(AT_ROWS, AT_KEYS);
         const uint32_t id_pv = idesc_bf16(AT_ROWS, DH) | IDESC_B_MN_MAJOR;
-        auto issue_qk = [&](int i) -> bool {
-          const int st = i % AT_STAGES;
-          if (!mbar_wait(bar(BKVF + st), (i / AT_STAGES) & 1, TC_TIMEOUT_NS)) return false;
-          waited = i + 1;
+        auto issue_qk = [&](int j) {
+          waited = j + 1;
           tc_fence_after();
-          const uint32_t ks = kv0 + st * KV_STAGE;
+          const uint32_t ks = kv0 + (j % ST) * KV_STAGE;
           for (int t = 0; t < nta; ++t) {
-            const uint32_t d = tmem + t * AT_TILE_COLS + (uint32_t)(i & 1) * AT_KEYS;
+            const uint32_t d = tmem + t * AT_TILE_COLS + (uint32_t)(j & 1) * AT_KEYS;
 #pragma unroll
             for (int h = 0; h < H; ++h)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 umma_bf16(d, sw128_desc(qs + (t * H + h) * QH) + 2 * kk,
                           sw128_desc(ks + h * KVH) + 2 * kk, id_qk, (h | kk) != 0);
-            umma_commit(bar(BSF + 2 * t + (i & 1)));
+            umma_commit(bar(BSF + 2 * t + (j & 1)));
           }
-          return true;
         };
-        if (!issue_qk(0)) timed_out = true;
+        if (mbar_wait(bar(BKVF), 0, TC_TIMEOUT_NS)) issue_qk(0);
+        else timed_out = true;
         for (int i = 0; i < nch && !timed_out; ++i) {
-          if (i + 1 < nch && !issue_qk(i + 1)) { timed_out = true; break; }
-          const uint32_t vs = kv0 + (i % AT_STAGES) * KV_STAGE + H * KVH;
+          const int j = i + 1;
+          bool qk_pending = j < nch;
+          if (qk_pending && mbar_test(bar(BKVF + j % ST), (j / ST) & 1)) {
+            issue_qk(j);
+            qk_pending = false;
+          }
+          const uint32_t vs = kv0 + (i % ST) * KV_STAGE + H * KVH;
           for (int t = 0; t < nta && !timed_out; ++t) {
             if (!mbar_wait(bar(BPR + 2 * t + (i & 1)), (i >> 1) & 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
             tc_fence_after();
@@ -217,7 +245,11 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
             umma_commit(bar(BOF + 2 * t + (i & 1)));
           }
           if (timed_out) break;
-          umma_commit(bar(BKVE + i % AT_STAGES));
+          umma_commit(bar(BKVE + i % ST));               // stage i read by every MMA
+          if (qk_pending) {
+            if (!mbar_wait(bar(BKVF + j % ST), (j / ST) & 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+            issue_qk(j);
+          }
         }
       }
       s_waited = waited;
@@ -233,8 +265,16 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
     uint8_t* pgen = smem_raw + (ps - sraw) + (size_t)(2 * t) * PT;
     const float sl2 = a.scale * 1.4426950408889634f;      // scores in base-2 units
     float m_use = -INFINITY, l_acc = 0.f;
+    // A warp whose 32 rows all lie past the block's rows only keeps pace: its arrivals
+    // for chunk i wait, as the others' do, until the P V of chunk i - 2 is done (its P
+    // rows are left as they are; their products land in O rows nobody reads).
+    const bool live = row0 + t * AT_ROWS + wl * 32 < R;
+    for (int i = 0; i < nch && !live; ++i) {
+      if (i >= 2 && !warp_wait(bar(BOF + 2 * t + (i & 1)), ((i - 2) >> 1) & 1)) { timed_out = true; break; }
+      mbar_arrive(bar(BPR + 2 * t + (i & 1)));
+    }
 
-    for (int i = 0; i < nch; ++i) {
+    for (int i = 0; i < nch && live; ++i) {
       if (!warp_wait(bar(BSF + 2 * t + (i & 1)), (i >> 1) & 1)) { timed_out = true; break; }
       tc_fence_after();
       float s[AT_KEYS];
@@ -246,18 +286,34 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
         for (int e = 0; e < 16; ++e) s[c + e] = v[e];
       }
       const int t0 = kbeg + i * AT_KEYS;
-      uint32_t w0 = 0xffffffffu, w1 = 0xffffffffu;
-      if (tree) {
-        w0 = row_ok ? a.mask[(long)node * kMaskWords + (t0 >> 5)] : 0u;
-        w1 = row_ok && (t0 >> 5) + 1 < kMaskWords ? a.mask[(long)node * kMaskWords + (t0 >> 5) + 1] : 0u;
-      }
-      float mx = -INFINITY;
+      // A whole chunk of prefix keys needs no mask: the maximum is taken over the raw
+      // scores and the scale is folded into the exponent's FMA below.
+      const bool full = !tree && t0 + AT_KEYS <= kend;
+      float mx;
+      if (full) {
+        float q0 = s[0], q1 = s[1], q2 = s[2], q3 = s[3];
 #pragma unroll
-      for (int j = 0; j < AT_KEYS; ++j) {
-        const bool bit = ((j < 32 ? w0 : w1) >> (j & 31)) & 1u;
-        const bool valid = (t0 + j < kend) && bit;
-        s[j] = valid ? s[j] * sl2 : -INFINITY;
-        mx = fmaxf(mx, s[j]);
+        for (int j = 4; j < AT_KEYS; j += 4) {
+          q0 = fmaxf(q0, s[j]);
+          q1 = fmaxf(q1, s[j + 1]);
+          q2 = fmaxf(q2, s[j + 2]);
+          q3 = fmaxf(q3, s[j + 3]);
+        }
+        mx = fmaxf(fmaxf(q0, q1), fmaxf(q2, q3)) * sl2;
+      } else {
+        uint32_t w0 = 0xffffffffu, w1 = 0xffffffffu;
+        if (tree) {
+          w0 = row_ok ? a.mask[(long)node * kMaskWords + (t0 >> 5)] : 0u;
+          w1 = row_ok && (t0 >> 5) + 1 < kMaskWords ? a.mask[(long)node * kMaskWords + (t0 >> 5) + 1] : 0u;
+        }
+        mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < AT_KEYS; ++j) {
+          const bool bit = ((j < 32 ? w0 : w1) >> (j & 31)) & 1u;
+          const bool valid = (t0 + j < kend) && bit;
+          s[j] = valid ? s[j] * sl2 : -INFINITY;
+          mx = fmaxf(mx, s[j]);
+        }
       }
       // this chunk's P buffer was last read by the P V of chunk i - 2
       if (i >= 2 && !warp_wait(bar(BOF + 2 * t + (i & 1)), ((i - 2) >> 1) & 1)) { timed_out = true; break; }
@@ -281,14 +337,33 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
         }
       }
       if (m_use == -INFINITY) m_use = mx;             // first keys of this row
-      float lsum = 0.f;
+      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+      if (full) {
+        const float nm = -m_use;
 #pragma unroll
-      for (int j = 0; j < AT_KEYS; ++j) {
-        const float p = s[j] == -INFINITY ? 0.f : ex2_approx(s[j] - m_use);
-        s[j] = p;
-        lsum += p;
+        for (int j = 0; j < AT_KEYS; j += 4) {
+          s[j] = ex2_approx(fmaf(s[j], sl2, nm));
+          s[j + 1] = ex2_approx(fmaf(s[j + 1], sl2, nm));
+          s[j + 2] = ex2_approx(fmaf(s[j + 2], sl2, nm));
+          s[j + 3] = ex2_approx(fmaf(s[j + 3], sl2, nm));
+          l0 += s[j];
+          l1 += s[j + 1];
+          l2 += s[j + 2];
+          l3 += s[j + 3];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < AT_KEYS; j += 4) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            s[j + e] = s[j + e] == -INFINITY ? 0.f : ex2_approx(s[j + e] - m_use);
+          l0 += s[j];
+          l1 += s[j + 1];
+          l2 += s[j + 2];
+          l3 += s[j + 3];
+        }
       }
-      l_acc += lsum;
+      l_acc += (l0 + l1) + (l2 + l3);
       // P row (bf16) into the 128-byte-swizzled K-major tile the PV MMA reads
       uint8_t* prow = pgen + (size_t)(i & 1) * PT + r * 128;
 #pragma unroll
@@ -311,7 +386,7 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
     float o[DH];
 #pragma unroll
     for (int c = 0; c < DH; ++c) o[c] = 0.f;
-    if (!timed_out && nch > 0) {
+    if (!timed_out && nch > 0 && live) {
       if (!warp_wait(bar(BOF + 2 * t + ((nch - 1) & 1)), ((nch - 1) >> 1) & 1)) {
         timed_out = true;
       } else {
@@ -340,7 +415,7 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
   if (tid == 0 && nch > 0) {                 // drain copies issued but never waited for
     if (!s_qok) mbar_wait(bar(BQ), 0, TC_TIMEOUT_NS / 16);
     for (int i = s_waited; i < s_issued; ++i)
-      mbar_wait(bar(BKVF + i % AT_STAGES), (i / AT_STAGES) & 1, TC_TIMEOUT_NS / 16);
+      mbar_wait(bar(BKVF + i % ST), (i / ST) & 1, TC_TIMEOUT_NS / 16);
   }
   __syncthreads();
   if (warp == 9) tmem_dealloc(tmem, tmem_cols);
@@ -405,8 +480,11 @@ cudaError_t launch_tree_attention_tc(const AttnArgs& a, const void* q_bf16, cuda
   if (a.rows_per_block != AT_ROWS && a.rows_per_block != AT_ROWS * AT_TILES) return cudaErrorInvalidValue;
   g.nt = a.rows_per_block / AT_ROWS;
   const int H = a.dh / 64;
-  const size_t smem = 1024 + (size_t)g.nt * H * AT_ROWS * 128 +
-                      (size_t)AT_STAGES * 2 * H * AT_KEYS * 128 + (size_t)g.nt * 2 * AT_ROWS * 128;
+  const size_t fixed = 1024 + (size_t)g.nt * H * AT_ROWS * 128 + (size_t)g.nt * 2 * AT_ROWS * 128;
+  const size_t kv_stage = (size_t)2 * H * AT_KEYS * 128;
+  g.stages = (int)std::min<size_t>(AT_STAGES, (226u * 1024u - fixed) / kv_stage);   // 227 KB per CTA
+  if (g.stages < 2) return cudaErrorInvalidValue;
+  const size_t smem = fixed + (size_t)g.stages * kv_stage;
   auto kern = a.dh == 128 ? tree_attn_tc_kernel<128> : tree_attn_tc_kernel<64>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

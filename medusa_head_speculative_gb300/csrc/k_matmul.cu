@@ -57,24 +57,49 @@ __global__ void __launch_bounds__(256) rowdot_kernel(MatArgs a, long total_rows)
       const W* w = reinterpret_cast<const W*>(s.w);
       for (int m0 = 0; m0 < a.M; m0 += MT) {
         const int mt = min(MT, a.M - m0);
-        __syncthreads();
-        for (int i = threadIdx.x; i < MT * k; i += blockDim.x) {
-          const int mm = i / k, kk = i - mm * k;
-          xs[i] = mm < mt ? s.x[(long)(m0 + mm) * s.ldx + kk] : 0.f;
+        // The warp's first U weight loads go out before the activations are staged, so
+        // the staging round trip overlaps the first HBM one.
+        uint4 buf[U];
+        const int rf = r0 + warp;
+        if (rf < r1) {
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int kk = lane * VEC + u * 32 * VEC;
+            if (kk < k) buf[u] = ld_stream16(w + (long)rf * k + kk);
+          }
         }
         __syncthreads();
-        for (int r = r0 + warp; r < r1; r += 8) {
+        if ((k & 3) == 0 && (s.ldx & 3) == 0 && (reinterpret_cast<uintptr_t>(s.x) & 15) == 0) {
+          const uint32_t xs0 = (uint32_t)__cvta_generic_to_shared(xs);
+          for (int i = threadIdx.x * 4; i < MT * k; i += blockDim.x * 4) {
+            const int mm = i / k, kk = i - mm * k;
+            const bool ok = mm < mt;
+            cp_async16(xs0 + 4u * (uint32_t)i, ok ? s.x + (long)(m0 + mm) * s.ldx + kk : s.x, ok ? 16 : 0);
+          }
+          cp_async_commit();
+          cp_async_wait<0>();
+        } else {
+          for (int i = threadIdx.x; i < MT * k; i += blockDim.x) {
+            const int mm = i / k, kk = i - mm * k;
+            xs[i] = mm < mt ? s.x[(long)(m0 + mm) * s.ldx + kk] : 0.f;
+          }
+        }
+        __syncthreads();
+        bool have = rf < r1;                           // buf holds the loads of (rf, lane*VEC)
+        for (int r = rf; r < r1; r += 8) {
           const W* wr = w + (long)r * k;
           float acc[MT];
 #pragma unroll
           for (int m = 0; m < MT; ++m) acc[m] = 0.f;
           for (int kb = lane * VEC; kb < k; kb += 32 * VEC * U) {
-            uint4 buf[U];
+            if (!have) {
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-              const int kk = kb + u * 32 * VEC;
-              if (kk < k) buf[u] = ld_stream16(wr + kk);
+              for (int u = 0; u < U; ++u) {
+                const int kk = kb + u * 32 * VEC;
+                if (kk < k) buf[u] = ld_stream16(wr + kk);
+              }
             }
+            have = false;
 #pragma unroll
             for (int u = 0; u < U; ++u) {
               const int kk = kb + u * 32 * VEC;
