@@ -7,6 +7,7 @@
 #include <queue>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <set>
@@ -15,6 +16,7 @@
 
 #include "../../include/medusa.h"
 #include "kernels.h"
+#include "launch.cuh"
 
 using namespace medusa;
 
@@ -587,6 +589,27 @@ bool medusa::heads_plan_view(const medusa_plan* p, HeadsPlanView* v) {
 }
 
 // ===================================================================== exported API
+namespace medusa {
+namespace {
+thread_local bool t_pdl_armed = false;       // a library kernel was the last launch ...
+thread_local cudaStream_t t_pdl_stream = nullptr;   // ... on this stream
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("MEDUSA_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+}  // namespace
+bool pdl_take(cudaStream_t st) {
+  const bool ok = t_pdl_armed && t_pdl_stream == st && pdl_enabled();
+  t_pdl_armed = true;
+  t_pdl_stream = st;
+  return ok;
+}
+void pdl_reset() { t_pdl_armed = false; }
+}  // namespace medusa
+
 extern "C" {
 
 medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec* tree,
@@ -792,6 +815,7 @@ medusa_status medusa_get_status(const medusa_plan* p, void* stream, uint32_t* fl
 medusa_status medusa_heads(const medusa_plan* p, const float* h, const int32_t* root_in,
                            const medusa_weights* w, float* logits, int32_t* topk_tok,
                            float* topk_val, int32_t* root, void* ws, size_t ws_bytes, void* stream) {
+  pdl_reset();
   if (!p || !h || !topk_tok || !topk_val || !root) return MEDUSA_ERR_INVALID;
   medusa_status s = check_weights(p, w, true, false, true);
   if (s != MEDUSA_OK) return s;
@@ -805,6 +829,7 @@ medusa_status medusa_heads(const medusa_plan* p, const float* h, const int32_t* 
 medusa_status medusa_tree_build(const medusa_plan* p, const int32_t* topk_tok, const int32_t* root,
                                 const int32_t* len, int32_t* tok, int32_t* pos, uint32_t* mask,
                                 int32_t* retrieve, void* stream) {
+  pdl_reset();
   if (!p || !topk_tok || !root || !len || !tok || !pos || !mask || !retrieve) return MEDUSA_ERR_INVALID;
   return tree_impl(p, topk_tok, root, len, tok, pos, mask, retrieve, S(stream));
 }
@@ -812,6 +837,7 @@ medusa_status medusa_tree_build(const medusa_plan* p, const int32_t* topk_tok, c
 medusa_status medusa_layer_qkv(const medusa_plan* p, const medusa_weights* w, const int32_t* tok,
                                const int32_t* pos, float* q, void* tk, void* tv, void* ws,
                                size_t ws_bytes, void* stream) {
+  pdl_reset();
   if (!p || !tok || !pos || !q || !tk || !tv) return MEDUSA_ERR_INVALID;
   medusa_status s = check_weights(p, w, false, true, false);
   if (s != MEDUSA_OK) return s;
@@ -823,6 +849,7 @@ medusa_status medusa_layer_qkv(const medusa_plan* p, const medusa_weights* w, co
 medusa_status medusa_tree_attention(const medusa_plan* p, const float* q, const medusa_kv* kv,
                                     const void* tk, const void* tv, const uint32_t* mask, float* o,
                                     void* ws, size_t ws_bytes, void* stream) {
+  pdl_reset();
   if (!p || !q || !tk || !tv || !mask || !o) return MEDUSA_ERR_INVALID;
   medusa_status s = check_kv(p, kv, false);
   if (s != MEDUSA_OK) return s;
@@ -832,6 +859,7 @@ medusa_status medusa_tree_attention(const medusa_plan* p, const float* q, const 
 
 medusa_status medusa_layer_out(const medusa_plan* p, const medusa_weights* w, const int32_t* tok,
                                const float* o, float* hprime, void* ws, size_t ws_bytes, void* stream) {
+  pdl_reset();
   if (!p || !tok || !o || !hprime) return MEDUSA_ERR_INVALID;
   medusa_status s = check_weights(p, w, false, true, false);
   if (s != MEDUSA_OK) return s;
@@ -843,6 +871,7 @@ medusa_status medusa_layer_out(const medusa_plan* p, const medusa_weights* w, co
 medusa_status medusa_verify_logits(const medusa_plan* p, const medusa_weights* w, const float* hprime,
                                    const int32_t* tok, medusa_accept acc, float* logits, int32_t* am,
                                    float* stats, void* ws, size_t ws_bytes, void* stream) {
+  pdl_reset();
   if (!p || !hprime || !tok || !am || !stats) return MEDUSA_ERR_INVALID;
   medusa_status s = check_weights(p, w, false, false, true);
   if (s != MEDUSA_OK) return s;
@@ -855,6 +884,7 @@ medusa_status medusa_verify_logits(const medusa_plan* p, const medusa_weights* w
 medusa_status medusa_verify(const medusa_plan* p, const int32_t* tok, const int32_t* am,
                             const float* stats, const int32_t* retrieve, const float* hprime,
                             medusa_accept acc, const medusa_outputs* out, void* stream) {
+  pdl_reset();
   if (!p || !tok || !am || !stats || !retrieve || !hprime || !out) return MEDUSA_ERR_INVALID;
   if (!out->out_tok || !out->n_acc || !out->h_next || !out->root_next) return MEDUSA_ERR_INVALID;
   medusa_status s = check_accept(acc);
@@ -866,6 +896,7 @@ medusa_status medusa_verify(const medusa_plan* p, const int32_t* tok, const int3
 medusa_status medusa_kv_compact(const medusa_plan* p, const medusa_kv* kv, const void* tk,
                                 const void* tv, const int32_t* path_nodes, const int32_t* n_acc,
                                 void* stream) {
+  pdl_reset();
   if (!p || !tk || !tv || !path_nodes || !n_acc) return MEDUSA_ERR_INVALID;
   medusa_status s = check_kv(p, kv, true);
   if (s != MEDUSA_OK) return s;
@@ -875,6 +906,7 @@ medusa_status medusa_kv_compact(const medusa_plan* p, const medusa_kv* kv, const
 medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* root_in,
                           const medusa_weights* w, const medusa_kv* kv, medusa_accept acc,
                           const medusa_outputs* out, void* ws, size_t ws_bytes, void* stream) {
+  pdl_reset();
   if (!p || !h || !out) return MEDUSA_ERR_INVALID;
   if (!out->out_tok || !out->n_acc || !out->h_next || !out->root_next) return MEDUSA_ERR_INVALID;
   medusa_status s = check_weights(p, w, true, true, true);

@@ -76,6 +76,13 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
 
+// ----------------------------------------------------------------- programmatic dependent launch
+// Let the next kernel on the stream start launching (once every CTA of this one has run
+// this), and wait until every earlier kernel has completed and its writes are visible.
+// Both are no-ops for kernels launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ----------------------------------------------------------------- cp.async / ldmatrix / mma
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

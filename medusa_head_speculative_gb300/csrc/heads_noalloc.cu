@@ -26,6 +26,7 @@
 
 #include "../../include/medusa.h"
 #include "kernels.h"
+#include "launch.cuh"
 
 using namespace medusa;
 
@@ -86,6 +87,7 @@ extern "C" medusa_status medusa_heads_noalloc(const medusa_plan* plan, const flo
                                               const int32_t* root_in, const medusa_weights* w,
                                               int32_t* topk_tok, float* topk_val, int32_t* root,
                                               void* stream) {
+  pdl_reset();
   HeadsPlanView v;
   if (!heads_plan_view(plan, &v)) return MEDUSA_ERR_INVALID;
   const Layout l = layout_of(v);

@@ -10,6 +10,7 @@
 // merges the partials by log-sum-exp.
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace medusa {
 
@@ -32,6 +33,8 @@ __device__ __forceinline__ long kv_offset(const AttnArgs& a, int b, int t, int g
 template <typename T, int DH, int RPW>
 __global__ void __launch_bounds__(256) tree_attn_kernel(AttnArgs a) {
   extern __shared__ float sm[];
+  pdl_trigger();
+  pdl_wait();
   constexpr int C = DH / 32;
   float* Qs = sm;                                   // [rows_per_block][DH]
   float* Ks = Qs + a.rows_per_block * DH;           // [TK][DH + 1]
@@ -152,6 +155,8 @@ __global__ void __launch_bounds__(256) tree_attn_kernel(AttnArgs a) {
 // pairs are read once per lane and reduced across the warp.
 template <int VPL>
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int R = a.n1 * a.G, S = a.nsplit + 1;
   const long wg = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (wg >= (long)a.B * a.Hkv * R) return;
@@ -206,19 +211,17 @@ static cudaError_t attn_go(const AttnArgs& a, cudaStream_t st) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.nsplit + 1, a.Hkv, a.B * a.nrb);
-  tree_attn_kernel<T, DH, RPW><<<grid, 256, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(tree_attn_kernel<T, DH, RPW>, grid, dim3(256), smem, st, 1, a);
 }
 
 cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st) {
   const long rows = (long)a.B * a.Hkv * a.n1 * a.G;
   const int blocks = (int)((rows + 7) / 8);           // 8 warps per CTA, one row each
   switch (a.dh) {
-    case 32: attn_combine_kernel<1><<<blocks, 256, 0, st>>>(a); break;
-    case 64: attn_combine_kernel<2><<<blocks, 256, 0, st>>>(a); break;
-    default: attn_combine_kernel<4><<<blocks, 256, 0, st>>>(a); break;
+    case 32: return launch_kernel(attn_combine_kernel<1>, dim3(blocks), dim3(256), 0, st, 1, a);
+    case 64: return launch_kernel(attn_combine_kernel<2>, dim3(blocks), dim3(256), 0, st, 1, a);
+    default: return launch_kernel(attn_combine_kernel<4>, dim3(blocks), dim3(256), 0, st, 1, a);
   }
-  return cudaGetLastError();
 }
 
 template <typename T, int DH>

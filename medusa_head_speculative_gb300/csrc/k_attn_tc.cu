@@ -30,6 +30,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 #include "tc_ptx.cuh"
 
 namespace medusa {
@@ -119,29 +120,38 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_trigger();                         // only once this CTA holds its TMEM
   const uint32_t tmem = tmem_slot;
   bool timed_out = false;
+  if (warp != 8) pdl_wait();             // q, tree K/V and the outputs belong to this call
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     // Lane 0 issues the copies.  For a paged cache the whole warp first reads the page ids
     // of the next 32 pages (lane l: page l), so a chunk's boxes never wait on a
     // dependent page-table load.
+    // The cached prefix is written by no kernel of this call: the first ring of its K/V
+    // chunks is requested before the wait for earlier kernels, Q and the tree keys after.
     if (nch > 0) {
       const uint64_t pol_kv = policy_evict_first(), pol_q = policy_evict_last();
-      if (lane == 0) {
-        mbar_expect_tx(bar(BQ), nta * H * QH);
-        for (int t = 0; t < nta; ++t) {
-          const int node0 = (row0 + t * AT_ROWS) / G;
+      auto load_q = [&]() {
+        pdl_wait();
+        if (lane == 0) {
+          mbar_expect_tx(bar(BQ), nta * H * QH);
+          for (int t = 0; t < nta; ++t) {
+            const int node0 = (row0 + t * AT_ROWS) / G;
 #pragma unroll
-          for (int h = 0; h < H; ++h)
-            tma_load_3d(qs + (t * H + h) * QH, &g.tq, h * 64, gk * G, b * a.n1 + node0, bar(BQ), pol_q);
+            for (int h = 0; h < H; ++h)
+              tma_load_3d(qs + (t * H + h) * QH, &g.tq, h * 64, gk * G, b * a.n1 + node0, bar(BQ), pol_q);
+          }
         }
-      }
+      };
+      const int pre = tree ? 0 : (nch < ST ? nch : ST);
       const bool paged = !tree && a.page_table;
       int pref0 = -1 << 30, my_page = 0;               // first key covered by the page ids held
       int i = 0;
       for (; i < nch; ++i) {
+        if (i == pre) load_q();
         const int st = i % ST;
         const int t0 = kbeg + i * AT_KEYS;
         if (paged && (t0 < pref0 || t0 + AT_KEYS > pref0 + 32 * a.page_size)) {
@@ -193,6 +203,7 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
           }
         }
       }
+      if (i == nch && pre == nch) load_q();            // every chunk went out early
       if (lane == 0) s_issued = i;
     }
   } else if (warp == 9) {
@@ -489,8 +500,7 @@ cudaError_t launch_tree_attention_tc(const AttnArgs& a, const void* q_bf16, cuda
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.nsplit + 1, a.Hkv, a.B * a.nrb);
-  kern<<<grid, AT_WARPS * 32, smem, st>>>(g);
-  return cudaGetLastError();
+  return launch_kernel(kern, grid, dim3(AT_WARPS * 32), smem, st, 1, g);
 }
 
 }  // namespace medusa

@@ -9,6 +9,7 @@
 // thousands of rows is in k_umma.cu.
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace medusa {
 
@@ -47,6 +48,7 @@ __global__ void __launch_bounds__(256) rowdot_kernel(MatArgs a, long total_rows)
   const long g1 = total_rows * (blockIdx.x + 1) / gridDim.x;
   const int k = a.k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_trigger();
   long seg_start = 0;
   for (int si = 0; si < a.nseg; ++si) {
     const MatSeg& s = a.seg[si];
@@ -68,6 +70,7 @@ __global__ void __launch_bounds__(256) rowdot_kernel(MatArgs a, long total_rows)
             if (kk < k) buf[u] = ld_stream16(w + (long)rf * k + kk);
           }
         }
+        pdl_wait();                                    // activations come from earlier kernels
         __syncthreads();
         if ((k & 3) == 0 && (s.ldx & 3) == 0 && (reinterpret_cast<uintptr_t>(s.x) & 15) == 0) {
           const uint32_t xs0 = (uint32_t)__cvta_generic_to_shared(xs);
@@ -157,8 +160,7 @@ static cudaError_t rowdot_go(const MatArgs& a, cudaStream_t st) {
   long grid = (long)per_sm * num_sms;
   const long by_rows = (total + 7) / 8;               // at least one row per warp
   grid = grid < by_rows ? grid : by_rows;
-  rowdot_kernel<W, MT><<<(int)grid, 256, smem, st>>>(a, total);
-  return cudaGetLastError();
+  return launch_kernel(rowdot_kernel<W, MT>, dim3((unsigned)grid), dim3(256), smem, st, 1, a, total);
 }
 
 cudaError_t launch_rowdot(const MatArgs& a, int dtype, cudaStream_t st) {
@@ -181,6 +183,8 @@ cudaError_t launch_rowdot(const MatArgs& a, int dtype, cudaStream_t st) {
 
 // =========================================================== small helpers
 __global__ void split_kernel(const float* x, bf16* hi, bf16* lo, long n) {
+  pdl_trigger();
+  pdl_wait();
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x)
     split_hi_lo(x[i], hi[i], lo[i]);
 }
@@ -188,11 +192,13 @@ __global__ void split_kernel(const float* x, bf16* hi, bf16* lo, long n) {
 cudaError_t launch_split(const float* x, bf16* hi, bf16* lo, long n, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   const long blocks = (n + 255) / 256;
-  split_kernel<<<(int)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(x, hi, lo, n);
-  return cudaGetLastError();
+  return launch_kernel(split_kernel, dim3((unsigned)(blocks < 4096 ? blocks : 4096)), dim3(256), 0, st, 1,
+                       x, hi, lo, n);
 }
 
 __global__ void to_bf16_kernel(const float* x, bf16* y, long n) {
+  pdl_trigger();
+  pdl_wait();
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x)
     y[i] = __float2bfloat16_rn(x[i]);
 }
@@ -200,12 +206,14 @@ __global__ void to_bf16_kernel(const float* x, bf16* y, long n) {
 cudaError_t launch_to_bf16(const float* x, bf16* y, long n, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   const long blocks = (n + 255) / 256;
-  to_bf16_kernel<<<(int)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(x, y, n);
-  return cudaGetLastError();
+  return launch_kernel(to_bf16_kernel, dim3((unsigned)(blocks < 4096 ? blocks : 4096)), dim3(256), 0, st, 1,
+                       x, y, n);
 }
 
 template <typename W>
 __global__ void gather_kernel(const W* emb, const int32_t* tok, int d, int V, float* xf, bf16* xb) {
+  pdl_trigger();
+  pdl_wait();
   const int m = blockIdx.x;
   int t = tok[m];
   t = (t < 0 || t >= V) ? 0 : t;                    // ids were range-checked upstream
@@ -227,10 +235,10 @@ cudaError_t launch_gather(const void* emb, int dtype, const int32_t* tok, int M,
                           float* xf, bf16* xb, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
   if (dtype == 0)
-    gather_kernel<float><<<M, 256, 0, st>>>(reinterpret_cast<const float*>(emb), tok, d, V, xf, xb);
-  else
-    gather_kernel<bf16><<<M, 256, 0, st>>>(reinterpret_cast<const bf16*>(emb), tok, d, V, xf, xb);
-  return cudaGetLastError();
+    return launch_kernel(gather_kernel<float>, dim3(M), dim3(256), 0, st, 1,
+                         reinterpret_cast<const float*>(emb), tok, d, V, xf, xb);
+  return launch_kernel(gather_kernel<bf16>, dim3(M), dim3(256), 0, st, 1,
+                       reinterpret_cast<const bf16*>(emb), tok, d, V, xf, xb);
 }
 
 }  // namespace medusa

@@ -11,6 +11,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace medusa {
 
@@ -101,13 +102,14 @@ __device__ void slice_topk(const TopkArgs& a, int sp, int k, int b) {
 }
 
 __global__ void __launch_bounds__(256) topk_partial_kernel(TopkArgs a) {
+  pdl_trigger();
+  pdl_wait();
   slice_topk(a, blockIdx.x, blockIdx.y + a.k0, blockIdx.z);
 }
 
 cudaError_t launch_topk_partial(const TopkArgs& a, cudaStream_t st) {
   dim3 grid(a.splits, a.nh - a.k0, a.B);
-  topk_partial_kernel<<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(topk_partial_kernel, grid, dim3(256), 0, st, 1, a);
 }
 
 // Merge of sequence b's vocab slices: warp w merges heads w, w+8 (head 0 is the LM head,
@@ -159,12 +161,13 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(MergeArgs a) {
   __shared__ float tv[MEDUSA_MAX_HEADS + 1][kTops];
   __shared__ int ti[MEDUSA_MAX_HEADS + 1][kTops];
   __shared__ int s_root;
+  pdl_trigger();
+  pdl_wait();
   merge_heads(a, blockIdx.x, tv, ti, &s_root);
 }
 
 cudaError_t launch_topk_merge(const MergeArgs& a, cudaStream_t st) {
-  topk_merge_kernel<<<a.B, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(topk_merge_kernel, dim3(a.B), dim3(256), 0, st, 1, a);
 }
 
 // Fused selection for the whole step: every CTA takes the top-16 of one vocab slice of one
@@ -176,6 +179,8 @@ __global__ void __launch_bounds__(256) heads_select_kernel(TopkArgs t, MergeArgs
   __shared__ float tv[MEDUSA_MAX_HEADS + 1][kTops];
   __shared__ int ti[MEDUSA_MAX_HEADS + 1][kTops];
   __shared__ int s_root, s_last;
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.z;
   slice_topk(t, blockIdx.x, blockIdx.y + t.k0, b);
   __threadfence();
@@ -192,8 +197,7 @@ __global__ void __launch_bounds__(256) heads_select_kernel(TopkArgs t, MergeArgs
 cudaError_t launch_heads_select(const TopkArgs& t, const MergeArgs& m, const TreeArgs& tr,
                                 int32_t* counter, cudaStream_t st) {
   dim3 grid(t.splits, t.nh - t.k0, t.B);
-  heads_select_kernel<<<grid, 256, 0, st>>>(t, m, tr, counter);
-  return cudaGetLastError();
+  return launch_kernel(heads_select_kernel, grid, dim3(256), 0, st, 1, t, m, tr, counter);
 }
 
 // One CTA per sequence: node tokens and position ids.  Block 0 also writes the per-tree
@@ -201,6 +205,8 @@ cudaError_t launch_heads_select(const TopkArgs& t, const MergeArgs& m, const Tre
 __global__ void __launch_bounds__(256) tree_build_kernel(TreeArgs a) {
   __shared__ int haschild[MEDUSA_MAX_NODES];
   __shared__ int leafidx[MEDUSA_MAX_NODES];
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x, tid = threadIdx.x;
   int L = a.len[b];
   if (L < 0) L = 0;
@@ -240,8 +246,7 @@ __global__ void __launch_bounds__(256) tree_build_kernel(TreeArgs a) {
 }
 
 cudaError_t launch_tree_build(const TreeArgs& a, cudaStream_t st) {
-  tree_build_kernel<<<a.B, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(tree_build_kernel, dim3(a.B), dim3(256), 0, st, 1, a);
 }
 
 // One CTA per node row.  cos/sin of pos * theta_i come from the plan's table (computed on
@@ -252,6 +257,8 @@ __global__ void __launch_bounds__(1024) rope_split_kernel(
     const float* __restrict__ qkv, const int32_t* __restrict__ pos, int Hq, int Hkv, int dh,
     const float* __restrict__ table, int rows, uint32_t* status, float* __restrict__ q,
     bf16* __restrict__ qb, T* __restrict__ tk, T* __restrict__ tv) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float cs[];                      // [dh/2] cos, [dh/2] sin
   const int m = blockIdx.x, half = dh / 2;
   int p = pos[m];
@@ -293,14 +300,12 @@ cudaError_t launch_rope_split(const float* qkv, const int32_t* pos, int M, int H
   if (M <= 0) return cudaSuccess;
   const size_t smem = dh * sizeof(float);
   if (dtype == 0)
-    rope_split_kernel<float><<<M, 1024, smem, st>>>(qkv, pos, Hq, Hkv, dh, table, rows, status, q, qb,
-                                                   reinterpret_cast<float*>(tk),
-                                                   reinterpret_cast<float*>(tv));
-  else
-    rope_split_kernel<bf16><<<M, 1024, smem, st>>>(qkv, pos, Hq, Hkv, dh, table, rows, status, q, qb,
-                                                  reinterpret_cast<bf16*>(tk),
-                                                  reinterpret_cast<bf16*>(tv));
-  return cudaGetLastError();
+    return launch_kernel(rope_split_kernel<float>, dim3(M), dim3(1024), smem, st, 1, qkv, pos, Hq, Hkv,
+                         dh, table, rows, status, q, qb, reinterpret_cast<float*>(tk),
+                         reinterpret_cast<float*>(tv));
+  return launch_kernel(rope_split_kernel<bf16>, dim3(M), dim3(1024), smem, st, 1, qkv, pos, Hq, Hkv, dh,
+                       table, rows, status, q, qb, reinterpret_cast<bf16*>(tk),
+                       reinterpret_cast<bf16*>(tv));
 }
 
 void rope_table(float base, int dh, int rows, float* out) {

@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 #include "tc_ptx.cuh"
 
 namespace medusa {
@@ -100,18 +101,31 @@ __global__ void __launch_bounds__(128, 2) umma_gemm_kernel(const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Dependents may launch only once every CTA holds its TMEM: a later kernel's CTA can
+  // then never take the columns an earlier kernel's CTA is still waiting for.
+  pdl_trigger();
   const uint32_t tmem = tmem_slot;
   bool timed_out = false;
 
   if (warp == 0 && lane == 0) {                         // ---- TMA producer
     const uint64_t pw = policy_evict_first(), pa = policy_evict_last();
+    // The weights of the first S stages go out before the wait for earlier kernels (no
+    // kernel writes them); the activations after it.
+    const int pre = nkl < S ? nkl : S;
+    for (int j = 0; j < pre; ++j) {
+      mbar_expect_tx(full(j), STAGE);
+      tma_load_2d(base + j * STAGE, &g.tw[si], (kt0 + j) * UM_K, rbase, full(j), pw);
+    }
+    pdl_wait();
     int j = 0;
     for (; j < nkl; ++j) {
       const int st = j % S, kx = (kt0 + j) * UM_K;
-      if (!mbar_wait(empty(st), ((j / S) & 1) ^ 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
-      mbar_expect_tx(full(st), STAGE);
       const uint32_t ws = base + st * STAGE;
-      tma_load_2d(ws, &g.tw[si], kx, rbase, full(st), pw);
+      if (j >= pre) {
+        if (!mbar_wait(empty(st), ((j / S) & 1) ^ 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+        mbar_expect_tx(full(st), STAGE);
+        tma_load_2d(ws, &g.tw[si], kx, rbase, full(st), pw);
+      }
       tma_load_2d(ws + UM_W_BYTES, &g.ta[si], kx, m0, full(st), pa);
       if (HAS_LO) tma_load_2d(ws + UM_W_BYTES + A_BYTES, &g.tl[si], kx, m0, full(st), pa);
     }
@@ -137,6 +151,7 @@ __global__ void __launch_bounds__(128, 2) umma_gemm_kernel(const __grid_constant
     umma_commit(accb);                                  // accumulator complete
   }
   __syncwarp();
+  pdl_wait();                                           // the epilogue reads and writes globals
   // ---- epilogue: thread = TMEM lane = weight row
   const bool acc_ok = mbar_wait(accb, 0, TC_TIMEOUT_NS);
   tc_fence_after();
@@ -239,18 +254,29 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
   __syncthreads();
   cluster_sync();                       // the peer's barriers exist before any copy or arrive
   tc_fence_after();
+  pdl_trigger();                        // after the TMEM allocation, as above
   const uint32_t tmem = tmem_slot;
   bool timed_out = false;
 
   if (warp == 0 && lane == 0) {                         // ---- TMA producer
     const uint64_t pw = policy_evict_first(), pa = policy_evict_last();
+    const uint32_t stage_tx = (has_w ? UW_W_BYTES : 0u) + A_BYTES * (HAS_LO ? 2 : 1);
+    // weights of the first S stages before the wait for earlier kernels, as above
+    const int pre = nkl < S ? nkl : S;
+    for (int j = 0; j < pre; ++j) {
+      mbar_expect_tx(full(j), stage_tx);
+      if (has_w) tma_load_2d(base + j * STAGE, &g.tw[si], (kt0 + j) * UM_K, rbase, full(j), pw);
+    }
+    pdl_wait();
     int j = 0;
     for (; j < nkl; ++j) {
       const int st = j % S, kx = (kt0 + j) * UM_K;
-      if (!mbar_wait(empty(st), ((j / S) & 1) ^ 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
-      mbar_expect_tx(full(st), (has_w ? UW_W_BYTES : 0u) + A_BYTES * (HAS_LO ? 2 : 1));
       const uint32_t ws = base + st * STAGE;
-      if (has_w) tma_load_2d(ws, &g.tw[si], kx, rbase, full(st), pw);
+      if (j >= pre) {
+        if (!mbar_wait(empty(st), ((j / S) & 1) ^ 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+        mbar_expect_tx(full(st), stage_tx);
+        if (has_w) tma_load_2d(ws, &g.tw[si], kx, rbase, full(st), pw);
+      }
       const uint32_t off = UW_W_BYTES + rank * (uint32_t)half * 128;
       tma_load_2d_mc(ws + off, &g.ta, kx, m0 + (int)rank * half, full(st), UW_PAIR, pa);
       if (HAS_LO) tma_load_2d_mc(ws + off + A_BYTES, &g.tl, kx, m0 + (int)rank * half, full(st), UW_PAIR, pa);
@@ -280,6 +306,7 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
     umma_commit(accb);
   }
   __syncwarp();
+  pdl_wait();
   const bool acc_ok = mbar_wait(accb, 0, TC_TIMEOUT_NS);
   tc_fence_after();
   __syncwarp();
@@ -326,6 +353,8 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
 // store (multi-segment EPI_STORE launches).  cols % 4 == 0.
 __global__ void splitk_reduce_kernel(const MatArgs a, const float* __restrict__ kpart, int ksplit, int cols) {
   constexpr int ZMAX = 8;
+  pdl_trigger();
+  pdl_wait();
   const int c4 = cols / 4;
   const long n = (long)a.M * c4;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
@@ -384,8 +413,8 @@ static cudaError_t launch_splitk_reduce(const MatArgs& a, int ksplit, cudaStream
   const int ncols = a.nseg == 1 ? a.seg[0].rows : (int)a.ldo;
   const long n4 = (long)a.M * (ncols / 4);
   const long blocks = (n4 + 255) / 256;
-  splitk_reduce_kernel<<<(int)(blocks < 8192 ? blocks : 8192), 256, 0, st>>>(a, a.kpart, ksplit, ncols);
-  return cudaGetLastError();
+  return launch_kernel(splitk_reduce_kernel, dim3((unsigned)(blocks < 8192 ? blocks : 8192)), dim3(256), 0, st,
+                       1, a, a.kpart, ksplit, ncols);
 }
 
 // K ranges for a launch of `ctas` CTAs that leaves SMs idle (single-segment launches, or
@@ -435,20 +464,7 @@ static cudaError_t launch_umma_wide(const MatArgs& m, uint32_t* status, int num_
   auto kern = has_lo ? umma_wide_kernel<true> : umma_wide_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(nct, ytiles, g.ksplit);
-  cfg.blockDim = dim3(128, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 2;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, g);
+  e = launch_kernel(kern, dim3(nct, ytiles, g.ksplit), dim3(128), smem, st, 2, g);
   if (e != cudaSuccess || g.ksplit == 1) return e;
   return launch_splitk_reduce(a, g.ksplit, st);
 }
@@ -515,9 +531,7 @@ cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st
   auto kern = has_lo ? umma_gemm_kernel<true> : umma_gemm_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(mchunks, a.tile_off[a.nseg], ksplit);
-  kern<<<grid, 128, smem, st>>>(g);
-  e = cudaGetLastError();
+  e = launch_kernel(kern, dim3(mchunks, a.tile_off[a.nseg], ksplit), dim3(128), smem, st, 1, g);
   if (e != cudaSuccess || ksplit == 1) return e;
   return launch_splitk_reduce(a, ksplit, st);
 }

@@ -10,6 +10,7 @@
 // prefix); "MEDUSA 精读" section 3 (only the accepted path stays in the KV cache).
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace medusa {
 
@@ -153,11 +154,14 @@ __device__ void row_stats(const VerifyArgs& a, int row) {
   if (threadIdx.x == 0) row_finish(a, row, r);
 }
 
-__global__ void __launch_bounds__(1024) verify_stats_kernel(VerifyArgs a) { row_stats(a, blockIdx.x); }
+__global__ void __launch_bounds__(1024) verify_stats_kernel(VerifyArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  row_stats(a, blockIdx.x);
+}
 
 cudaError_t launch_verify_stats(const VerifyArgs& a, cudaStream_t st) {
-  verify_stats_kernel<<<a.B * a.n1, 1024, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(verify_stats_kernel, dim3(a.B * a.n1), dim3(1024), 0, st, 1, a);
 }
 
 // Acceptance of sequence b by one CTA; thread c decides candidate c, thread p walks path
@@ -228,11 +232,14 @@ __device__ void accept_seq(const VerifyArgs& a, int b) {
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(256) verify_accept_kernel(VerifyArgs a) { accept_seq(a, blockIdx.x); }
+__global__ void __launch_bounds__(256) verify_accept_kernel(VerifyArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  accept_seq(a, blockIdx.x);
+}
 
 cudaError_t launch_verify_accept(const VerifyArgs& a, cudaStream_t st) {
-  verify_accept_kernel<<<a.B, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(verify_accept_kernel, dim3(a.B), dim3(256), 0, st, 1, a);
 }
 
 // One CTA per sequence: slot len + l <- tree node path_nodes[l], l < n_acc, in 16-byte
@@ -313,7 +320,11 @@ __device__ void compact_seq(const CompactArgs& a, int b) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256) kv_compact_kernel(CompactArgs a) { compact_seq<T>(a, blockIdx.x); }
+__global__ void __launch_bounds__(256) kv_compact_kernel(CompactArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  compact_seq<T>(a, blockIdx.x);
+}
 
 // Fused verification for the whole step.  Each node row's vocabulary is split over
 // kVerifySlices CTAs; the last slice CTA of a row (per-row counter) merges the partials and
@@ -325,6 +336,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) verify_commit_kernel(VerifyArgs v, CompactArgs c, int32_t* row_cnt,
                                                             int32_t* seq_cnt, float* parts) {
   __shared__ int s_last;
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x, sl = blockIdx.y, b = row / v.n1;
   const int per = ((v.V + kVerifySlices - 1) / kVerifySlices + 3) / 4 * 4;
   const int v0 = min(v.V, sl * per), v1 = min(v.V, v0 + per);
@@ -370,18 +383,13 @@ cudaError_t launch_verify_commit(const VerifyArgs& v, const CompactArgs& c, int3
                                  int32_t* seq_cnt, float* parts, cudaStream_t st) {
   dim3 grid(v.B * v.n1, kVerifySlices);
   if (c.dtype == 0)
-    verify_commit_kernel<float><<<grid, 256, 0, st>>>(v, c, row_cnt, seq_cnt, parts);
-  else
-    verify_commit_kernel<bf16><<<grid, 256, 0, st>>>(v, c, row_cnt, seq_cnt, parts);
-  return cudaGetLastError();
+    return launch_kernel(verify_commit_kernel<float>, grid, dim3(256), 0, st, 1, v, c, row_cnt, seq_cnt, parts);
+  return launch_kernel(verify_commit_kernel<bf16>, grid, dim3(256), 0, st, 1, v, c, row_cnt, seq_cnt, parts);
 }
 
 cudaError_t launch_kv_compact(const CompactArgs& a, cudaStream_t st) {
-  if (a.dtype == 0)
-    kv_compact_kernel<float><<<a.B, 256, 0, st>>>(a);
-  else
-    kv_compact_kernel<bf16><<<a.B, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  if (a.dtype == 0) return launch_kernel(kv_compact_kernel<float>, dim3(a.B), dim3(256), 0, st, 1, a);
+  return launch_kernel(kv_compact_kernel<bf16>, dim3(a.B), dim3(256), 0, st, 1, a);
 }
 
 }  // namespace medusa
