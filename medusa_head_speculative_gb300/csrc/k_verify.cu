@@ -73,32 +73,82 @@ struct RowPart {
   SoftStat st;
   bool nonfinite;
 };
+// Each thread visits its logits in increasing index order, so a strict ">" keeps the
+// lowest index among equal maxima (the merge across threads breaks ties by index).  The
+// softmax sums move their reference maximum once per batch of 32 logits.  A non-finite
+// logit makes the running sum of the logits non-finite.
 __device__ RowPart row_part(const VerifyArgs& a, int row, int v0, int v1) {
   __shared__ float sv[32], sS[32], sU[32];
   __shared__ int si[32];
+  constexpr int NB = 8;                                // float4 loads in flight per thread
   const float* z = a.logits + (long)row * a.V;
   const bool typ = a.typical != 0;
-  const float T = a.temperature;
+  const float invT = typ ? 1.f / a.temperature : 0.f;
   RowPart r{-INFINITY, 0x7fffffff, SoftStat{-INFINITY, 0.f, 0.f}, false};
-  auto take = [&](float x, int v) {
-    r.nonfinite |= !isfinite(x);
-    if (better(x, v, r.bv, r.bi)) { r.bv = x; r.bi = v; }
-    if (typ) stat_add(r.st, x / T);
-  };
-  if ((a.V & 3) == 0 && (v0 & 3) == 0) {
-    const float4* z4 = reinterpret_cast<const float4*>(z);
-    const int q1 = v1 / 4;
-    for (int q = v0 / 4 + threadIdx.x; q < q1; q += blockDim.x) {
-      const float4 x = z4[q];
-      take(x.x, 4 * q);
-      take(x.y, 4 * q + 1);
-      take(x.z, 4 * q + 2);
-      take(x.w, 4 * q + 3);
+  float sx = 0.f;
+  auto raise_to = [&](float bm) {                      // move the reference maximum up to bm
+    if (bm > r.st.m) {
+      if (r.st.m != -INFINITY) {
+        const float f = __expf(r.st.m - bm);
+        r.st.U = f * (r.st.U + (r.st.m - bm) * r.st.S);
+        r.st.S *= f;
+      }
+      r.st.m = bm;
     }
-    for (int v = q1 * 4 + threadIdx.x; v < v1; v += blockDim.x) take(z[v], v);
-  } else {
-    for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) take(z[v], v);
+  };
+  const bool vec = (a.V & 3) == 0 && (v0 & 3) == 0;
+  const int q0 = vec ? v0 / 4 : 0, q1 = vec ? v1 / 4 : 0;
+  for (int qb = q0 + threadIdx.x; qb < q1; qb += NB * blockDim.x) {
+    float4 x[NB];
+    bool ok[NB];
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+      const int q = qb + u * blockDim.x;
+      ok[u] = q < q1;
+      x[u] = ok[u] ? reinterpret_cast<const float4*>(z)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float bm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+      if (!ok[u]) continue;
+      const int q = qb + u * blockDim.x;
+      const float xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        sx += xs[e];
+        if (xs[e] > r.bv) { r.bv = xs[e]; r.bi = 4 * q + e; }
+        bm = fmaxf(bm, xs[e]);
+      }
+    }
+    if (typ) {
+      raise_to(bm * invT);
+#pragma unroll
+      for (int u = 0; u < NB; ++u) {
+        if (!ok[u]) continue;
+        const float xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float d = xs[e] * invT - r.st.m;
+          const float w = __expf(d);
+          r.st.S += w;
+          r.st.U += d * w;
+        }
+      }
+    }
   }
+  for (int v = (vec ? 4 * q1 : v0) + threadIdx.x; v < v1; v += blockDim.x) {   // ragged tail
+    const float x = z[v];
+    sx += x;
+    if (x > r.bv) { r.bv = x; r.bi = v; }
+    if (typ) {
+      raise_to(x * invT);
+      const float d = x * invT - r.st.m;
+      const float w = __expf(d);
+      r.st.S += w;
+      r.st.U += d * w;
+    }
+  }
+  r.nonfinite = __syncthreads_or(!isfinite(sx)) != 0;   // any thread's logits
   if (typ) {                                   // merge the statistics across the CTA
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
