@@ -18,20 +18,21 @@ namespace medusa {
 #define NEG_INF (-INFINITY)
 constexpr int NO_IDX = 0x7fffffff;
 
-// Sorted (descending) per-thread candidate list kept in registers.
-struct TopList {
-  float v[kTops];
-  int i[kTops];
+// Sorted (descending) per-thread candidate list of depth N kept in registers.
+template <int N>
+struct TopListN {
+  float v[N];
+  int i[N];
   __device__ __forceinline__ void init() {
 #pragma unroll
-    for (int t = 0; t < kTops; ++t) { v[t] = NEG_INF; i[t] = NO_IDX; }
+    for (int t = 0; t < N; ++t) { v[t] = NEG_INF; i[t] = NO_IDX; }
   }
   __device__ __forceinline__ void insert(float x, int idx) {
-    if (!better(x, idx, v[kTops - 1], i[kTops - 1])) return;
-    v[kTops - 1] = x;
-    i[kTops - 1] = idx;
+    if (!better(x, idx, v[N - 1], i[N - 1])) return;
+    v[N - 1] = x;
+    i[N - 1] = idx;
 #pragma unroll
-    for (int t = kTops - 1; t > 0; --t) {
+    for (int t = N - 1; t > 0; --t) {
       if (better(v[t], i[t], v[t - 1], i[t - 1])) {
         float tv = v[t]; v[t] = v[t - 1]; v[t - 1] = tv;
         int ti = i[t]; i[t] = i[t - 1]; i[t - 1] = ti;
@@ -40,11 +41,12 @@ struct TopList {
   }
   __device__ __forceinline__ void pop() {
 #pragma unroll
-    for (int t = 0; t < kTops - 1; ++t) { v[t] = v[t + 1]; i[t] = i[t + 1]; }
-    v[kTops - 1] = NEG_INF;
-    i[kTops - 1] = NO_IDX;
+    for (int t = 0; t < N - 1; ++t) { v[t] = v[t + 1]; i[t] = i[t + 1]; }
+    v[N - 1] = NEG_INF;
+    i[N - 1] = NO_IDX;
   }
 };
+using TopList = TopListN<kTops>;
 
 // Order-preserving 32-bit key of a float (larger float -> larger key; -0 as +0; NaN lowest).
 __device__ __forceinline__ uint32_t float_key(float v) {
@@ -57,10 +59,13 @@ __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Merge the 32 lanes' sorted lists: kTops rounds of a warp reduction over the list heads
-// (max of the value keys, then min of the token ids among the lanes holding that value);
-// the winning lane pops.  Token ids are distinct across lanes (sentinels aside).
-__device__ __forceinline__ void warp_merge(TopList& L, float* ov, int* oi, int rounds = kTops) {
+// Merge the 32 lanes' sorted lists into the first `rounds` ranks of ov/oi (kTops entries;
+// ranks past `rounds` are written as sentinels): each round is a warp reduction over the
+// list heads (max of the value keys, then min of the token ids among the lanes holding
+// that value) and the winning lane pops.  Token ids are distinct across lanes (sentinels
+// aside).
+template <int N>
+__device__ __forceinline__ void warp_merge(TopListN<N>& L, float* ov, int* oi, int rounds = kTops) {
   const int lane = threadIdx.x & 31;
   rounds = rounds < 1 || rounds > kTops ? kTops : rounds;
   if (lane == 0)                                   // ranks past `rounds` are not needed
@@ -79,23 +84,35 @@ __device__ __forceinline__ void warp_merge(TopList& L, float* ov, int* oi, int r
 }
 
 // The 16 best (logit, token) pairs of one vocab slice of one head, by a 256-thread CTA.
+// Slices of up to 1024 logits leave each thread at most 4 of them, so the per-thread and
+// per-warp lists are 4 deep; the 8 warps' lists (one run of up to 16 per warp) are then
+// spread 4 entries per lane over warp 0 and merged the same way.
 __device__ void slice_topk(const TopkArgs& a, int sp, int k, int b) {
   __shared__ float sv[8][kTops];
   __shared__ int si[8][kTops];
   const float* z = a.logits + ((long)b * a.nh + k) * a.V;
   const int lo = sp * a.chunk, hi = min(a.V, lo + a.chunk);
-  TopList L;
-  L.init();
-  for (int v = lo + threadIdx.x; v < hi; v += blockDim.x) L.insert(z[v], v);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  warp_merge(L, sv[warp], si[warp], a.rounds[k]);
+  if (hi - lo <= 4 * (int)blockDim.x) {
+    TopListN<4> L;
+    L.init();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = lo + threadIdx.x + u * blockDim.x;
+      if (v < hi) L.insert(z[v], v);
+    }
+    warp_merge(L, sv[warp], si[warp], a.rounds[k]);
+  } else {
+    TopList L;
+    L.init();
+    for (int v = lo + threadIdx.x; v < hi; v += blockDim.x) L.insert(z[v], v);
+    warp_merge(L, sv[warp], si[warp], a.rounds[k]);
+  }
   __syncthreads();
   if (warp == 0) {
-    L.init();
-    if (lane < 8) {
+    TopListN<4> L;                                  // lane l: entries 4(l/8).. of warp l%8
 #pragma unroll
-      for (int t = 0; t < kTops; ++t) { L.v[t] = sv[lane][t]; L.i[t] = si[lane][t]; }
-    }
+    for (int t = 0; t < 4; ++t) { L.v[t] = sv[lane & 7][4 * (lane >> 3) + t]; L.i[t] = si[lane & 7][4 * (lane >> 3) + t]; }
     const long o = (((long)b * a.nh + k) * a.splits + sp) * kTops;
     warp_merge(L, a.cand_val + o, a.cand_idx + o, a.rounds[k]);
   }
