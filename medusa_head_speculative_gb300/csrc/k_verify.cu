@@ -80,7 +80,7 @@ struct RowPart {
 __device__ RowPart row_part(const VerifyArgs& a, int row, int v0, int v1) {
   __shared__ float sv[32], sS[32], sU[32];
   __shared__ int si[32];
-  constexpr int NB = 8;                                // float4 loads in flight per thread
+  constexpr int NB = 4;                                // float4 loads in flight per thread
   const float* z = a.logits + (long)row * a.V;
   const bool typ = a.typical != 0;
   const float invT = typ ? 1.f / a.temperature : 0.f;
@@ -339,7 +339,7 @@ __device__ void compact_seq(const CompactArgs& a, int b) {
   const uint4* tk = reinterpret_cast<const uint4*>(a.tk);
   const uint4* tv = reinterpret_cast<const uint4*>(a.tv);
   constexpr int EPV = 16 / sizeof(T);                   // elements per piece
-  constexpr int BATCH = 8;                              // loads in flight before the stores
+  constexpr int BATCH = 4;                              // loads in flight before the stores
   const int total = n * per, step = blockDim.x;
   for (int e0 = threadIdx.x; e0 < total; e0 += step * BATCH) {
     uint4 kb[BATCH], vb[BATCH];
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(CompactArgs a) {
 constexpr int kVerifySlices = 4;
 
 template <typename T>
-__global__ void __launch_bounds__(256) verify_commit_kernel(VerifyArgs v, CompactArgs c, int32_t* row_cnt,
+__global__ void __launch_bounds__(256, 4) verify_commit_kernel(VerifyArgs v, CompactArgs c, int32_t* row_cnt,
                                                             int32_t* seq_cnt, float* parts) {
   __shared__ int s_last;
   pdl_trigger();
