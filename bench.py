@@ -36,6 +36,9 @@ METRIC = "Medusa verify steps/s and tree-nodes/s on 1 GB300; HBM GB/s vs ~8 TB/s
 FALLBACK_HBM_GBS = 6800.0
 
 
+FALLBACK_BF16_TFLOPS = 1700.0    # sustained figure of the fallback measurement
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -44,6 +47,16 @@ def peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 TFLOP/s for kernels timed inside a long step: the measured sustained
+    figure (power-capped), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def config_of(w: S.Workload, n1: int):
@@ -71,6 +84,23 @@ def kernel_bytes(w: S.Workload, n1: int, tc_heads: bool):
         "tree_attention": kv_prefix + M * (qd * 4 + 2 * kd * es),
         "layer_out": d * qd * es + M * qd * 4 + M * d * (2 + 4 + 4),
         "verify_logits": V * d * es + M * d * 4 + M * V * 4,
+    }
+
+
+def kernel_flops(w: S.Workload, n1: int):
+    """Algorithmic FLOPs per launch of the contractions (the method's products, counted
+    once: the hi/lo activation halves that double the tensor-core work are not counted)."""
+    B, d, V, K = w.B, w.d, w.V, w.K
+    M = B * n1
+    qd, kd = w.Hq * w.dh, w.Hkv * w.dh
+    prefix = sum(w.lengths)
+    return {
+        "heads_w1": 2 * B * K * d * d,
+        "heads_vocab": 2 * B * (K + 1) * V * d,
+        "layer_qkv": 2 * M * (qd + 2 * kd) * d,
+        "tree_attention": 4 * n1 * w.Hq * w.dh * prefix + 4 * B * n1 * n1 * w.Hq * w.dh // 2,
+        "layer_out": 2 * M * d * qd,
+        "verify_logits": 2 * M * V * d,
     }
 
 
@@ -139,6 +169,23 @@ def steady_state(args, w: S.Workload, st, stream, barrier):
             "steps": 2 * reps, "launch": mode,
             "note": "root_in = previous root_next, h = previous h_next: the LM head is read "
                     "once per step; prefix length held fixed"}
+
+
+# ----------------------------------------------------------------------- ranks
+def max_over_ranks(x: float, dist, device) -> float:
+    """The maximum of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    dev = device if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank: float, ms: float) -> float:
+    """Units per second of the whole job when every rank processed units_per_rank in (at
+    most) ms milliseconds: the replicas are independent, so their work adds up."""
+    return world * units_per_rank / (ms / 1e3)
 
 
 # ----------------------------------------------------------------------- clocks
@@ -300,10 +347,7 @@ def run_ours(args, w: S.Workload):
     for _ in range(kp):
         one_step()
     kernels, _ = plan.profile_stop()
-    t = torch.tensor([ms], dtype=torch.float64, device=device)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dist, device)
     assert plan.status() == 0, "device status word set during the timed region"
     n_acc_mean = float(st["out"]["n_acc"].float().mean())
     steady = steady_state(args, w, st, stream, barrier)
@@ -327,10 +371,9 @@ def run_ours(args, w: S.Workload):
     barrier()
     e2e_ms = e0.elapsed_time(e1)
     wall = time.perf_counter() - t0
-    te = torch.tensor([max(e2e_ms, wall * 1e3)], dtype=torch.float64, device=device)
-    if dist is not None:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_ms = float(te.item())
+    e2e_ms = max_over_ranks(max(e2e_ms, wall * 1e3), dist, device)
+    steady_ms = max_over_ranks(steady["ms_per_step"], dist, device)
+    steady.update(value=round(whole_job_rate(world, 1, steady_ms), 2), ms_per_step=round(steady_ms, 5))
 
     if rank != 0:
         if dist is not None:
@@ -348,11 +391,30 @@ def run_ours(args, w: S.Workload):
         if name in kb:
             row["gbs"] = round(kb[name] / (us * 1e-6) / 1e9, 1)
         ktab[name] = row
+    kf = kernel_flops(w, n1)
+    tflops, tflops_kind = tensor_peak()
+    ridge = tflops * 1e12 / (hbm * 1e9)                 # FLOP per byte where the bounds meet
     dom = max((n for n in kernels if n in kb), key=lambda n: kernels[n][1])
     dom_us = kernels[dom][1] * 1e3 / kernels[dom][0]
-    achieved = kb[dom] / (dom_us * 1e-6) / 1e9
     traffic = load_traffic(w.name, dom)
-    steps_per_s = world * K / (ms_max / 1e3)
+    if kf.get(dom, 0) / kb[dom] > ridge:                # a dense contraction at this size
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(kf[dom] / (dom_us * 1e-6) / 1e12, 1),
+                "peak": tflops, "unit": "TFLOP/s",
+                "frac": round(kf[dom] / (dom_us * 1e-6) / 1e12 / tflops, 4), "traffic": traffic,
+                "algorithmic_flops": kf[dom],
+                "peak_source": f"{tflops_kind} (MEASURED_PEAKS.json bf16_tflops_sustained)"
+                if tflops_kind == "measured" else "fallback 1.7 PFLOP/s sustained"}
+    else:
+        achieved = kb[dom] / (dom_us * 1e-6) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "traffic": traffic, "algorithmic_bytes": kb[dom],
+                "peak_source": f"{hbm_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if hbm_kind == "measured" else "fallback 6.8 TB/s"}
+    # The whole step against its roofline: each modelled kernel bound by the slower of its
+    # bytes at the HBM peak and its FLOPs at the tensor peak; the remaining kernels at zero.
+    ideal_us = sum(max(kb[n] / (hbm * 1e9), kf.get(n, 0) / (tflops * 1e12)) * 1e6 for n in kb)
+    steps_per_s = whole_job_rate(world, K, ms_max)
     sb = step_bytes(w, n1)
     res = {
         "metric": METRIC, "value": round(steps_per_s, 2), "unit": "steps/s", "n_gpus": world,
@@ -365,13 +427,12 @@ def run_ours(args, w: S.Workload):
         "step_hbm_frac": round(sb / (ms_max / K * 1e-3) / 1e9 / hbm, 4),
         "step_bytes": sb,
         "mean_tokens_per_step": round(n_acc_mean, 3),
-        "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
-                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "traffic": traffic, "algorithmic_bytes": kb[dom],
-                     "peak_source": f"{hbm_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                     if hbm_kind == "measured" else "fallback 6.8 TB/s"},
+        "roofline": roof,
+        "step_roofline": {"ideal_us": round(ideal_us, 1), "frac": round(ideal_us / (ms_max / K * 1e3), 4),
+                          "note": "per-kernel max(algorithmic bytes / HBM peak, FLOPs / bf16 "
+                                  "sustained peak), summed over the modelled kernels"},
         "kernels": ktab,
-        "e2e": {"value": round(world * ke / (e2e_ms / 1e3), 2), "unit": "steps/s",
+        "e2e": {"value": round(whole_job_rate(world, ke, e2e_ms), 2), "unit": "steps/s",
                 "h2d_bytes_per_step": int(h_host.numel() * 4),
                 "d2h_bytes_per_step": int(tok_host.numel() * 4 + nacc_host.numel() * 4)},
         "clocks": clk,
