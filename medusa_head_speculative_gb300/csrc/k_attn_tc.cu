@@ -289,13 +289,7 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
       if (!warp_wait(bar(BSF + 2 * t + (i & 1)), (i >> 1) & 1)) { timed_out = true; break; }
       tc_fence_after();
       float s[AT_KEYS];
-#pragma unroll
-      for (int c = 0; c < AT_KEYS; c += 16) {
-        float v[16];
-        tmem_ld16(lane_base + (uint32_t)(i & 1) * AT_KEYS + c, v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) s[c + e] = v[e];
-      }
+      tmem_ld64(lane_base + (uint32_t)(i & 1) * AT_KEYS, s);     // one round trip
       const int t0 = kbeg + i * AT_KEYS;
       // A whole chunk of prefix keys needs no mask: the maximum is taken over the raw
       // scores and the scale is folded into the exponent's FMA below.
@@ -403,11 +397,11 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
       } else {
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < DH; c += 16) {
-          float v[16];
-          tmem_ld16(lane_base + 128 + c, v);
+        for (int c = 0; c < DH; c += 64) {
+          float v[64];
+          tmem_ld64(lane_base + 128 + c, v);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[c + e] = v[e];
+          for (int e = 0; e < 64; ++e) o[c + e] = v[e];
         }
       }
     }
