@@ -243,12 +243,14 @@ medusa_status medusa_kv_compact(const medusa_plan* plan, const medusa_kv* kv,
                                 const int32_t* path_nodes, const int32_t* n_acc, void* stream);
 
 /* ------------------------------------------------------------------ tracing */
-/* Per-kernel timing (CUDA events recorded on the launching stream around every kernel the
- * following calls on this plan launch).  medusa_profile_start() creates the events for up to
- * max_launches launches (host-side resource, no device memory); launches past that are not
- * timed.  medusa_profile_stop() synchronises `stream`, aggregates by kernel name into out
- * (up to max_kernels entries, in first-launch order), writes the entry count to *n, the
- * timed launches to *launches, and ends profiling. */
+/* Per-stage timing (CUDA events recorded on the launching stream around every stage the
+ * following calls on this plan run; a stage is one kernel, or a projection and its split-K
+ * summation pass).  medusa_profile_start() creates the events for up to max_launches stages
+ * (host-side resource, no device memory); stages past that are not timed.
+ * medusa_profile_stop() synchronises `stream`, aggregates by stage name into out (up to
+ * max_kernels entries, in first-launch order), writes the entry count to *n and the number
+ * of kernels the calling thread launched meanwhile (split-K passes included) to
+ * *launches, and ends profiling.  Each call also appears as an NVTX range named after it. */
 typedef struct {
   char name[32];
   int launches;

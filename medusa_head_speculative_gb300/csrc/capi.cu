@@ -46,6 +46,7 @@ struct Profiler {
   int used = 0;
   std::vector<cudaEvent_t> ev;      // two per timed launch
   std::vector<int> name;
+  long kernels0 = 0;                // kernel-launch count when profiling started
   void release() {
     for (cudaEvent_t e : ev) cudaEventDestroy(e);
     ev.clear();
@@ -591,6 +592,7 @@ bool medusa::heads_plan_view(const medusa_plan* p, HeadsPlanView* v) {
 // ===================================================================== exported API
 namespace medusa {
 namespace {
+thread_local long t_kernels = 0;             // kernels launched by this host thread
 thread_local bool t_pdl_armed = false;       // a library kernel was the last launch ...
 thread_local cudaStream_t t_pdl_stream = nullptr;   // ... on this stream
 bool pdl_enabled() {
@@ -601,7 +603,9 @@ bool pdl_enabled() {
   return on;
 }
 }  // namespace
+long kernels_launched() { return t_kernels; }
 bool pdl_take(cudaStream_t st) {
+  ++t_kernels;                                // every kernel launch passes through here
   const bool ok = t_pdl_armed && t_pdl_stream == st && pdl_enabled();
   t_pdl_armed = true;
   t_pdl_stream = st;
@@ -768,6 +772,7 @@ medusa_status medusa_profile_start(medusa_plan* p, int max_launches) {
       return MEDUSA_ERR_CUDA;
     }
   p->prof.on = true;
+  p->prof.kernels0 = kernels_launched();
   return MEDUSA_OK;
 }
 
@@ -787,7 +792,7 @@ medusa_status medusa_profile_stop(medusa_plan* p, void* stream, medusa_kernel_ti
     if (count[k]++ == 0) order.push_back(k);
     ms[k] += t;
   }
-  *launches = p->prof.used;
+  *launches = (int)(kernels_launched() - p->prof.kernels0);   // kernels, incl. split-K passes
   int m = 0;
   for (int k : order) {
     if (m >= max_kernels) break;
@@ -815,7 +820,7 @@ medusa_status medusa_get_status(const medusa_plan* p, void* stream, uint32_t* fl
 medusa_status medusa_heads(const medusa_plan* p, const float* h, const int32_t* root_in,
                            const medusa_weights* w, float* logits, int32_t* topk_tok,
                            float* topk_val, int32_t* root, void* ws, size_t ws_bytes, void* stream) {
-  pdl_reset();
+  EntryScope scope("medusa_heads");
   if (!p || !h || !topk_tok || !topk_val || !root) return MEDUSA_ERR_INVALID;
   medusa_status s = check_weights(p, w, true, false, true);
   if (s != MEDUSA_OK) return s;
@@ -829,7 +834,7 @@ medusa_status medusa_heads(const medusa_plan* p, const float* h, const int32_t* 
 medusa_status medusa_tree_build(const medusa_plan* p, const int32_t* topk_tok, const int32_t* root,
                                 const int32_t* len, int32_t* tok, int32_t* pos, uint32_t* mask,
                                 int32_t* retrieve, void* stream) {
-  pdl_reset();
+  EntryScope scope("medusa_tree_build");
   if (!p || !topk_tok || !root || !len || !tok || !pos || !mask || !retrieve) return MEDUSA_ERR_INVALID;
   return tree_impl(p, topk_tok, root, len, tok, pos, mask, retrieve, S(stream));
 }
@@ -837,7 +842,7 @@ medusa_status medusa_tree_build(const medusa_plan* p, const int32_t* topk_tok, c
 medusa_status medusa_layer_qkv(const medusa_plan* p, const medusa_weights* w, const int32_t* tok,
                                const int32_t* pos, float* q, void* tk, void* tv, void* ws,
                                size_t ws_bytes, void* stream) {
-  pdl_reset();
+  EntryScope scope("medusa_layer_qkv");
   if (!p || !tok || !pos || !q || !tk || !tv) return MEDUSA_ERR_INVALID;
   medusa_status s = check_weights(p, w, false, true, false);
   if (s != MEDUSA_OK) return s;
@@ -849,7 +854,7 @@ medusa_status medusa_layer_qkv(const medusa_plan* p, const medusa_weights* w, co
 medusa_status medusa_tree_attention(const medusa_plan* p, const float* q, const medusa_kv* kv,
                                     const void* tk, const void* tv, const uint32_t* mask, float* o,
                                     void* ws, size_t ws_bytes, void* stream) {
-  pdl_reset();
+  EntryScope scope("medusa_tree_attention");
   if (!p || !q || !tk || !tv || !mask || !o) return MEDUSA_ERR_INVALID;
   medusa_status s = check_kv(p, kv, false);
   if (s != MEDUSA_OK) return s;
@@ -859,7 +864,7 @@ medusa_status medusa_tree_attention(const medusa_plan* p, const float* q, const 
 
 medusa_status medusa_layer_out(const medusa_plan* p, const medusa_weights* w, const int32_t* tok,
                                const float* o, float* hprime, void* ws, size_t ws_bytes, void* stream) {
-  pdl_reset();
+  EntryScope scope("medusa_layer_out");
   if (!p || !tok || !o || !hprime) return MEDUSA_ERR_INVALID;
   medusa_status s = check_weights(p, w, false, true, false);
   if (s != MEDUSA_OK) return s;
@@ -871,7 +876,7 @@ medusa_status medusa_layer_out(const medusa_plan* p, const medusa_weights* w, co
 medusa_status medusa_verify_logits(const medusa_plan* p, const medusa_weights* w, const float* hprime,
                                    const int32_t* tok, medusa_accept acc, float* logits, int32_t* am,
                                    float* stats, void* ws, size_t ws_bytes, void* stream) {
-  pdl_reset();
+  EntryScope scope("medusa_verify_logits");
   if (!p || !hprime || !tok || !am || !stats) return MEDUSA_ERR_INVALID;
   medusa_status s = check_weights(p, w, false, false, true);
   if (s != MEDUSA_OK) return s;
@@ -884,7 +889,7 @@ medusa_status medusa_verify_logits(const medusa_plan* p, const medusa_weights* w
 medusa_status medusa_verify(const medusa_plan* p, const int32_t* tok, const int32_t* am,
                             const float* stats, const int32_t* retrieve, const float* hprime,
                             medusa_accept acc, const medusa_outputs* out, void* stream) {
-  pdl_reset();
+  EntryScope scope("medusa_verify");
   if (!p || !tok || !am || !stats || !retrieve || !hprime || !out) return MEDUSA_ERR_INVALID;
   if (!out->out_tok || !out->n_acc || !out->h_next || !out->root_next) return MEDUSA_ERR_INVALID;
   medusa_status s = check_accept(acc);
@@ -896,7 +901,7 @@ medusa_status medusa_verify(const medusa_plan* p, const int32_t* tok, const int3
 medusa_status medusa_kv_compact(const medusa_plan* p, const medusa_kv* kv, const void* tk,
                                 const void* tv, const int32_t* path_nodes, const int32_t* n_acc,
                                 void* stream) {
-  pdl_reset();
+  EntryScope scope("medusa_kv_compact");
   if (!p || !tk || !tv || !path_nodes || !n_acc) return MEDUSA_ERR_INVALID;
   medusa_status s = check_kv(p, kv, true);
   if (s != MEDUSA_OK) return s;
@@ -906,7 +911,7 @@ medusa_status medusa_kv_compact(const medusa_plan* p, const medusa_kv* kv, const
 medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* root_in,
                           const medusa_weights* w, const medusa_kv* kv, medusa_accept acc,
                           const medusa_outputs* out, void* ws, size_t ws_bytes, void* stream) {
-  pdl_reset();
+  EntryScope scope("medusa_step");
   if (!p || !h || !out) return MEDUSA_ERR_INVALID;
   if (!out->out_tok || !out->n_acc || !out->h_next || !out->root_next) return MEDUSA_ERR_INVALID;
   medusa_status s = check_weights(p, w, true, true, true);

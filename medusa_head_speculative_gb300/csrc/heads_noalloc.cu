@@ -87,7 +87,7 @@ extern "C" medusa_status medusa_heads_noalloc(const medusa_plan* plan, const flo
                                               const int32_t* root_in, const medusa_weights* w,
                                               int32_t* topk_tok, float* topk_val, int32_t* root,
                                               void* stream) {
-  pdl_reset();
+  EntryScope scope("medusa_heads_noalloc");
   HeadsPlanView v;
   if (!heads_plan_view(plan, &v)) return MEDUSA_ERR_INVALID;
   const Layout l = layout_of(v);

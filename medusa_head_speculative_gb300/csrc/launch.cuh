@@ -12,6 +12,7 @@
 // waits, as usual, for everything the caller queued before the call.
 #pragma once
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstring>
 #include <utility>
@@ -23,6 +24,20 @@ namespace medusa {
 bool pdl_take(cudaStream_t st);
 // Called on entry to every public function that launches kernels.
 void pdl_reset();
+// Kernels launched so far by the calling host thread.
+long kernels_launched();
+
+// Scope of one public entry point: the first launch inside it does not overlap earlier
+// work, and the call shows up as an NVTX range (named after the entry point) in profilers.
+struct EntryScope {
+  explicit EntryScope(const char* name) {
+    pdl_reset();
+    nvtxRangePushA(name);
+  }
+  ~EntryScope() { nvtxRangePop(); }
+  EntryScope(const EntryScope&) = delete;
+  EntryScope& operator=(const EntryScope&) = delete;
+};
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,

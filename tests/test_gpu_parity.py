@@ -227,3 +227,70 @@ def test_workspace_too_small_is_rejected():
     with pytest.raises(Bnd.MedusaError) as e:
         run_step(dev)
     assert e.value.code == Bnd.MEDUSA_ERR_WORKSPACE
+
+
+def test_nonfinite_hidden_state_is_contained_and_flagged():
+    """A NaN in one sequence's h_t never faults: its candidate tokens come out of range and
+    are flagged (then clamped), and the other sequences' outputs are unchanged."""
+    w = _mid()
+    dev = setup(w)
+    clean = run_step(dev, len_out=torch.empty_like(dev.length))
+    assert dev.plan.status() == 0
+    dev.h[0, 5] = float("nan")
+    bad = run_step(dev, len_out=torch.empty_like(dev.length))
+    assert dev.plan.status() & (Bnd.FLAG_TOKEN_RANGE | Bnd.FLAG_NONFINITE)
+    np.testing.assert_array_equal(bad["out_tok"][1:], clean["out_tok"][1:])
+    np.testing.assert_array_equal(bad["path"][1:], clean["path"][1:])
+    np.testing.assert_array_equal(bad["h_next"][1:].cpu().numpy(), clean["h_next"][1:].cpu().numpy())
+    assert ((bad["out_tok"][0] >= -1) & (bad["out_tok"][0] < w.V)).all()
+
+
+def _guarded(n, dtype, fill):
+    """A flat buffer of n elements with 4096-element guard bands filled with `fill`."""
+    G = 4096
+    big = torch.full((n + 2 * G,), fill, dtype=dtype, device="cuda")
+    return big, big[G:G + n]
+
+
+def test_step_writes_stay_inside_the_buffers():
+    """Canary bands around every buffer the step writes (outputs, lengths, workspace) stay
+    intact, and the inputs it only reads (h_t, the cached prefix) are unchanged."""
+    for w in (_mid(page_size=16), _mid(B=2, Hq=4, Hkv=4, N=150, lengths=(70, 200)), S.workload("tiny")):
+        dev = setup(w)
+        B, K, d = w.B, w.K, w.d
+        i32 = torch.int32
+        canary = {}
+        def buf(name, shape, dtype, fill):
+            n = int(np.prod(shape))
+            big, mid = _guarded(n, dtype, fill)
+            canary[name] = (big, n, fill)
+            return mid.view(shape)
+        out_tok = buf("out_tok", (B, K + 1), i32, -12345)
+        n_acc = buf("n_acc", (B,), i32, -12345)
+        path = buf("path", (B, K + 1), i32, -12345)
+        h_next = buf("h_next", (B, d), torch.float32, 1234.5)
+        root_next = buf("root_next", (B,), i32, -12345)
+        len_out = buf("len_out", (B,), i32, -12345)
+        ws = buf("ws", (dev.plan.workspace_size,), torch.uint8, 0xA5)
+        h0 = dev.h.clone()
+        k0 = dev.kc.clone()
+        kv = Bnd.kv_struct(dev.kc, dev.vc, dev.length, len_out, dev.pt)
+        outs = Bnd.outputs_struct(out_tok, n_acc, path, h_next, root_next)
+        from harness import accept_of
+        Bnd.step(dev.plan, dev.h, None, dev.wstruct, kv, Bnd.accept_struct(**accept_of(w)), outs, ws)
+        torch.cuda.synchronize()
+        assert dev.plan.status() == 0
+        G = 4096
+        for name, (big, n, fill) in canary.items():
+            lo, hi = big[:G], big[G + n:]
+            ref = torch.full_like(lo, fill)
+            assert torch.equal(lo, ref) and torch.equal(hi, ref), f"{w.name}: {name} guard band written"
+        assert torch.equal(dev.h, h0)
+        # the cache changes only in the slots after each prefix (the compacted path)
+        kc = dev.kc.float().cpu()
+        kref = k0.float().cpu()
+        if not w.page_size:
+            for b in range(B):
+                L = w.lengths[b]
+                assert torch.equal(kc[b, :L], kref[b, :L])
+                assert torch.equal(kc[b, L + int(n_acc[b]):], kref[b, L + int(n_acc[b]):])
