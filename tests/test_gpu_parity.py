@@ -42,6 +42,9 @@ CASES = {
     "vicuna13b": (S.workload("vicuna13b"), (0, 5)),
     "zephyr7b": (S.workload("zephyr7b"), (3, 12)),
     "vicuna33b_b4_l1024_n16": (S.vicuna33b(4, 1024, 16), (2,)),
+    # 2064 node rows: the clustered wide projections over many activation tiles, and
+    # two 128-row attention tiles (129 nodes x 1 query head per KV head)
+    "vicuna33b_b16_l1024_n128": (S.vicuna33b(16, 1024, 128), (5,)),
 }
 
 
