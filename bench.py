@@ -182,6 +182,52 @@ def steady_state(args, w: S.Workload, st, stream, barrier):
                     "once per step; prefix length held fixed"}
 
 
+def decode_loop(args, w: S.Workload, st, device):
+    """The library's decode loop (medusa_loop_*): one captured step with root, h and the
+    cache lengths carried in place, replayed back to back from the workload's prefix while
+    the context grows by each step's kept tokens.  Own plan and cache, sized for the run."""
+    import dataclasses
+    from medusa_head_speculative_gb300 import binding as Bnd
+    steps = max(2, min(args.steps, 1000))
+    wl = dataclasses.replace(w, reserve=steps * (w.K + 1) + 128)
+    parent, rank = st["parent"], st["rank"]
+    dtype = Bnd.F32 if w.dtype == "f32" else Bnd.BF16
+    plan = Bnd.Plan(w.B, w.d, w.V, w.K, w.Hq, w.Hkv, w.dh, dtype, wl.capacity, w.s, parent, rank,
+                    rope_base=w.rope_base, page_size=w.page_size,
+                    num_pages=w.B * wl.pages_per_seq if w.page_size else 0)
+    kc, vc, pt = S.kv_cache(wl)
+    kc, vc = kc.to(device), vc.to(device)
+    pt = None if pt is None else pt.to(device)
+    length = torch.tensor(w.lengths, dtype=torch.int32, device=device)
+    ws = torch.empty(plan.workspace_size, dtype=torch.uint8, device=device)
+    i32 = dict(dtype=torch.int32, device=device)
+    h = st["h"].clone()
+    root = torch.empty(w.B, **i32)
+    kv = Bnd.kv_struct(kc, vc, length, length, pt)
+    first = Bnd.outputs_struct(torch.empty(w.B, w.K + 1, **i32), torch.empty(w.B, **i32), None, h, root)
+    Bnd.step(plan, h, None, st["wstruct"], kv, st["acc"], first, ws)       # root from the LM head
+    tokens = torch.empty(steps, w.B, w.K + 1, **i32)
+    n_acc = torch.empty(steps, w.B, **i32)
+    loop = Bnd.Loop(plan, st["wstruct"], kv, st["acc"], h, root, tokens, n_acc, ws)
+    stream = torch.cuda.current_stream(device)
+    torch.cuda.synchronize(device)
+    len0 = [int(x) for x in length.cpu()]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    loop.run(steps)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / steps
+    assert loop.steps() == steps and plan.status() == 0, "decode loop failed"
+    mean_tok = float(n_acc.float().mean())
+    res = {"value": round(1e3 / ms, 2), "unit": "steps/s", "ms_per_step": round(ms, 5),
+           "steps": steps, "mean_tokens_per_step": round(mean_tok, 3),
+           "tokens_per_s": round(1e3 / ms * mean_tok * w.B, 1),
+           "context": [min(len0), int(length.max())], "launch": "cuda_graph (medusa_loop)"}
+    loop.close()
+    return res
+
+
 # ----------------------------------------------------------------------- ranks
 def max_over_ranks(x: float, dist, device) -> float:
     """The maximum of x over all ranks (x itself without a process group)."""
@@ -363,6 +409,7 @@ def run_ours(args, w: S.Workload):
     assert plan.status() == 0, "device status word set during the timed region"
     n_acc_mean = float(st["out"]["n_acc"].float().mean())
     steady = steady_state(args, w, st, stream, barrier)
+    loop = decode_loop(args, w, st, device)
 
     # end to end: h_t from pinned host memory, result (tokens, counts) back, every step
     ke = min(K, 500)
@@ -454,6 +501,7 @@ def run_ours(args, w: S.Workload):
         "steady_state": dict(steady, step_hbm_frac=round(
             steady_bytes(w, n1) / (steady["ms_per_step"] * 1e-3) / 1e9 / hbm, 4),
             step_bytes=steady_bytes(w, n1)),
+        "decode_loop": loop,
         "gpu_launches": int(launches),
         "launch": launch_mode,
     }

@@ -155,7 +155,9 @@ medusa_status medusa_get_status(const medusa_plan* plan, void* stream, uint32_t*
  * h: device [B][d] last hidden state.  root_in: device [B] first token carried from the
  * previous step's root_next, or NULL to take the LM head's greedy token on h.  With
  * root_in given the LM head is not applied to h (it would only yield the root), so a
- * step of the steady-state decode loop reads the LM head once, for verification. */
+ * step of the steady-state decode loop reads the LM head once, for verification.
+ * out->h_next may alias h and out->root_next may alias root_in: both inputs are read
+ * before the step writes its outputs. */
 medusa_status medusa_step(const medusa_plan* plan, const float* h, const int32_t* root_in,
                           const medusa_weights* w, const medusa_kv* kv, medusa_accept acc,
                           const medusa_outputs* out, void* workspace, size_t ws_bytes,
@@ -241,6 +243,33 @@ medusa_status medusa_verify(const medusa_plan* plan, const int32_t* tok, const i
 medusa_status medusa_kv_compact(const medusa_plan* plan, const medusa_kv* kv,
                                 const void* tree_k, const void* tree_v,
                                 const int32_t* path_nodes, const int32_t* n_acc, void* stream);
+
+/* ------------------------------------------------------------------ decode loop */
+/* The steady-state decode loop ([MEDUSA] §3.2: every step's first token is the previous
+ * step's greedy token at the last accepted node, and decoding continues from the hidden
+ * state there).  medusa_loop_create() captures, once, one medusa_step whose state is
+ * carried in place (root_in = root_next = root, h = h_next = h, kv->len_out == kv->len:
+ * the cache grows by each step's kept tokens) followed by the bookkeeping that appends the
+ * step's out_tok [B][K+1] and n_acc [B] to the caller's rings tokens [max_steps][B][K+1] and
+ * n_acc [max_steps][B] (position: steps appended so far, modulo max_steps) as a CUDA graph;
+ * medusa_loop_run() replays it n_steps times on `stream` (asynchronous).
+ *   - h: device [B][d], root: device [B] (e.g. a first medusa_step's h_next and root_next);
+ *     both hold the latest state after every step.
+ *   - Every pointer given here (weights, cache, lengths, state, rings, workspace) is used by
+ *     every replay: keep them allocated, and the plan alive, until medusa_loop_destroy().
+ *   - The cache must have room for the steps to be run (len + K + 1 <= capacity at every
+ *     step); past that MEDUSA_FLAG_KV_CAPACITY is set, as in medusa_step.
+ *   - Creation allocates the loop's small device state (B*(K+2) ints and a counter) and
+ *     captures on a private stream; it launches nothing.
+ * medusa_loop_steps() synchronises `stream` and returns the number of steps appended. */
+typedef struct medusa_loop medusa_loop;
+medusa_status medusa_loop_create(const medusa_plan* plan, const medusa_weights* w,
+                                 const medusa_kv* kv, medusa_accept acc, float* h, int32_t* root,
+                                 int32_t* tokens, int32_t* n_acc, int max_steps, void* workspace,
+                                 size_t ws_bytes, medusa_loop** out);
+medusa_status medusa_loop_run(medusa_loop* loop, int n_steps, void* stream);
+medusa_status medusa_loop_steps(const medusa_loop* loop, void* stream, long long* steps);
+void medusa_loop_destroy(medusa_loop* loop);
 
 /* ------------------------------------------------------------------ tracing */
 /* Per-stage timing (CUDA events recorded on the launching stream around every stage the

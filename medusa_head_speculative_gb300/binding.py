@@ -100,6 +100,11 @@ def lib():
                                       C.POINTER(C.c_int32)]),
         "medusa_tree_greedy": (I, [I, C.POINTER(C.c_int), I, C.POINTER(C.c_double), I,
                                    C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
+        "medusa_loop_create": (I, [P, C.POINTER(Weights), C.POINTER(KV), Accept, P, P, P, P, I, P,
+                                   SZ, C.POINTER(P)]),
+        "medusa_loop_run": (I, [P, I, P]),
+        "medusa_loop_steps": (I, [P, P, C.POINTER(C.c_longlong)]),
+        "medusa_loop_destroy": (None, [P]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -294,3 +299,39 @@ def kv_compact(plan, kv, tk, tv, path_nodes, n_acc, stream=None):
     _check("medusa_kv_compact", lib().medusa_kv_compact(plan.handle, C.byref(kv), ptr(tk), ptr(tv),
                                                         ptr(path_nodes), ptr(n_acc),
                                                         _stream(stream)))
+
+
+class Loop:
+    """Owns a medusa_loop: one medusa_step with its state carried in place (h, root, cache
+    lengths) plus the append to the token rings, captured once as a CUDA graph.  The
+    tensors passed here must outlive the loop (its replays use their addresses)."""
+
+    def __init__(self, plan, wts, kv, accept, h, root, tokens, n_acc, ws):
+        self._keep = (plan, wts, kv, h, root, tokens, n_acc, ws)
+        self.max_steps = tokens.shape[0]
+        out = P()
+        _check("medusa_loop_create",
+               lib().medusa_loop_create(plan.handle, C.byref(wts), C.byref(kv), accept, ptr(h),
+                                        ptr(root), ptr(tokens), ptr(n_acc), self.max_steps,
+                                        ptr(ws), ws.numel() * ws.element_size(), C.byref(out)))
+        self.handle = out
+
+    def run(self, n_steps, stream=None):
+        _check("medusa_loop_run", lib().medusa_loop_run(self.handle, int(n_steps), _stream(stream)))
+
+    def steps(self, stream=None):
+        n = C.c_longlong(0)
+        _check("medusa_loop_steps", lib().medusa_loop_steps(self.handle, _stream(stream), C.byref(n)))
+        return n.value
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().medusa_loop_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+

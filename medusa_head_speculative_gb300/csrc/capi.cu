@@ -975,4 +975,93 @@ medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* r
   return MEDUSA_OK;
 }
 
+// ------------------------------------------------------------------ decode loop
+struct medusa_loop {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int32_t* d_tok = nullptr;      // [B][K+1] tokens of the step in flight
+  int32_t* d_nacc = nullptr;     // [B]
+  long long* d_count = nullptr;  // steps appended so far
+};
+
+void medusa_loop_destroy(medusa_loop* L) {
+  if (!L) return;
+  if (L->exec) cudaGraphExecDestroy(L->exec);
+  if (L->graph) cudaGraphDestroy(L->graph);
+  if (L->d_tok) cudaFree(L->d_tok);
+  if (L->d_nacc) cudaFree(L->d_nacc);
+  if (L->d_count) cudaFree(L->d_count);
+  delete L;
+}
+
+medusa_status medusa_loop_create(const medusa_plan* p, const medusa_weights* w, const medusa_kv* kv,
+                                 medusa_accept acc, float* h, int32_t* root, int32_t* tokens,
+                                 int32_t* n_acc, int max_steps, void* ws, size_t ws_bytes,
+                                 medusa_loop** out) {
+  if (!p || !kv || !h || !root || !tokens || !n_acc || !out || max_steps < 1) return MEDUSA_ERR_INVALID;
+  if (!kv->len_out || (const int32_t*)kv->len_out != kv->len) return MEDUSA_ERR_INVALID;
+  *out = nullptr;
+  medusa_status s = check_weights(p, w, true, true, true);
+  if (s != MEDUSA_OK) return s;
+  if ((s = check_kv(p, kv, true)) != MEDUSA_OK) return s;
+  if ((s = check_accept(acc)) != MEDUSA_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MEDUSA_OK) return s;
+  medusa_loop* L = new (std::nothrow) medusa_loop();
+  if (!L) return MEDUSA_ERR_CUDA;
+  const int B = p->d.B, W = p->K + 1;
+  if (cudaMalloc(&L->d_tok, sizeof(int32_t) * B * W) != cudaSuccess ||
+      cudaMalloc(&L->d_nacc, sizeof(int32_t) * B) != cudaSuccess ||
+      cudaMalloc(&L->d_count, sizeof(long long)) != cudaSuccess ||
+      cudaMemset(L->d_count, 0, sizeof(long long)) != cudaSuccess) {
+    medusa_loop_destroy(L);
+    return MEDUSA_ERR_CUDA;
+  }
+  // One step with its state updated in place (h_next = h, root_next = root, len_out = len),
+  // then the append, captured on a private stream (the legacy default stream cannot
+  // capture).  Per-launch profiling is suspended during the capture.
+  cudaStream_t cap = nullptr;
+  if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) {
+    medusa_loop_destroy(L);
+    return MEDUSA_ERR_CUDA;
+  }
+  const bool prof = p->prof.on;
+  p->prof.on = false;
+  medusa_outputs o{L->d_tok, L->d_nacc, nullptr, h, root};
+  cudaError_t e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+  if (e == cudaSuccess) {
+    s = medusa_step(p, h, root, w, kv, acc, &o, ws, ws_bytes, cap);
+    if (s == MEDUSA_OK && launch_loop_append(L->d_tok, L->d_nacc, B, W, max_steps, L->d_count, tokens,
+                                             n_acc, cap) != cudaSuccess)
+      s = MEDUSA_ERR_CUDA;
+    const cudaError_t e2 = cudaStreamEndCapture(cap, &L->graph);
+    if (s == MEDUSA_OK && e2 != cudaSuccess) s = MEDUSA_ERR_CUDA;
+  } else {
+    s = MEDUSA_ERR_CUDA;
+  }
+  p->prof.on = prof;
+  if (s == MEDUSA_OK && cudaGraphInstantiate(&L->exec, L->graph, 0) != cudaSuccess) s = MEDUSA_ERR_CUDA;
+  cudaStreamDestroy(cap);
+  if (s != MEDUSA_OK) {
+    medusa_loop_destroy(L);
+    return s;
+  }
+  *out = L;
+  return MEDUSA_OK;
+}
+
+medusa_status medusa_loop_run(medusa_loop* L, int n_steps, void* stream) {
+  if (!L || n_steps < 0) return MEDUSA_ERR_INVALID;
+  for (int i = 0; i < n_steps; ++i)
+    if (cudaGraphLaunch(L->exec, S(stream)) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  return MEDUSA_OK;
+}
+
+medusa_status medusa_loop_steps(const medusa_loop* L, void* stream, long long* steps) {
+  if (!L || !steps) return MEDUSA_ERR_INVALID;
+  if (cudaStreamSynchronize(S(stream)) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  if (cudaMemcpy(steps, L->d_count, sizeof(long long), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MEDUSA_ERR_CUDA;
+  return MEDUSA_OK;
+}
+
 }  // extern "C"

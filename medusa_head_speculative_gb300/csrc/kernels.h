@@ -160,6 +160,12 @@ cudaError_t launch_kv_compact(const CompactArgs& a, cudaStream_t st);
 cudaError_t launch_verify_commit(const VerifyArgs& v, const CompactArgs& c, int32_t* row_cnt,
                                  int32_t* seq_cnt, float* parts, cudaStream_t st);
 
+// Decode loop: ring_tok[c % max_steps] = tok ([B][W]), ring_nacc[c % max_steps] = n_acc,
+// then *count = c + 1, where c = *count (one CTA).
+cudaError_t launch_loop_append(const int32_t* tok, const int32_t* n_acc, int B, int W, int max_steps,
+                               long long* count, int32_t* ring_tok, int32_t* ring_nacc,
+                               cudaStream_t st);
+
 // Plan fields used by the workspace-free heads entry point (defined in capi.cu).
 struct HeadsPlanView {
   medusa_dims dims;
