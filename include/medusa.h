@@ -58,7 +58,7 @@ typedef enum {
 } medusa_status;
 
 enum { MEDUSA_F32 = 0, MEDUSA_BF16 = 1 };
-enum { MEDUSA_GREEDY = 0, MEDUSA_TYPICAL = 1 };
+enum { MEDUSA_GREEDY = 0, MEDUSA_TYPICAL = 1, MEDUSA_REJECT = 2 };
 
 /* device status word bits */
 #define MEDUSA_FLAG_TOKEN_RANGE 0x1u  /* a selected token id fell outside [0, V) */
@@ -118,12 +118,28 @@ typedef struct {
   int32_t* len_out;           /* device [B] lengths after compaction (may alias len) */
 } medusa_kv;
 
-/* Acceptance rule ([MEDUSA] §3.4 Typical Acceptance Scheme). */
+/* Acceptance rule ([MEDUSA] §3.4 Typical Acceptance Scheme and the speculative-decoding
+ * rejection rule it replaces).
+ *   MEDUSA_GREEDY   a candidate is kept iff it is its parent's greedy token.
+ *   MEDUSA_TYPICAL  kept iff p(x) > min(eps, delta * exp(-H(p))), p = softmax(z / T).
+ *   MEDUSA_REJECT   rejection sampling with the heads' top-s tokens as point-mass drafts:
+ *                   from the root, the current node's children are tried in rank order,
+ *                   child x kept iff u < p(x) / R (R = probability mass not yet rejected
+ *                   at this node, 1 at first), else R -= p(x); the first kept child becomes
+ *                   the current node.  Where no child is kept, the next step's root is
+ *                   drawn from p at the current node without the rejected tokens (the
+ *                   smallest token whose cumulative weight exceeds u_final times the
+ *                   remaining total).  The emitted tokens are then distributed as p.
+ *                   uniforms: device [B][1 + 16 K] floats in [0, 1): [b][0] = u_final,
+ *                   [b][1 + 16 (d - 1) + j] = u of the j-th child tried at depth d.  A new
+ *                   set is needed for every step, so the decode loop rejects this mode.
+ * Temperature 0 is greedy in every mode. */
 typedef struct {
-  int mode;           /* MEDUSA_GREEDY or MEDUSA_TYPICAL */
-  float temperature;  /* typical: softmax temperature; 0 means greedy */
+  int mode;           /* MEDUSA_GREEDY, MEDUSA_TYPICAL or MEDUSA_REJECT */
+  float temperature;  /* typical / reject: softmax temperature; 0 means greedy */
   float eps;          /* typical: hard threshold epsilon */
   float delta;        /* typical: entropy-threshold multiplier delta */
+  const float* uniforms;  /* reject: see above; unused (may be NULL) otherwise */
 } medusa_accept;
 
 /* Step outputs (device). */
@@ -232,11 +248,14 @@ medusa_status medusa_verify_logits(const medusa_plan* plan, const medusa_weights
  * handling): the root is kept; candidate c is accepted iff tok[c] == am[parent[c]]
  * (greedy, or typical at T = 0) or log p_parent(tok[c]) > min(log eps, log delta - H)
  * (typical).  The longest run of accepted nodes along a root->leaf path wins, ties to the
- * lowest path index.  Writes every medusa_outputs field; h_next is hprime at the last kept
- * node and root_next its greedy token. */
+ * lowest path index.  MEDUSA_REJECT walks the tree instead (see medusa_accept) and draws
+ * root_next from `logits` ([B][N+1][V], as written by medusa_verify_logits; required in that
+ * mode, unused and may be NULL otherwise).  Writes every medusa_outputs field; h_next is
+ * hprime at the last kept node and root_next its greedy token (or the draw). */
 medusa_status medusa_verify(const medusa_plan* plan, const int32_t* tok, const int32_t* am,
-                            const float* stats, const int32_t* retrieve, const float* hprime,
-                            medusa_accept acc, const medusa_outputs* out, void* stream);
+                            const float* stats, const float* logits, const int32_t* retrieve,
+                            const float* hprime, medusa_accept acc, const medusa_outputs* out,
+                            void* stream);
 /* (h) KV compaction ([READING] section 3: only the accepted path stays in the cache):
  * slots len .. len+n_acc-1 receive the tree keys/values of path_nodes; len_out = len +
  * n_acc.  Slots past capacity are not written and set MEDUSA_FLAG_KV_CAPACITY. */

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libmedusa.so")
 MEDUSA_OK, MEDUSA_ERR_INVALID, MEDUSA_ERR_UNSUPPORTED = 0, -1, -2
 MEDUSA_ERR_CUDA, MEDUSA_ERR_DEVICE, MEDUSA_ERR_WORKSPACE = -3, -4, -6
 F32, BF16 = 0, 1
-GREEDY, TYPICAL = 0, 1
+GREEDY, TYPICAL, REJECT = 0, 1, 2
 MAX_HEADS, MAX_TOPS, MAX_NODES = 8, 16, 256
 FLAG_TOKEN_RANGE, FLAG_KV_CAPACITY, FLAG_PAGE_RANGE, FLAG_NONFINITE = 1, 2, 4, 8
 STATUS_NAMES = {0: "OK", -1: "INVALID", -2: "UNSUPPORTED", -3: "CUDA", -4: "DEVICE", -6: "WORKSPACE"}
@@ -51,7 +51,7 @@ class KV(C.Structure):
 
 class Accept(C.Structure):
     _fields_ = [("mode", C.c_int), ("temperature", C.c_float), ("eps", C.c_float),
-                ("delta", C.c_float)]
+                ("delta", C.c_float), ("uniforms", C.c_void_p)]
 
 
 class KernelTime(C.Structure):
@@ -92,7 +92,7 @@ def lib():
         "medusa_tree_attention": (I, [P, P, C.POINTER(KV), P, P, P, P, P, SZ, P]),
         "medusa_layer_out": (I, [P, C.POINTER(Weights), P, P, P, P, SZ, P]),
         "medusa_verify_logits": (I, [P, C.POINTER(Weights), P, P, Accept, P, P, P, P, SZ, P]),
-        "medusa_verify": (I, [P, P, P, P, P, P, Accept, C.POINTER(Outputs), P]),
+        "medusa_verify": (I, [P, P, P, P, P, P, P, Accept, C.POINTER(Outputs), P]),
         "medusa_kv_compact": (I, [P, C.POINTER(KV), P, P, P, P, P]),
         "medusa_profile_start": (I, [P, I]),
         "medusa_profile_stop": (I, [P, P, C.POINTER(KernelTime), I, C.POINTER(I), C.POINTER(I)]),
@@ -225,8 +225,9 @@ def kv_struct(k, v, length, len_out=None, page_table=None):
     return KV(ptr(k), ptr(v), ptr(page_table), ptr(length), ptr(len_out))
 
 
-def accept_struct(mode="greedy", temperature=0.0, eps=0.09, delta=0.3):
-    return Accept(TYPICAL if mode == "typical" else GREEDY, temperature, eps, delta)
+def accept_struct(mode="greedy", temperature=0.0, eps=0.09, delta=0.3, uniforms=None):
+    code = {"typical": TYPICAL, "reject": REJECT}.get(mode, GREEDY)
+    return Accept(code, temperature, eps, delta, ptr(uniforms))
 
 
 def outputs_struct(out_tok, n_acc, path_nodes, h_next, root_next):
@@ -289,10 +290,10 @@ def verify_logits(plan, wts, hprime, tok, accept, logits, am, stats, ws, stream=
                                       ws.numel() * ws.element_size(), _stream(stream)))
 
 
-def verify(plan, tok, am, stats, retrieve, hprime, accept, outs, stream=None):
+def verify(plan, tok, am, stats, retrieve, hprime, accept, outs, stream=None, logits=None):
     _check("medusa_verify", lib().medusa_verify(plan.handle, ptr(tok), ptr(am), ptr(stats),
-                                                ptr(retrieve), ptr(hprime), accept, C.byref(outs),
-                                                _stream(stream)))
+                                                ptr(logits), ptr(retrieve), ptr(hprime), accept,
+                                                C.byref(outs), _stream(stream)))
 
 
 def kv_compact(plan, kv, tk, tv, path_nodes, n_acc, stream=None):

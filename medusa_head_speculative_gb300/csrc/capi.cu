@@ -454,8 +454,11 @@ VerifyArgs verify_args(const medusa_plan* p, const int32_t* tok, medusa_accept a
   v.K = p->K;
   v.P = p->P;
   v.d = p->d.d;
-  v.typical = acc.mode == MEDUSA_TYPICAL && acc.temperature > 0.f;
+  // rejection sampling needs the same per-row softmax statistics as typical acceptance
+  v.reject = acc.mode == MEDUSA_REJECT && acc.temperature > 0.f;
+  v.typical = (acc.mode == MEDUSA_TYPICAL && acc.temperature > 0.f) || v.reject;
   v.temperature = v.typical ? acc.temperature : 1.f;
+  v.uniforms = v.reject ? acc.uniforms : nullptr;
   v.eps = acc.eps;
   v.delta = acc.delta;
   v.status = p->d_status;
@@ -497,10 +500,11 @@ medusa_status vlogits_impl(const medusa_plan* p, const medusa_weights* w, const 
 }
 
 medusa_status accept_impl(const medusa_plan* p, const int32_t* tok, const int32_t* am,
-                          const float* stats, const int32_t* retr, const float* hp,
-                          medusa_accept acc, int32_t* out_tok, int32_t* n_acc, int32_t* path,
-                          float* h_next, int32_t* root_next, cudaStream_t st) {
+                          const float* stats, const float* logits, const int32_t* retr,
+                          const float* hp, medusa_accept acc, int32_t* out_tok, int32_t* n_acc,
+                          int32_t* path, float* h_next, int32_t* root_next, cudaStream_t st) {
   VerifyArgs v = verify_args(p, tok, acc);
+  v.logits = logits;                           // rejection sampling draws from these
   v.am = const_cast<int32_t*>(am);
   v.stats = const_cast<float*>(stats);
   v.retrieve = retr;
@@ -567,11 +571,13 @@ medusa_status check_kv(const medusa_plan* p, const medusa_kv* kv, bool compact) 
 }
 
 medusa_status check_accept(medusa_accept a) {
-  if (a.mode != MEDUSA_GREEDY && a.mode != MEDUSA_TYPICAL) return MEDUSA_ERR_INVALID;
-  if (a.mode == MEDUSA_TYPICAL) {
-    if (!(a.temperature >= 0.f) || !std::isfinite(a.temperature)) return MEDUSA_ERR_INVALID;
-    if (a.temperature > 0.f && (!(a.eps > 0.f) || !(a.delta > 0.f))) return MEDUSA_ERR_INVALID;
-  }
+  if (a.mode != MEDUSA_GREEDY && a.mode != MEDUSA_TYPICAL && a.mode != MEDUSA_REJECT)
+    return MEDUSA_ERR_INVALID;
+  if (a.mode != MEDUSA_GREEDY && (!(a.temperature >= 0.f) || !std::isfinite(a.temperature)))
+    return MEDUSA_ERR_INVALID;
+  if (a.mode == MEDUSA_TYPICAL && a.temperature > 0.f && (!(a.eps > 0.f) || !(a.delta > 0.f)))
+    return MEDUSA_ERR_INVALID;
+  if (a.mode == MEDUSA_REJECT && a.temperature > 0.f && !a.uniforms) return MEDUSA_ERR_INVALID;
   return MEDUSA_OK;
 }
 
@@ -887,14 +893,16 @@ medusa_status medusa_verify_logits(const medusa_plan* p, const medusa_weights* w
 }
 
 medusa_status medusa_verify(const medusa_plan* p, const int32_t* tok, const int32_t* am,
-                            const float* stats, const int32_t* retrieve, const float* hprime,
-                            medusa_accept acc, const medusa_outputs* out, void* stream) {
+                            const float* stats, const float* logits, const int32_t* retrieve,
+                            const float* hprime, medusa_accept acc, const medusa_outputs* out,
+                            void* stream) {
   EntryScope scope("medusa_verify");
   if (!p || !tok || !am || !stats || !retrieve || !hprime || !out) return MEDUSA_ERR_INVALID;
   if (!out->out_tok || !out->n_acc || !out->h_next || !out->root_next) return MEDUSA_ERR_INVALID;
   medusa_status s = check_accept(acc);
   if (s != MEDUSA_OK) return s;
-  return accept_impl(p, tok, am, stats, retrieve, hprime, acc, out->out_tok, out->n_acc,
+  if (acc.mode == MEDUSA_REJECT && acc.temperature > 0.f && !logits) return MEDUSA_ERR_INVALID;
+  return accept_impl(p, tok, am, stats, logits, retrieve, hprime, acc, out->out_tok, out->n_acc,
                      out->path_nodes, out->h_next, out->root_next, S(stream));
 }
 
@@ -1001,6 +1009,7 @@ medusa_status medusa_loop_create(const medusa_plan* p, const medusa_weights* w, 
   if (!p || !kv || !h || !root || !tokens || !n_acc || !out || max_steps < 1) return MEDUSA_ERR_INVALID;
   if (!kv->len_out || (const int32_t*)kv->len_out != kv->len) return MEDUSA_ERR_INVALID;
   *out = nullptr;
+  if (acc.mode == MEDUSA_REJECT && acc.temperature > 0.f) return MEDUSA_ERR_UNSUPPORTED;   // fixed uniforms
   medusa_status s = check_weights(p, w, true, true, true);
   if (s != MEDUSA_OK) return s;
   if ((s = check_kv(p, kv, true)) != MEDUSA_OK) return s;

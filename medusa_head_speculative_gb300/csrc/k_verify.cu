@@ -216,7 +216,118 @@ cudaError_t launch_verify_stats(const VerifyArgs& a, cudaStream_t st) {
 
 // Acceptance of sequence b by one CTA; thread c decides candidate c, thread p walks path
 // p.  Statistics are read through L2 (other CTAs of the same launch may have written them).
+// Rejection-sampling verification of sequence b (whole CTA).  Thread 0 walks the tree from
+// the root: the current node's children, in packed (rank) order, are tested with their own
+// uniforms against the mass R not yet rejected at that node (child x kept iff u R < p(x),
+// else R -= p(x) and x leaves the distribution); the first kept child becomes the current
+// node.  The CTA then draws the next root from the current node's remaining distribution
+// by inverse CDF in token order: per-thread contiguous token ranges, their sums scanned in
+// thread order, and the thread whose range holds u_final times the total walks it.
+__device__ void reject_seq(const VerifyArgs& a, int b) {
+  __shared__ int s_path[MEDUSA_MAX_HEADS + 1];
+  __shared__ int s_excl[kTops];
+  __shared__ int s_m, s_nex, s_v;
+  __shared__ float s_sum[1024];
+  const int tid = threadIdx.x;
+  const long rb = (long)b * a.n1;
+  const int W = a.K + 1, ustride = 1 + 16 * a.K;
+  const float* uni = a.uniforms + (long)b * ustride;
+  if (tid == 0) {
+    int u = 0, m = 0, nex = 0;
+    s_path[0] = 0;
+    for (;;) {
+      const float* su = a.stats + (rb + u) * 4;
+      const float mu = __ldcg(su), lsu = __ldcg(su + 1);   // max z/T, log sum e^(z/T - max)
+      float R = 1.f;
+      int j = 0, next = -1;
+      nex = 0;
+      for (int c = u + 1; c < a.n1 && next < 0; ++c) {
+        if (a.parent[c] != u) continue;
+        const float px = __expf(__ldcg(a.stats + (rb + c) * 4 + 3) - mu - lsu);   // p_u(tok_c)
+        const float uu = __ldg(uni + 1 + 16 * m + j);
+        if (uu * R < px) {
+          next = c;
+        } else {
+          R -= px;
+          if (nex < kTops) s_excl[nex++] = a.tok[rb + c];
+          ++j;
+        }
+      }
+      if (next < 0 || m + 1 >= W) break;
+      s_path[++m] = next;
+      u = next;
+    }
+    s_m = m;
+    s_nex = nex;
+    s_v = -1;
+  }
+  __syncthreads();
+  const int m = s_m, nex = s_nex, last = s_path[m];
+  if (!a.logits) {                                       // checked on the host; never read null
+    if (tid == 0) set_flag(a.status, MEDUSA_FLAG_TOKEN_RANGE);
+    return;
+  }
+  const float* z = a.logits + (rb + last) * a.V;
+  const float mu = __ldcg(a.stats + (rb + last) * 4), invT = 1.f / a.temperature;
+  auto weight = [&](int v) {
+    for (int e = 0; e < nex; ++e)
+      if (s_excl[e] == v) return 0.f;
+    return __expf(__ldcg(z + v) * invT - mu);
+  };
+  const int chunk = (a.V + blockDim.x - 1) / blockDim.x;
+  const int v0 = min(a.V, tid * chunk), v1 = min(a.V, v0 + chunk);
+  float own = 0.f;
+  for (int v = v0; v < v1; ++v) own += weight(v);
+  s_sum[tid] = own;
+  __syncthreads();
+  if (tid == 0) {                                        // exclusive scan in thread order
+    float c = 0.f;
+    for (int t = 0; t < (int)blockDim.x; ++t) {
+      const float x = s_sum[t];
+      s_sum[t] = c;
+      c += x;
+    }
+    s_sum[blockDim.x] = c;                               // blockDim.x < 1024
+  }
+  __syncthreads();
+  const float total = s_sum[blockDim.x], thr = __ldg(uni) * total;
+  const float before = s_sum[tid];
+  if (own > 0.f && before <= thr && thr < before + own) {
+    float c = before;
+    for (int v = v0; v < v1; ++v) {
+      const float w = weight(v);
+      if (w > 0.f && c + w > thr) { s_v = v; break; }
+      c += w;
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && s_v < 0) {                             // thr at the very top (rounding)
+    for (int v = a.V - 1; v >= 0; --v)
+      if (weight(v) > 0.f) { s_v = v; break; }
+  }
+  __syncthreads();
+  if (tid < W) {
+    const int node = tid <= m ? s_path[tid] : -1;
+    if (a.path_nodes) a.path_nodes[(long)b * W + tid] = node;
+    a.out_tok[(long)b * W + tid] = node >= 0 ? a.tok[rb + node] : -1;
+    if (tid == 0) {
+      a.n_acc[b] = m + 1;
+      int v = s_v;
+      if (v < 0 || v >= a.V) { set_flag(a.status, MEDUSA_FLAG_TOKEN_RANGE); v = 0; }
+      a.root_next[b] = v;
+    }
+  }
+  const float4* __restrict__ src = reinterpret_cast<const float4*>(a.hprime + (rb + last) * a.d);
+  float4* __restrict__ dst = reinterpret_cast<float4*>(a.h_next + (long)b * a.d);
+  for (int j = tid; j < a.d / 4; j += blockDim.x) dst[j] = src[j];
+  __syncthreads();
+}
+
 __device__ void accept_seq(const VerifyArgs& a, int b) {
+  if (a.reject) {
+    reject_seq(a, b);
+    return;
+  }
   __shared__ int acc[MEDUSA_MAX_NODES];
   __shared__ int sret[MEDUSA_MAX_NODES * (MEDUSA_MAX_HEADS + 1)];
   __shared__ float sv[32];

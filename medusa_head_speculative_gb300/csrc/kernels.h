@@ -136,7 +136,8 @@ struct VerifyArgs {
   const float* logits;      // [M][V]
   const int32_t* tok; const int32_t* parent; const int32_t* depth;
   int B, n1, V, K, P, d;
-  int typical; float temperature, eps, delta;
+  int typical; float temperature, eps, delta;       // typical: softmax statistics per row
+  int reject; const float* uniforms;                // rejection sampling: [B][1 + 16 K]
   int32_t* am; float* stats;                        // [M], [M][4]
   const int32_t* retrieve; const float* hprime;     // [n1][K+1], [M][d]
   int32_t* out_tok; int32_t* n_acc; int32_t* path_nodes; float* h_next; int32_t* root_next;

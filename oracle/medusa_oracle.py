@@ -31,6 +31,19 @@ Readings where the pages are silent or disagree (each also listed in the design 
   R7  Greedy tree construction adds, at each step, the frontier node with the largest
       path product of marginal accuracies ([NOTES] section 4 E[L] over all nodes);
       ties go to the lexicographically smaller rank path.
+  R8  Rejection-sampling verification ([MEDUSA] §3.4, the speculative-decoding rule:
+      accept a draft x with probability min(1, p(x)/q(x)), else draw from
+      norm(max(0, p - q))).  The candidates are the heads' top-s tokens, i.e. drafts
+      with a point-mass q = delta_x, so x is accepted with probability p(x) and a
+      rejection removes x from p.  Walking from the root, the current node's children
+      are tried in packed (rank) order against the remaining mass R: child x is accepted
+      iff u < p(x) / R (u its own uniform), else R -= p(x); the first accepted child
+      becomes the current node (fresh p, R = 1).  When no child is accepted (or the node
+      has none) the next token is drawn from the remaining distribution at the current
+      node by inverse CDF in token order (the smallest v whose cumulative remaining
+      weight exceeds u_final times the remaining total); it is the next step's root.
+      p = softmax(z / T); T = 0 is greedy.  Uniforms are inputs: uniforms[0] for the
+      draw, uniforms[1 + (d - 1) * 16 + j] for the j-th child tried at depth d.
 """
 from __future__ import annotations
 
@@ -350,6 +363,65 @@ def accept_flags(spec, tok, zv, am, am_margin, accept):
     return acc, margin
 
 
+NEAR_P = 1e-4   # rejection sampling: decisions within this (probability units) are flagged
+
+
+def children(spec, u):
+    """Packed indices of node u's children, in packed (rank) order."""
+    return [c for c in range(1, spec.N + 1) if spec.parent[c] == u]
+
+
+def inverse_cdf_draw(weights, u):
+    """The smallest index v with sum(weights[:v+1]) > u * sum(weights) (R8), and the
+    distance of that threshold to the nearest cumulative boundary, in units of the total.
+    Zero weights are never drawn."""
+    total = float(np.sum(weights))
+    thr = u * total
+    cum = 0.0
+    last = -1
+    for v, w in enumerate(weights):
+        if w <= 0.0:
+            continue
+        last = v
+        if cum + w > thr:
+            return v, min(thr - cum, cum + w - thr) / total
+        cum += w
+    return last, 0.0
+
+
+def rejection_walk(spec, tok, zv, T, uniforms):
+    """Rejection-sampling verification of the candidate tree (R8).
+
+    tok: [N+1] node tokens; zv: [N+1][V] verification logits; uniforms: [1 + 16 K].
+    Returns (packed indices of the kept nodes root..last, the drawn next token, the
+    smallest decision margin in probability units)."""
+    path = [0]
+    u = 0
+    margin = math.inf
+    while True:
+        p = softmax_T(zv[u], T)
+        R = 1.0
+        excluded = []
+        nxt = None
+        d = len(path)                                  # depth of the children tried
+        for j, c in enumerate(children(spec, u)):
+            x = int(tok[c])
+            uu = float(uniforms[1 + (d - 1) * 16 + j])
+            margin = min(margin, abs(uu * R - p[x]))
+            if uu * R < p[x]:
+                nxt = c
+                break
+            R -= p[x]
+            excluded.append(x)
+        if nxt is None:
+            w = p.copy()
+            w[excluded] = 0.0
+            v, mar = inverse_cdf_draw(w, float(uniforms[0]))
+            return np.array(path, dtype=np.int64), v, min(margin, mar)
+        path.append(nxt)
+        u = nxt
+
+
 def longest_accepted(spec, acc):
     """The longest accepted prefix among all root -> leaf paths (R6).
 
@@ -380,6 +452,7 @@ class StepResult:
     topk_margin: np.ndarray = None
     root: int = 0
     root_margin: float = math.inf
+    rs_margin: float = math.inf    # rejection sampling: smallest decision margin (R8)
     tok: np.ndarray = None         # [N+1]
     pos: np.ndarray = None         # [N+1]
     q: np.ndarray = None           # [N+1][Hq][dh]
@@ -478,7 +551,22 @@ def medusa_step(wts, h, kc, vc, spec, dims, accept, root=None, s=None):
         r.am[n], r.am_margin[n] = argmax_lowest(r.zv[n])
 
     # (5) acceptance of each candidate, then the longest accepted prefix
-    r.acc, r.acc_margin = accept_flags(spec, r.tok, r.zv, r.am, r.am_margin, accept)
+    T = accept.get("temperature", 0.0)
+    if accept["mode"] == "reject" and T > 0.0:
+        # R8: rejection sampling walks the tree with the given uniforms
+        r.path_nodes, r.root_next, r.rs_margin = rejection_walk(spec, r.tok, r.zv, T,
+                                                                accept["uniforms"])
+        r.m = len(r.path_nodes) - 1
+        r.acc = np.zeros(n1, dtype=np.int64)
+        r.acc[r.path_nodes] = 1
+        r.acc_margin = np.full(n1, np.inf)
+        r.out_tok = r.tok[r.path_nodes]
+        last = int(r.path_nodes[-1])
+        r.h_next = r.hp[last].copy()
+        r.kv_new = (r.k[r.path_nodes].copy(), r.v[r.path_nodes].copy())
+        return r
+    greedy_accept = dict(accept, mode="greedy") if accept["mode"] == "reject" else accept
+    r.acc, r.acc_margin = accept_flags(spec, r.tok, r.zv, r.am, r.am_margin, greedy_accept)
     r.path_len, r.best, r.m, r.path_nodes = longest_accepted(spec, r.acc)
     r.out_tok = r.tok[r.path_nodes]
     last = int(r.path_nodes[-1])

@@ -25,7 +25,8 @@ import numpy as np
 import torch
 
 _TAGS = {"w1": 1, "w2": 2, "lm": 3, "emb": 4, "wq": 5, "wk": 6, "wv": 7, "wo": 8,
-         "h": 9, "kc": 10, "vc": 11, "len": 12, "pages": 13, "perm": 14, "rho": 15}
+         "h": 9, "kc": 10, "vc": 11, "len": 12, "pages": 13, "perm": 14, "rho": 15,
+         "uni": 16}
 
 
 @dataclass(frozen=True)
@@ -145,6 +146,14 @@ def weights(w: Workload) -> dict:
 def hidden(w: Workload) -> torch.Tensor:
     """Last hidden state h_t [B][d] as fp32 holding dtype-rounded N(0,1) values."""
     return _normal(w, "h", (w.B, w.d), 1.0).to(torch.float32)
+
+
+def uniforms(w: Workload, step: int = 0) -> torch.Tensor:
+    """Uniform draws in [0, 1) for rejection-sampling verification, [B][1 + 16 K] float32:
+    [b][0] for the final draw, [b][1 + 16 (d - 1) + j] for the j-th child tried at depth d.
+    One seeded stream per step."""
+    a = _rng(w, "uni", step).random((w.B, 1 + 16 * w.K), dtype=np.float32)
+    return torch.from_numpy(a)
 
 
 def kv_prefix(w: Workload, b: int):

@@ -67,6 +67,7 @@ class Device:
     ws: torch.Tensor
     spec: O.TreeSpec
     cpu: dict = field(default_factory=dict)
+    uni: torch.Tensor = None          # rejection sampling: device uniforms [B][1 + 16 K]
 
 
 def setup(w: S.Workload, wts_cpu=None, h_cpu=None):
@@ -85,11 +86,26 @@ def setup(w: S.Workload, wts_cpu=None, h_cpu=None):
                  torch.tensor(w.lengths, dtype=torch.int32, device="cuda"),
                  torch.empty(plan.workspace_size, dtype=torch.uint8, device="cuda"), spec)
     dev.cpu = {"wts": wts_cpu, "h": h_cpu}
+    if w.mode == "reject":
+        dev.uni = S.uniforms(w).cuda()
     return dev
 
 
-def accept_of(w: S.Workload):
-    return {"mode": w.mode, "temperature": w.temperature, "eps": w.eps, "delta": w.delta}
+def accept_of(w: S.Workload, dev=None):
+    """Acceptance parameters for the binding (dev given: with the device uniforms of a
+    rejection-sampling workload)."""
+    a = {"mode": w.mode, "temperature": w.temperature, "eps": w.eps, "delta": w.delta}
+    if w.mode == "reject" and dev is not None:
+        a["uniforms"] = dev.uni
+    return a
+
+
+def oracle_accept(w: S.Workload, b: int):
+    """The same parameters for the oracle's sequence b."""
+    a = {"mode": w.mode, "temperature": w.temperature, "eps": w.eps, "delta": w.delta}
+    if w.mode == "reject":
+        a["uniforms"] = S.uniforms(w)[b].numpy().astype(np.float64)
+    return a
 
 
 def run_stages(dev: Device, root_in=None):
@@ -118,7 +134,7 @@ def run_stages(dev: Device, root_in=None):
     Bnd.tree_attention(p, q, kv, tk, tv, mask, o, dev.ws)
     hp = torch.empty(B, n1, d, **f32)
     Bnd.layer_out(p, dev.wstruct, tok, o, hp, dev.ws)
-    acc = Bnd.accept_struct(**accept_of(w))
+    acc = Bnd.accept_struct(**accept_of(w, dev))
     vlog = torch.empty(B, n1, V, **f32)
     am = torch.empty(B, n1, **i32)
     stats = torch.empty(B, n1, 4, **f32)
@@ -129,7 +145,7 @@ def run_stages(dev: Device, root_in=None):
     h_next = torch.empty(B, d, **f32)
     root_next = torch.empty(B, **i32)
     outs = Bnd.outputs_struct(out_tok, n_acc, path, h_next, root_next)
-    Bnd.verify(p, tok, am, stats, retr, hp, acc, outs)
+    Bnd.verify(p, tok, am, stats, retr, hp, acc, outs, logits=vlog)
     torch.cuda.synchronize()
     for name, t in [("logits", logits), ("topk_tok", ttok), ("topk_val", tval), ("root", root),
                     ("tok", tok), ("pos", pos), ("mask", mask), ("retrieve", retr), ("q", q),
@@ -154,7 +170,7 @@ def run_step(dev: Device, root_in=None, len_out=None):
     len_out = dev.length if len_out is None else len_out
     kv = Bnd.kv_struct(dev.kc, dev.vc, dev.length, len_out, dev.pt)
     outs = Bnd.outputs_struct(out_tok, n_acc, path, h_next, root_next)
-    Bnd.step(p, dev.h, root_in, dev.wstruct, kv, Bnd.accept_struct(**accept_of(w)), outs, dev.ws)
+    Bnd.step(p, dev.h, root_in, dev.wstruct, kv, Bnd.accept_struct(**accept_of(w, dev)), outs, dev.ws)
     torch.cuda.synchronize()
     return dict(out_tok=out_tok.cpu().numpy(), n_acc=n_acc.cpu().numpy(), path=path.cpu().numpy(),
                 h_next=h_next, root_next=root_next, len_out=len_out.cpu().numpy())
@@ -165,7 +181,7 @@ def oracle_step(dev: Device, b: int, ow=None, root=None):
     ow = ow if ow is not None else O.oracle_weights(dev.cpu["wts"])
     k, v = S.kv_prefix(w, b)
     dims = {"Hq": w.Hq, "Hkv": w.Hkv, "dh": w.dh, "rope_base": w.rope_base}
-    return O.medusa_step(ow, dev.cpu["h"][b], k, v, dev.spec, dims, accept_of(w), root=root,
+    return O.medusa_step(ow, dev.cpu["h"][b], k, v, dev.spec, dims, oracle_accept(w, b), root=root,
                          s=list(w.s))
 
 
@@ -224,6 +240,20 @@ def compare_sequence(g: dict, r: O.StepResult, b: int, spec: O.TreeSpec, w: S.Wo
             if r.am_margin[n] < NEAR:
                 raise Flagged(f"argmax node {n}")
             raise AssertionError(f"argmax node {n}")
+    if w.mode == "reject" and w.temperature > 0:
+        # rejection sampling: the walk and the draw, flagged within NEAR_P of a boundary
+        gm = int(g["n_acc"][b]) - 1
+        same = (gm == r.m and list(g["path"][b, :gm + 1]) == list(r.path_nodes)
+                and g["root_next"][b] == r.root_next)
+        if not same:
+            if r.rs_margin < O.NEAR_P:
+                raise Flagged("rejection sampling")
+            raise AssertionError(f"rejection walk {g['path'][b]} -> {g['root_next'][b]} != "
+                                 f"{r.path_nodes} -> {r.root_next}")
+        assert list(g["out_tok"][b, :gm + 1]) == list(r.out_tok)
+        assert (g["out_tok"][b, gm + 1:] == -1).all()
+        assert close(g["h_next"][b], r.h_next) <= 0, "h_next"
+        return
     # acceptance: recompute the GPU's decisions from its statistics only to locate flags
     for c in range(1, n1):
         if r.acc_margin[c] < NEAR:

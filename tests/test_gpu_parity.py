@@ -39,6 +39,9 @@ CASES = {
     "mid_n150_mha": (_mid(B=2, Hq=4, Hkv=4, N=150, lengths=(70, 200)), None),
     "vicuna7b": (S.workload("vicuna7b"), None),
     "vicuna7b_typical": (S.workload("vicuna7b_typical"), None),
+    # rejection sampling with seeded uniforms (mostly draws at the root on random weights)
+    "mid_reject": (_mid(mode="reject", temperature=0.8), None),
+    "vicuna7b_reject": (S.workload("vicuna7b", mode="reject", temperature=0.7), None),
     "vicuna13b": (S.workload("vicuna13b"), (0, 5)),
     "zephyr7b": (S.workload("zephyr7b"), (3, 12)),
     "vicuna33b_b4_l1024_n16": (S.vicuna33b(4, 1024, 16), (2,)),
@@ -297,3 +300,67 @@ def test_step_writes_stay_inside_the_buffers():
                 L = w.lengths[b]
                 assert torch.equal(kc[b, :L], kref[b, :L])
                 assert torch.equal(kc[b, L + int(n_acc[b]):], kref[b, L + int(n_acc[b]):])
+
+
+def test_reject_on_planted_tiny_model_follows_the_oracle_over_steps():
+    """Rejection sampling on a model whose heads are usually right: candidates are accepted
+    and the walk goes deep; each step (fresh uniforms) matches the oracle's."""
+    import dataclasses as dc
+    w = dc.replace(S.workload("tiny"), mode="reject", temperature=1.0)
+    wts = S.planted_weights(w)
+    h0 = wts["emb"][7].float().unsqueeze(0).clone()
+    dev = setup(w, wts_cpu=wts, h_cpu=h0)
+    ow = O.oracle_weights(wts)
+    dims = {"Hq": w.Hq, "Hkv": w.Hkv, "dh": w.dh, "rope_base": w.rope_base}
+    k, v = S.kv_prefix(w, 0)
+    k, v = k.double().numpy(), v.double().numpy()
+    h = h0[0].double().numpy()
+    root = None
+    deepest = 0
+    for step in range(6):
+        dev.uni = S.uniforms(w, step).cuda()
+        acc = {"mode": "reject", "temperature": 1.0, "eps": w.eps, "delta": w.delta,
+               "uniforms": S.uniforms(w, step)[0].numpy().astype(np.float64)}
+        r = O.medusa_step(ow, h, k, v, dev.spec, dims, acc,
+                          root=None if root is None else int(root[0]), s=list(w.s))
+        g = run_step(dev, root_in=root)
+        gm = int(g["n_acc"][0]) - 1
+        if r.rs_margin >= O.NEAR_P:
+            assert list(g["path"][0, :gm + 1]) == list(r.path_nodes), step
+            assert int(g["root_next"][0]) == r.root_next, step
+        else:
+            break
+        deepest = max(deepest, gm)
+        # carry the state: the cache grows by the kept nodes' keys/values (oracle side)
+        k = np.concatenate([k, r.kv_new[0]])
+        v = np.concatenate([v, r.kv_new[1]])
+        h = r.h_next
+        dev.h = g["h_next"]
+        root = g["root_next"]
+    assert deepest >= 1
+    assert dev.plan.status() == 0
+
+
+def test_reject_at_temperature_zero_is_greedy():
+    import dataclasses as dc
+    wg = _mid()
+    wr = dc.replace(wg, mode="reject", temperature=0.0)
+    g1 = run_stages(setup(wg))
+    g2 = run_stages(setup(wr))
+    np.testing.assert_array_equal(g1["out_tok"], g2["out_tok"])
+    np.testing.assert_array_equal(g1["root_next"], g2["root_next"])
+
+
+def test_loop_rejects_rejection_sampling():
+    import dataclasses as dc
+    from harness import accept_of
+    w = dc.replace(_mid(), mode="reject", temperature=0.8)
+    dev = setup(w)
+    root = torch.zeros(w.B, dtype=torch.int32, device="cuda")
+    kv = Bnd.kv_struct(dev.kc, dev.vc, dev.length, dev.length, dev.pt)
+    tokens = torch.empty(2, w.B, w.K + 1, dtype=torch.int32, device="cuda")
+    n_acc = torch.empty(2, w.B, dtype=torch.int32, device="cuda")
+    with pytest.raises(Bnd.MedusaError) as e:
+        Bnd.Loop(dev.plan, dev.wstruct, kv, Bnd.accept_struct(**accept_of(w, dev)), dev.h, root,
+                 tokens, n_acc, dev.ws)
+    assert e.value.code == Bnd.MEDUSA_ERR_UNSUPPORTED

@@ -376,3 +376,66 @@ def test_step_positions_and_compaction_slots():
     assert r.out_tok[0] == r.root == O.argmax_lowest(O.lm_head(ow["lm"], O.f64(h)))[0]
     # the kept keys are those of the nodes at depths 0..m on the best path
     assert [spec.depth[n] for n in r.path_nodes] == list(range(r.m + 1))
+
+
+# ------------------------------------------------------------ rejection sampling (R8)
+def _rs_tree():
+    """Root with children (0), (1); (0) has children (0,0), (0,1); (1) has child (1,0)."""
+    spec = O.pack_tree([[0], [1], [0, 0], [0, 1], [1, 0]])
+    tok = np.array([5, 2, 0, 3, 1, 4])          # distinct among siblings, as top-s tokens are
+    rng = np.random.default_rng(3)
+    zv = rng.standard_normal((spec.N + 1, 6)) * 1.5
+    return spec, tok, zv
+
+
+def test_inverse_cdf_draw_closed_forms():
+    w = np.array([0.0, 0.2, 0.0, 0.3, 0.5])
+    assert O.inverse_cdf_draw(w, 0.0)[0] == 1           # the first token with weight
+    assert O.inverse_cdf_draw(w, 0.5)[0] == 4           # cumulative 0.5 is not > 0.5
+    assert O.inverse_cdf_draw(w, 0.49)[0] == 3
+    assert O.inverse_cdf_draw(w, 0.999999)[0] == 4
+    assert O.inverse_cdf_draw(np.array([0.0, 0.0, 2.0]), 0.7)[0] == 2
+
+
+def test_rejection_walk_emits_the_backbone_distribution():
+    """The speculative-sampling guarantee: the first token after the root is distributed
+    as p_root, and the token after an accepted child c as p_c, whatever the drafts."""
+    spec, tok, zv = _rs_tree()
+    T = 0.9
+    n = 40000
+    rng = np.random.default_rng(11)
+    first = np.zeros(6)
+    second = np.zeros(6)
+    child = O.children(spec, 0)[0]                      # node (0), token 2
+    n_child = 0
+    for _ in range(n):
+        uni = rng.random(1 + 16 * 2)
+        path, v, _ = O.rejection_walk(spec, tok, zv, T, uni)
+        t1 = tok[path[1]] if len(path) > 1 else v
+        first[t1] += 1
+        if len(path) > 1 and path[1] == child:
+            n_child += 1
+            second[tok[path[2]] if len(path) > 2 else v] += 1
+    p0 = O.softmax_T(zv[0], T)
+    pc = O.softmax_T(zv[child], T)
+    assert n_child > 1000
+    for emp, p, m in ((first / n, p0, n), (second / n_child, pc, n_child)):
+        sigma = np.sqrt(p * (1 - p) / m)
+        assert (np.abs(emp - p) < 5 * sigma + 1e-12).all(), (emp, p)
+
+
+def test_rejection_walk_at_low_temperature_is_the_greedy_walk():
+    spec, tok, zv = _rs_tree()
+    tok = tok.copy()                                    # plant greedy matches along (0), (0,1)
+    tok[1] = int(np.argmax(zv[0]))                      # child (0) is the root's greedy token
+    tok[2] = (tok[1] + 1) % 6
+    tok[4] = int(np.argmax(zv[1]))                      # child (0,1) is (0)'s greedy token
+    tok[3] = (tok[4] + 1) % 6
+    rng = np.random.default_rng(5)
+    am = np.array([int(np.argmax(z)) for z in zv])
+    acc, _ = O.accept_flags(spec, tok, zv, am, np.full(spec.N + 1, np.inf), {"mode": "greedy"})
+    _, _, m, greedy_path = O.longest_accepted(spec, acc)
+    for _ in range(20):
+        path, v, _ = O.rejection_walk(spec, tok, zv, 1e-4, rng.random(1 + 32) * 0.999 + 0.0005)
+        assert list(path) == list(greedy_path)
+        assert v == am[path[-1]]
