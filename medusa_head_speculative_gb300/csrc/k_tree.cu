@@ -287,28 +287,54 @@ __global__ void __launch_bounds__(1024) rope_split_kernel(
   __syncthreads();
   const int W = (Hq + 2 * Hkv) * dh;
   const float* row = qkv + (long)m * W;
-  for (int e = threadIdx.x; e < (Hq + Hkv) * half; e += blockDim.x) {
-    const int h = e / half, i = e - h * half;
-    const float* x = row + h * dh;
-    const float c = cs[i], s = cs[half + i];
-    const float y0 = x[i] * c - x[i + half] * s;
-    const float y1 = x[i + half] * c + x[i] * s;
-    if (h < Hq) {
-      const long o = ((long)m * Hq + h) * dh;
-      q[o + i] = y0;
-      q[o + i + half] = y1;
-      if (qb) {
-        qb[o + i] = __float2bfloat16_rn(y0);
-        qb[o + i + half] = __float2bfloat16_rn(y1);
+  // Every load of a batch goes out before its first store (one round trip per batch).
+  constexpr int NB = 4;
+  const int npair = (Hq + Hkv) * half, step = blockDim.x;
+  for (int e0 = threadIdx.x; e0 < npair; e0 += NB * step) {
+    float a[NB], bb[NB];
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+      const int e = e0 + u * step;
+      if (e < npair) {
+        const int h = e / half, i = e - h * half;
+        a[u] = row[h * dh + i];
+        bb[u] = row[h * dh + i + half];
       }
-    } else {
-      T* ko = tk + ((long)m * Hkv + (h - Hq)) * dh;
-      ko[i] = from_f32<T>(y0);
-      ko[i + half] = from_f32<T>(y1);
+    }
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+      const int e = e0 + u * step;
+      if (e >= npair) continue;
+      const int h = e / half, i = e - h * half;
+      const float c = cs[i], s = cs[half + i];
+      const float y0 = a[u] * c - bb[u] * s;
+      const float y1 = bb[u] * c + a[u] * s;
+      if (h < Hq) {
+        const long o = ((long)m * Hq + h) * dh;
+        q[o + i] = y0;
+        q[o + i + half] = y1;
+        if (qb) {
+          qb[o + i] = __float2bfloat16_rn(y0);
+          qb[o + i + half] = __float2bfloat16_rn(y1);
+        }
+      } else {
+        T* ko = tk + ((long)m * Hkv + (h - Hq)) * dh;
+        ko[i] = from_f32<T>(y0);
+        ko[i + half] = from_f32<T>(y1);
+      }
     }
   }
   const float* vr = row + (Hq + Hkv) * dh;
-  for (int e = threadIdx.x; e < Hkv * dh; e += blockDim.x) tv[(long)m * Hkv * dh + e] = from_f32<T>(vr[e]);
+  const int nv = Hkv * dh;
+  for (int e0 = threadIdx.x; e0 < nv; e0 += NB * step) {
+    float x[NB];
+#pragma unroll
+    for (int u = 0; u < NB; ++u)
+      if (e0 + u * step < nv) x[u] = vr[e0 + u * step];
+#pragma unroll
+    for (int u = 0; u < NB; ++u)
+      if (e0 + u * step < nv) tv[(long)m * nv + e0 + u * step] = from_f32<T>(x[u]);
+  }
 }
 
 cudaError_t launch_rope_split(const float* qkv, const int32_t* pos, int M, int Hq, int Hkv, int dh,
