@@ -8,7 +8,7 @@
 // activations arrive as bf16 hi + lo halves; both MMAs accumulate into one fp32 TMEM
 // accumulator, so the products keep ~fp32 accuracy at no extra TMEM.  Warp 0 lane 0
 // issues the TMA loads, warp 1 lane 0 the MMAs; then all four warps read their 32 TMEM
-// lanes and run the epilogue (one weight row per thread, coalesced over r).
+// lanes, transpose through the idle stage ring and run the epilogue on whole rows.
 //
 // Every wait is bounded (~1 s of GPU time): on expiry the CTA sets MEDUSA_FLAG_TIMEOUT,
 // drains (again bounded) the copies it issued, frees its TMEM and returns.
@@ -42,23 +42,104 @@ struct UmmaArgs {
   uint32_t* status;
 };
 
-__device__ __forceinline__ void umma_epilogue(const MatArgs& a, const MatSeg& s, int m, int r,
-                                              float acc) {
-  float y = acc;
-  if (a.epi == EPI_SILU_RES) {
-    y = silu(acc) + a.res_f32[(long)m * a.ldr + r];
-  } else if (a.epi == EPI_RES_ADD) {
-    const float res = a.res_f32 ? a.res_f32[(long)m * a.ldr + r]
-                                : to_f32(reinterpret_cast<const bf16*>(a.res_w)[(long)m * a.ldr + r]);
-    y = acc + res;
+__device__ __forceinline__ bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+__device__ __forceinline__ bool aligned8(const void* p) { return ((uintptr_t)p & 7) == 0; }
+
+// Outputs r..r+3 (weight rows of segment s) of activation row m: the epilogue with 16-byte
+// loads and stores where all four exist and the addresses allow it, else per element.
+__device__ __forceinline__ void epilogue4(const MatArgs& a, const MatSeg& s, int m, int r, float4 v,
+                                          float* kpart_row) {
+  float y[4] = {v.x, v.y, v.z, v.w};
+  const int n = min(4, s.rows - r);
+  if (kpart_row) {                                      // raw partial sum of a K range
+    float* kp = kpart_row + s.out_off + r;
+    if (n == 4 && aligned16(kp)) *reinterpret_cast<float4*>(kp) = v;
+    else for (int e = 0; e < n; ++e) kp[e] = y[e];
+    return;
   }
   const long o = (long)m * a.ldo + s.out_off + r;
-  a.out[o] = y;
+  if (a.epi != EPI_STORE) {
+    const long ro = (long)m * a.ldr + r;
+    float res[4] = {0.f, 0.f, 0.f, 0.f};
+    if (a.res_f32) {
+      const float* rp = a.res_f32 + ro;
+      if (n == 4 && aligned16(rp)) {
+        const float4 q = *reinterpret_cast<const float4*>(rp);
+        res[0] = q.x; res[1] = q.y; res[2] = q.z; res[3] = q.w;
+      } else {
+        for (int e = 0; e < n; ++e) res[e] = rp[e];
+      }
+    } else {
+      const bf16* rw = reinterpret_cast<const bf16*>(a.res_w) + ro;
+      if (n == 4 && aligned8(rw)) {
+        const uint2 q = *reinterpret_cast<const uint2*>(rw);
+        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&q.x);
+        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&q.y);
+        res[0] = __low2float(p0); res[1] = __high2float(p0);
+        res[2] = __low2float(p1); res[3] = __high2float(p1);
+      } else {
+        for (int e = 0; e < n; ++e) res[e] = to_f32(rw[e]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) y[e] = (a.epi == EPI_SILU_RES ? silu(y[e]) : y[e]) + res[e];
+  }
+  float* op = a.out + o;
+  if (n == 4 && aligned16(op)) *reinterpret_cast<float4*>(op) = make_float4(y[0], y[1], y[2], y[3]);
+  else for (int e = 0; e < n; ++e) op[e] = y[e];
   if (a.out_hi) {
-    bf16 hi, lo;
-    split_hi_lo(y, hi, lo);
-    a.out_hi[o] = hi;
-    a.out_lo[o] = lo;
+    bf16 hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split_hi_lo(y[e], hi[e], lo[e]);
+    bf16* hp = a.out_hi + o;
+    bf16* lp = a.out_lo + o;
+    if (n == 4 && aligned8(hp) && aligned8(lp)) {
+      __nv_bfloat162 t[4] = {__halves2bfloat162(hi[0], hi[1]), __halves2bfloat162(hi[2], hi[3]),
+                             __halves2bfloat162(lo[0], lo[1]), __halves2bfloat162(lo[2], lo[3])};
+      *reinterpret_cast<uint2*>(hp) = *reinterpret_cast<const uint2*>(&t[0]);
+      *reinterpret_cast<uint2*>(lp) = *reinterpret_cast<const uint2*>(&t[2]);
+    } else {
+      for (int e = 0; e < n; ++e) {
+        hp[e] = hi[e];
+        lp[e] = lo[e];
+      }
+    }
+  }
+}
+
+// Epilogue of a CTA's accumulators through shared memory.  Thread = TMEM lane = weight
+// row, so reading TMEM gives each thread one output column for many activation rows;
+// written out directly, a warp's store covers only 128 bytes of 16 different rows.
+// Instead each chunk of 32 activation rows goes to `stage` ([32][rt] fp32, rt = 128 per
+// accumulator) and comes back row-major: every thread then handles 4 consecutive
+// outputs of one row (16-byte loads of the residual and stores of the result).  All 128
+// threads must call this together.
+__device__ void staged_epilogue(const MatArgs& a, const MatSeg& s, int rbase, int nacc, int m0,
+                                int nbox, uint32_t tmem, uint32_t acc_stride, float* stage,
+                                float* kpart /* split-K partials for blockIdx.z, or null */) {
+  constexpr int CM = 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rt = 128 * nacc, q4 = rt / 4;
+  for (int c0 = 0; c0 < nbox; c0 += CM) {
+    const int cm = min(CM, nbox - c0);                  // 32, or a 16-column tail
+    for (int t = 0; t < nacc; ++t) {
+      for (int cc = 0; cc < cm; cc += 16) {
+        float v[16];
+        tmem_ld16(tmem + t * acc_stride + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c0 + cc), v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) stage[(cc + j) * rt + t * 128 + warp * 32 + lane] = v[j];
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < cm * q4; i += 128) {
+      const int ml = i / q4, q = i - ml * q4;
+      const int m = m0 + c0 + ml, r = rbase + 4 * q;
+      if (m < a.M && r < s.rows) {
+        const float4 v = *reinterpret_cast<const float4*>(stage + ml * rt + 4 * q);
+        epilogue4(a, s, m, r, v, kpart ? kpart + ((long)blockIdx.z * a.M + m) * a.ldo : nullptr);
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -67,7 +148,7 @@ __global__ void __launch_bounds__(128, 2) umma_gemm_kernel(const __grid_constant
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[2 * 8 + 1];
   __shared__ uint32_t tmem_slot;
-  __shared__ int s_issued, s_consumed;
+  __shared__ int s_issued, s_consumed, s_bad;
   const MatArgs& a = g.m;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int si = 0;
@@ -95,6 +176,7 @@ __global__ void __launch_bounds__(128, 2) umma_gemm_kernel(const __grid_constant
     mbar_init(accb, 1);
     s_issued = 0;
     s_consumed = 0;
+    s_bad = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), g.tmem_cols);
@@ -117,62 +199,60 @@ __global__ void __launch_bounds__(128, 2) umma_gemm_kernel(const __grid_constant
       tma_load_2d(base + j * STAGE, &g.tw[si], (kt0 + j) * UM_K, rbase, full(j), pw);
     }
     pdl_wait();
-    int j = 0;
+    const CUtensorMap* tw = &g.tw[si];
+    const CUtensorMap* ta = &g.ta[si];
+    const CUtensorMap* tl = &g.tl[si];
+    int j = 0, st = 0;
+    uint32_t ph = 0;                                    // phase of the ring's current pass
     for (; j < nkl; ++j) {
-      const int st = j % S, kx = (kt0 + j) * UM_K;
+      const int kx = (kt0 + j) * UM_K;
       const uint32_t ws = base + st * STAGE;
       if (j >= pre) {
-        if (!mbar_wait(empty(st), ((j / S) & 1) ^ 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+        if (!mbar_wait(empty(st), ph ^ 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
         mbar_expect_tx(full(st), STAGE);
-        tma_load_2d(ws, &g.tw[si], kx, rbase, full(st), pw);
+        tma_load_2d(ws, tw, kx, rbase, full(st), pw);
       }
-      tma_load_2d(ws + UM_W_BYTES, &g.ta[si], kx, m0, full(st), pa);
-      if (HAS_LO) tma_load_2d(ws + UM_W_BYTES + A_BYTES, &g.tl[si], kx, m0, full(st), pa);
+      tma_load_2d(ws + UM_W_BYTES, ta, kx, m0, full(st), pa);
+      if (HAS_LO) tma_load_2d(ws + UM_W_BYTES + A_BYTES, tl, kx, m0, full(st), pa);
+      if (++st == S) { st = 0; ph ^= 1; }
     }
     s_issued = j;
+    if (timed_out) s_bad = 1;
   } else if (warp == 1 && lane == 0) {                  // ---- MMA issuer
     const uint32_t idesc = idesc_bf16(UM_R, g.nbox);
-    int j = 0;
+    // descriptors of stage 0; stage st adds st * STAGE bytes to the start address field
+    const uint64_t ad0 = sw128_desc(base), bd0 = sw128_desc(base + UM_W_BYTES);
+    const uint64_t ld0 = sw128_desc(base + UM_W_BYTES + A_BYTES);
+    const uint64_t dstep = STAGE >> 4;
+    int j = 0, st = 0;
+    uint32_t ph = 0;
+    uint64_t off = 0;
     for (; j < nkl; ++j) {
-      const int st = j % S;
-      if (!mbar_wait(full(st), (j / S) & 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+      if (!mbar_wait(full(st), ph, TC_TIMEOUT_NS)) { timed_out = true; break; }
       tc_fence_after();
-      const uint32_t ws = base + st * STAGE;
-      const uint64_t ad = sw128_desc(ws), bd = sw128_desc(ws + UM_W_BYTES);
-      const uint64_t ld = sw128_desc(ws + UM_W_BYTES + A_BYTES);
+      const uint64_t ad = ad0 + off, bd = bd0 + off, ld = ld0 + off;
 #pragma unroll
       for (int ks = 0; ks < UM_K / 16; ++ks) {          // +32 bytes along K per step
         umma_bf16(tmem, ad + 2 * ks, bd + 2 * ks, idesc, (j | ks) != 0);
         if (HAS_LO) umma_bf16(tmem, ad + 2 * ks, ld + 2 * ks, idesc, 1);
       }
       umma_commit(empty(st));                           // frees the stage when read
+      if (++st == S) { st = 0; ph ^= 1; off = 0; } else { off += dstep; }
     }
     s_consumed = j;
+    if (timed_out) s_bad = 1;
     umma_commit(accb);                                  // accumulator complete
   }
   __syncwarp();
   pdl_wait();                                           // the epilogue reads and writes globals
-  // ---- epilogue: thread = TMEM lane = weight row
+  // ---- epilogue, staged through the (now idle) ring
   const bool acc_ok = mbar_wait(accb, 0, TC_TIMEOUT_NS);
   tc_fence_after();
-  __syncwarp();
-  if (acc_ok && nkl > 0) {
-    const int r = rbase + warp * 32 + lane;
-    for (int c0 = 0; c0 < g.nbox; c0 += 16) {
-      float v[16];
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-      if (r < s.rows) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int m = m0 + c0 + j;
-          if (m >= a.M) continue;
-          if (g.ksplit > 1)                             // raw partial sum of this K range
-            g.kpart[((long)blockIdx.z * a.M + m) * a.ldo + s.out_off + r] = v[j];
-          else
-            umma_epilogue(a, s, m, r, v[j]);
-        }
-      }
-    }
+  // every MMA has read its stage and every copy has landed unless a wait expired
+  const bool run = __syncthreads_and(acc_ok) && !s_bad && nkl > 0;
+  if (run) {
+    float* stage = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)));
+    staged_epilogue(a, s, rbase, 1, m0, g.nbox, tmem, 0, stage, g.ksplit > 1 ? g.kpart : nullptr);
   }
   if (timed_out || !acc_ok) set_flag(g.status, MEDUSA_FLAG_TIMEOUT);
   tc_fence_before();
@@ -215,7 +295,7 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[2 * 8 + 1];
   __shared__ uint32_t tmem_slot;
-  __shared__ int s_issued, s_consumed;
+  __shared__ int s_issued, s_consumed, s_bad;
   const MatArgs& a = g.m;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank();
@@ -247,6 +327,7 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
     mbar_init(accb, 1);
     s_issued = 0;
     s_consumed = 0;
+    s_bad = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), g.tmem_cols);
@@ -268,67 +349,73 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
       if (has_w) tma_load_2d(base + j * STAGE, &g.tw[si], (kt0 + j) * UM_K, rbase, full(j), pw);
     }
     pdl_wait();
-    int j = 0;
+    const CUtensorMap* tw = &g.tw[si];
+    const uint32_t aoff = UW_W_BYTES + rank * (uint32_t)half * 128;
+    const int arow = m0 + (int)rank * half;
+    int j = 0, st = 0;
+    uint32_t ph = 0;                                    // phase of the ring's current pass
     for (; j < nkl; ++j) {
-      const int st = j % S, kx = (kt0 + j) * UM_K;
+      const int kx = (kt0 + j) * UM_K;
       const uint32_t ws = base + st * STAGE;
       if (j >= pre) {
-        if (!mbar_wait(empty(st), ((j / S) & 1) ^ 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+        if (!mbar_wait(empty(st), ph ^ 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
         mbar_expect_tx(full(st), stage_tx);
-        if (has_w) tma_load_2d(ws, &g.tw[si], kx, rbase, full(st), pw);
+        if (has_w) tma_load_2d(ws, tw, kx, rbase, full(st), pw);
       }
-      const uint32_t off = UW_W_BYTES + rank * (uint32_t)half * 128;
-      tma_load_2d_mc(ws + off, &g.ta, kx, m0 + (int)rank * half, full(st), UW_PAIR, pa);
-      if (HAS_LO) tma_load_2d_mc(ws + off + A_BYTES, &g.tl, kx, m0 + (int)rank * half, full(st), UW_PAIR, pa);
+      tma_load_2d_mc(ws + aoff, &g.ta, kx, arow, full(st), UW_PAIR, pa);
+      if (HAS_LO) tma_load_2d_mc(ws + aoff + A_BYTES, &g.tl, kx, arow, full(st), UW_PAIR, pa);
+      if (++st == S) { st = 0; ph ^= 1; }
     }
     s_issued = j;
+    if (timed_out) s_bad = 1;
   } else if (warp == 1 && lane == 0) {                  // ---- MMA issuer
     const uint32_t idesc = idesc_bf16(128, g.nbox);
-    int j = 0;
+    // descriptors of stage 0; stage st adds st * STAGE bytes to the start address field
+    const uint64_t a0 = sw128_desc(base), a1 = sw128_desc(base + UM_W_BYTES);
+    const uint64_t b0 = sw128_desc(base + UW_W_BYTES), l0 = sw128_desc(base + UW_W_BYTES + A_BYTES);
+    const uint64_t dstep = STAGE >> 4;
+    const uint32_t d1 = tmem + g.acc_stride;
+    int j = 0, st = 0;
+    uint32_t ph = 0;
+    uint64_t off = 0;
     for (; j < nkl; ++j) {
-      const int st = j % S;
-      if (!mbar_wait(full(st), (j / S) & 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
+      if (!mbar_wait(full(st), ph, TC_TIMEOUT_NS)) { timed_out = true; break; }
       tc_fence_after();
-      const uint32_t ws = base + st * STAGE;
-      const uint64_t bd = sw128_desc(ws + UW_W_BYTES), ld = sw128_desc(ws + UW_W_BYTES + A_BYTES);
-      for (int t = 0; t < nacc; ++t) {
-        const uint64_t ad = sw128_desc(ws + t * UM_W_BYTES);
-        const uint32_t d = tmem + t * g.acc_stride;
+      const uint64_t bd = b0 + off, ld = l0 + off;
+      if (nacc > 0) {
+        const uint64_t ad = a0 + off;
 #pragma unroll
         for (int ks = 0; ks < UM_K / 16; ++ks) {
-          umma_bf16(d, ad + 2 * ks, bd + 2 * ks, idesc, (j | ks) != 0);
-          if (HAS_LO) umma_bf16(d, ad + 2 * ks, ld + 2 * ks, idesc, 1);
+          umma_bf16(tmem, ad + 2 * ks, bd + 2 * ks, idesc, (j | ks) != 0);
+          if (HAS_LO) umma_bf16(tmem, ad + 2 * ks, ld + 2 * ks, idesc, 1);
+        }
+      }
+      if (nacc > 1) {
+        const uint64_t ad = a1 + off;
+#pragma unroll
+        for (int ks = 0; ks < UM_K / 16; ++ks) {
+          umma_bf16(d1, ad + 2 * ks, bd + 2 * ks, idesc, (j | ks) != 0);
+          if (HAS_LO) umma_bf16(d1, ad + 2 * ks, ld + 2 * ks, idesc, 1);
         }
       }
       umma_commit_mc(empty(st), UW_PAIR);               // frees the stage in both CTAs
+      if (++st == S) { st = 0; ph ^= 1; off = 0; } else { off += dstep; }
     }
     s_consumed = j;
+    if (timed_out) s_bad = 1;
     umma_commit(accb);
   }
   __syncwarp();
   pdl_wait();
   const bool acc_ok = mbar_wait(accb, 0, TC_TIMEOUT_NS);
   tc_fence_after();
-  __syncwarp();
-  if (acc_ok && nkl > 0) {
-    for (int t = 0; t < nacc; ++t) {
-      const int r = rbase + t * 128 + warp * 32 + lane;
-      for (int c0 = 0; c0 < g.nbox; c0 += 16) {
-        float v[16];
-        tmem_ld16(tmem + t * g.acc_stride + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-        if (r < s.rows) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int m = m0 + c0 + j;
-            if (m >= a.M) continue;
-            if (g.ksplit > 1)
-              g.kpart[((long)blockIdx.z * a.M + m) * a.ldo + s.out_off + r] = v[j];
-            else
-              umma_epilogue(a, s, m, r, v[j]);
-          }
-        }
-      }
-    }
+  // every MMA has read its stage and every copy (ours and the peer's multicast halves)
+  // has landed in this CTA's ring unless a wait expired: the ring is free for staging
+  const bool run = __syncthreads_and(acc_ok) && !s_bad && nkl > 0 && nacc > 0;
+  if (run) {
+    float* stage = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)));
+    staged_epilogue(a, s, rbase, nacc, m0, g.nbox, tmem, g.acc_stride, stage,
+                    g.ksplit > 1 ? g.kpart : nullptr);
   }
   if (timed_out || !acc_ok) set_flag(g.status, MEDUSA_FLAG_TIMEOUT);
   tc_fence_before();
@@ -372,10 +459,13 @@ __global__ void splitk_reduce_kernel(const MatArgs a, const float* __restrict__ 
       acc[2] += v[z].z;
       acc[3] += v[z].w;
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (a.nseg == 1) umma_epilogue(a, a.seg[0], m, c + e, acc[e]);
-      else a.out[(long)m * a.ldo + c + e] = acc[e];
+    const float4 y = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    if (a.nseg == 1) {
+      epilogue4(a, a.seg[0], m, c, y, nullptr);
+    } else {
+      float* op = a.out + (long)m * a.ldo + c;
+      if (aligned16(op)) *reinterpret_cast<float4*>(op) = y;
+      else for (int e = 0; e < 4; ++e) op[e] = acc[e];
     }
   }
 }
