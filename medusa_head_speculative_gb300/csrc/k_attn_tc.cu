@@ -6,8 +6,8 @@
 // one chunk of the prefix, or (split == nsplit) the tree keys under the ancestor bitmask,
 // for up to two 128-row query tiles (row = node x query head of the group) that share every
 // K/V tile, so up to 256 rows read the prefix once.  Inside the CTA the keys are walked in
-// 64-key chunks:
-//   warp 8 (one lane)  TMA: Q once, then K and V chunks through a 3-stage mbarrier ring
+// chunks of 128 keys (one query tile) or 64 (two tiles, whose S buffers fill the TMEM):
+//   warp 8 (one lane)  TMA: Q once, then K and V chunks through a 2- to 4-stage mbarrier ring
 //                      (paged caches: one box per page)
 //   warp 9 (one lane)  MMAs: S = Q K^T into one of two TMEM buffers per tile (issued one
 //                      chunk ahead), then O += P V into the tile's TMEM accumulator, V as
@@ -37,18 +37,18 @@ namespace medusa {
 
 constexpr int AT_ROWS = 128;      // query rows per tile (MMA M, TMEM lanes)
 constexpr int AT_TILES = 2;       // query tiles per CTA at most
-constexpr int AT_KEYS = 64;       // keys per chunk (S columns, PV reduction)
+constexpr int AT_KEYS = 64;       // keys per chunk with two query tiles (S columns, PV reduction)
+constexpr int AT_KEYS1 = 128;     // keys per chunk with one query tile
 constexpr int AT_STAGES = 4;      // K/V ring depth at most (3 when two query tiles)
 constexpr int AT_WARPS = 4 * AT_TILES + 2;
-constexpr uint32_t AT_TILE_COLS = 256;   // per tile: S0 [0,64), S1 [64,128), O [128, 128+dh)
 constexpr float AT_LAZY = 8.f;           // log2 headroom before O is rescaled
 
 struct AttnTcArgs {
   CUtensorMap tq;        // q bf16:    dims {dh, Hq, B*n1},   box {64, G, 128/G}
   CUtensorMap tk, tv;    // cache:     dims {dh, Hkv, slots}, box {64, 1, kbox}
-  CUtensorMap ttk, ttv;  // tree K/V:  dims {dh, Hkv, B*n1},  box {64, 1, 64}
+  CUtensorMap ttk, ttv;  // tree K/V:  dims {dh, Hkv, B*n1},  box {64, 1, keys per chunk}
   AttnArgs a;
-  int kbox;              // cache rows per TMA box: 64 (contiguous) or the page size
+  int kbox;              // cache rows per TMA box: keys per chunk (contiguous) or the page size
   int nt;                // query tiles per CTA: rows_per_block / 128
   int stages;            // K/V ring depth (<= AT_STAGES)
 };
@@ -68,14 +68,19 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, TC_TIMEOUT_NS));
 }
 
-template <int DH>
+// KEYS keys per chunk: 64 (up to two query tiles) or 128 (one tile).  TMEM per tile:
+// S0 [0, KEYS), S1 [KEYS, 2 KEYS), O [2 KEYS, 2 KEYS + DH).
+template <int DH, int KEYS>
 __global__ void __launch_bounds__(AT_WARPS * 32, 1)
 tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
   constexpr int H = DH / 64;                        // 64-column halves of a head
   constexpr uint32_t QH = AT_ROWS * 128;            // one half of a Q tile: 16 KB
-  constexpr uint32_t KVH = AT_KEYS * 128;           // one half of a 64-key K or V tile: 8 KB
+  constexpr uint32_t KVH = KEYS * 128;              // one half of a K or V chunk
   constexpr uint32_t KV_STAGE = 2 * H * KVH;
-  constexpr uint32_t PT = AT_ROWS * 128;            // one P buffer: 128 rows x 64 keys bf16
+  constexpr uint32_t PA = AT_ROWS * 128;            // one 64-key swizzle atom of P: 16 KB
+  constexpr uint32_t PT = PA * (KEYS / 64);         // one P buffer: 128 rows x KEYS keys bf16
+  constexpr uint32_t TILE_COLS = KEYS == 64 ? 256 : 512;
+  constexpr uint32_t OCOL = 2 * KEYS;               // O's first TMEM column
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[BCOUNT];
   __shared__ uint32_t tmem_slot;
@@ -92,12 +97,12 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
   L = L < 0 ? 0 : (L > a.capacity ? a.capacity : L);
   const int kbeg = tree ? 0 : split * a.chunk;
   const int kend = tree ? a.n1 : min(L, kbeg + a.chunk);
-  const int nch = kend > kbeg ? (kend - kbeg + AT_KEYS - 1) / AT_KEYS : 0;
+  const int nch = kend > kbeg ? (kend - kbeg + KEYS - 1) / KEYS : 0;
   const uint32_t sraw = smem_u32(smem_raw);
   const uint32_t base = (sraw + 1023u) & ~1023u;
   const uint32_t qs = base, kv0 = base + nt * H * QH, ps = kv0 + ST * KV_STAGE;
   const uint32_t bar0 = smem_u32(bars);
-  const uint32_t tmem_cols = AT_TILE_COLS * nt;
+  const uint32_t tmem_cols = TILE_COLS * nt;
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
   if (tid == 0) {
@@ -153,8 +158,8 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
       for (; i < nch; ++i) {
         if (i == pre) load_q();
         const int st = i % ST;
-        const int t0 = kbeg + i * AT_KEYS;
-        if (paged && (t0 < pref0 || t0 + AT_KEYS > pref0 + 32 * a.page_size)) {
+        const int t0 = kbeg + i * KEYS;
+        if (paged && (t0 < pref0 || t0 + KEYS > pref0 + 32 * a.page_size)) {
           pref0 = t0 - t0 % a.page_size;
           const int t = pref0 + lane * a.page_size;
           my_page = 0;
@@ -166,9 +171,9 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
             }
           }
         }
-        int pages[AT_KEYS / 8];                          // one per box of this chunk
+        int pages[KEYS / 8];                             // one per box of this chunk
         if (paged) {
-          for (int j = 0, q = 0; j < AT_KEYS; j += g.kbox, ++q)
+          for (int j = 0, q = 0; j < KEYS; j += g.kbox, ++q)
             pages[q] = __shfl_sync(0xffffffffu, my_page, (t0 + j - pref0) / a.page_size);
         }
         bool ok = true;
@@ -187,7 +192,7 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
             tma_load_3d(vs + h * KVH, &g.ttv, h * 64, gk, b * a.n1 + t0, bar(BKVF + st), pol_kv);
           }
         } else if (paged) {
-          for (int j = 0, q = 0; j < AT_KEYS; j += g.kbox, ++q) {
+          for (int j = 0, q = 0; j < KEYS; j += g.kbox, ++q) {
             const int row = pages[q] * a.page_size;
 #pragma unroll
             for (int h = 0; h < H; ++h) {
@@ -218,14 +223,14 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
         timed_out = true;
       } else {
         s_qok = 1;
-        const uint32_t id_qk = idesc_bf16(AT_ROWS, AT_KEYS);
+        const uint32_t id_qk = idesc_bf16(AT_ROWS, KEYS);
         const uint32_t id_pv = idesc_bf16(AT_ROWS, DH) | IDESC_B_MN_MAJOR;
         auto issue_qk = [&](int j) {
           waited = j + 1;
           tc_fence_after();
           const uint32_t ks = kv0 + (j % ST) * KV_STAGE;
           for (int t = 0; t < nta; ++t) {
-            const uint32_t d = tmem + t * AT_TILE_COLS + (uint32_t)(j & 1) * AT_KEYS;
+            const uint32_t d = tmem + t * TILE_COLS + (uint32_t)(j & 1) * KEYS;
 #pragma unroll
             for (int h = 0; h < H; ++h)
 #pragma unroll
@@ -250,8 +255,8 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
             tc_fence_after();
             const uint32_t pt = ps + (uint32_t)(2 * t + (i & 1)) * PT;
 #pragma unroll
-            for (int kk = 0; kk < AT_KEYS / 16; ++kk)
-              umma_bf16(tmem + t * AT_TILE_COLS + 128, sw128_desc(pt) + 2 * kk,
+            for (int kk = 0; kk < KEYS / 16; ++kk)           // 16 keys per MMA; P atom kk / 4
+              umma_bf16(tmem + t * TILE_COLS + OCOL, sw128_desc(pt + (kk >> 2) * PA) + 2 * (kk & 3),
                         sw128_desc_mn(vs + kk * 2048, KVH), id_pv, (i | kk) != 0);
             umma_commit(bar(BOF + 2 * t + (i & 1)));
           }
@@ -272,7 +277,7 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
     const int gr = row0 + t * AT_ROWS + r;
     const int node = gr / G;
     const bool row_ok = gr < R;
-    const uint32_t lane_base = tmem + t * AT_TILE_COLS + ((uint32_t)(wl * 32) << 16);
+    const uint32_t lane_base = tmem + t * TILE_COLS + ((uint32_t)(wl * 32) << 16);
     uint8_t* pgen = smem_raw + (ps - sraw) + (size_t)(2 * t) * PT;
     const float sl2 = a.scale * 1.4426950408889634f;      // scores in base-2 units
     float m_use = -INFINITY, l_acc = 0.f;
@@ -288,17 +293,19 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
     for (int i = 0; i < nch && live; ++i) {
       if (!warp_wait(bar(BSF + 2 * t + (i & 1)), (i >> 1) & 1)) { timed_out = true; break; }
       tc_fence_after();
-      float s[AT_KEYS];
-      tmem_ld64(lane_base + (uint32_t)(i & 1) * AT_KEYS, s);     // one round trip
-      const int t0 = kbeg + i * AT_KEYS;
+      float s[KEYS];
+#pragma unroll
+      for (int h = 0; h < KEYS / 64; ++h)
+        tmem_ld64(lane_base + (uint32_t)(i & 1) * KEYS + 64 * h, *reinterpret_cast<float(*)[64]>(s + 64 * h));
+      const int t0 = kbeg + i * KEYS;
       // A whole chunk of prefix keys needs no mask: the maximum is taken over the raw
       // scores and the scale is folded into the exponent's FMA below.
-      const bool full = !tree && t0 + AT_KEYS <= kend;
+      const bool full = !tree && t0 + KEYS <= kend;
       float mx;
       if (full) {
         float q0 = s[0], q1 = s[1], q2 = s[2], q3 = s[3];
 #pragma unroll
-        for (int j = 4; j < AT_KEYS; j += 4) {
+        for (int j = 4; j < KEYS; j += 4) {
           q0 = fmaxf(q0, s[j]);
           q1 = fmaxf(q1, s[j + 1]);
           q2 = fmaxf(q2, s[j + 2]);
@@ -306,15 +313,17 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
         }
         mx = fmaxf(fmaxf(q0, q1), fmaxf(q2, q3)) * sl2;
       } else {
-        uint32_t w0 = 0xffffffffu, w1 = 0xffffffffu;
-        if (tree) {
-          w0 = row_ok ? a.mask[(long)node * kMaskWords + (t0 >> 5)] : 0u;
-          w1 = row_ok && (t0 >> 5) + 1 < kMaskWords ? a.mask[(long)node * kMaskWords + (t0 >> 5) + 1] : 0u;
+        uint32_t w[KEYS / 32];                       // ancestor bits of this chunk's keys
+#pragma unroll
+        for (int q = 0; q < KEYS / 32; ++q) {
+          const int wi = (t0 >> 5) + q;
+          w[q] = !tree ? 0xffffffffu
+                       : (row_ok && wi < kMaskWords ? a.mask[(long)node * kMaskWords + wi] : 0u);
         }
         mx = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < AT_KEYS; ++j) {
-          const bool bit = ((j < 32 ? w0 : w1) >> (j & 31)) & 1u;
+        for (int j = 0; j < KEYS; ++j) {
+          const bool bit = (w[j >> 5] >> (j & 31)) & 1u;
           const bool valid = (t0 + j < kend) && bit;
           s[j] = valid ? s[j] * sl2 : -INFINITY;
           mx = fmaxf(mx, s[j]);
@@ -331,10 +340,10 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
 #pragma unroll
         for (int c = 0; c < DH; c += 16) {
           float v[16];
-          tmem_ld16(lane_base + 128 + c, v);
+          tmem_ld16(lane_base + OCOL + c, v);
 #pragma unroll
           for (int e = 0; e < 16; ++e) v[e] *= f;
-          tmem_st16(lane_base + 128 + c, v);
+          tmem_st16(lane_base + OCOL + c, v);
         }
         if (raise) {
           l_acc *= f;
@@ -346,7 +355,7 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
       if (full) {
         const float nm = -m_use;
 #pragma unroll
-        for (int j = 0; j < AT_KEYS; j += 4) {
+        for (int j = 0; j < KEYS; j += 4) {
           s[j] = ex2_approx(fmaf(s[j], sl2, nm));
           s[j + 1] = ex2_approx(fmaf(s[j + 1], sl2, nm));
           s[j + 2] = ex2_approx(fmaf(s[j + 2], sl2, nm));
@@ -358,7 +367,7 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < AT_KEYS; j += 4) {
+        for (int j = 0; j < KEYS; j += 4) {
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             s[j + e] = s[j + e] == -INFINITY ? 0.f : ex2_approx(s[j + e] - m_use);
@@ -372,7 +381,7 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
       // P row (bf16) into the 128-byte-swizzled K-major tile the PV MMA reads
       uint8_t* prow = pgen + (size_t)(i & 1) * PT + r * 128;
 #pragma unroll
-      for (int c = 0; c < AT_KEYS / 8; ++c) {
+      for (int c = 0; c < KEYS / 8; ++c) {            // 16-byte unit c: atom c / 8, unit c % 8
         uint4 u;
         __nv_bfloat162 p0 = __floats2bfloat162_rn(s[8 * c + 0], s[8 * c + 1]);
         __nv_bfloat162 p1 = __floats2bfloat162_rn(s[8 * c + 2], s[8 * c + 3]);
@@ -382,7 +391,7 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
         u.y = *reinterpret_cast<uint32_t*>(&p1);
         u.z = *reinterpret_cast<uint32_t*>(&p2);
         u.w = *reinterpret_cast<uint32_t*>(&p3);
-        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = u;
+        *reinterpret_cast<uint4*>(prow + (c >> 3) * PA + (((c & 7) ^ (r & 7)) << 4)) = u;
       }
       fence_proxy_async();
       tc_fence_before();
@@ -399,7 +408,7 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
 #pragma unroll
         for (int c = 0; c < DH; c += 64) {
           float v[64];
-          tmem_ld64(lane_base + 128 + c, v);
+          tmem_ld64(lane_base + OCOL + c, v);
 #pragma unroll
           for (int e = 0; e < 64; ++e) o[c + e] = v[e];
         }
@@ -467,6 +476,28 @@ cudaError_t launch_tree_attention_tc(const AttnArgs& a, const void* q_bf16, cuda
   std::lock_guard<std::mutex> lock(mu);
   std::memset(&g, 0, sizeof(g));
   g.a = a;
+  if (a.rows_per_block != AT_ROWS && a.rows_per_block != AT_ROWS * AT_TILES) return cudaErrorInvalidValue;
+  g.nt = a.rows_per_block / AT_ROWS;
+  const int H = a.dh / 64;
+  // shared memory: Q tiles, two P buffers per tile, then as many K/V stages as fit (227 KB)
+  auto plan = [&](int keys, size_t& smem) {
+    const size_t fixed = 1024 + (size_t)g.nt * H * AT_ROWS * 128 + (size_t)g.nt * 2 * AT_ROWS * keys * 2;
+    const size_t kv_stage = (size_t)2 * H * keys * 128;
+    const int stages = fixed < 226u * 1024u ? (int)std::min<size_t>(AT_STAGES, (226u * 1024u - fixed) / kv_stage) : 0;
+    smem = fixed + (size_t)stages * kv_stage;
+    return stages;
+  };
+  // one query tile: 128-key chunks (half the MMA issues, waits and commits per key) when
+  // two stages of them fit; two tiles keep 64-key chunks (TMEM holds 2 x 256 columns)
+  size_t smem = 0;
+  int keys = AT_KEYS;
+  g.stages = plan(AT_KEYS, smem);
+  if (g.nt == 1) {
+    size_t smem1 = 0;
+    const int st1 = plan(AT_KEYS1, smem1);
+    if (st1 >= 2) { keys = AT_KEYS1; g.stages = st1; smem = smem1; }
+  }
+  if (g.stages < 2) return cudaErrorInvalidValue;
   const long nodes = (long)a.B * a.n1;
   if (!make_map3(&g.tq, q_bf16, a.dh, a.Hq, nodes, a.G, AT_ROWS / a.G)) return cudaErrorInvalidValue;
   if (a.page_table) {
@@ -475,22 +506,16 @@ cudaError_t launch_tree_attention_tc(const AttnArgs& a, const void* q_bf16, cuda
     if (!make_map3(&g.tk, a.kc, a.dh, a.Hkv, slots, 1, a.page_size)) return cudaErrorInvalidValue;
     if (!make_map3(&g.tv, a.vc, a.dh, a.Hkv, slots, 1, a.page_size)) return cudaErrorInvalidValue;
   } else {
-    g.kbox = AT_KEYS;
+    g.kbox = keys;
     const long slots = (long)a.B * a.capacity;
-    if (!make_map3(&g.tk, a.kc, a.dh, a.Hkv, slots, 1, AT_KEYS)) return cudaErrorInvalidValue;
-    if (!make_map3(&g.tv, a.vc, a.dh, a.Hkv, slots, 1, AT_KEYS)) return cudaErrorInvalidValue;
+    if (!make_map3(&g.tk, a.kc, a.dh, a.Hkv, slots, 1, keys)) return cudaErrorInvalidValue;
+    if (!make_map3(&g.tv, a.vc, a.dh, a.Hkv, slots, 1, keys)) return cudaErrorInvalidValue;
   }
-  if (!make_map3(&g.ttk, a.tk, a.dh, a.Hkv, nodes, 1, AT_KEYS)) return cudaErrorInvalidValue;
-  if (!make_map3(&g.ttv, a.tv, a.dh, a.Hkv, nodes, 1, AT_KEYS)) return cudaErrorInvalidValue;
-  if (a.rows_per_block != AT_ROWS && a.rows_per_block != AT_ROWS * AT_TILES) return cudaErrorInvalidValue;
-  g.nt = a.rows_per_block / AT_ROWS;
-  const int H = a.dh / 64;
-  const size_t fixed = 1024 + (size_t)g.nt * H * AT_ROWS * 128 + (size_t)g.nt * 2 * AT_ROWS * 128;
-  const size_t kv_stage = (size_t)2 * H * AT_KEYS * 128;
-  g.stages = (int)std::min<size_t>(AT_STAGES, (226u * 1024u - fixed) / kv_stage);   // 227 KB per CTA
-  if (g.stages < 2) return cudaErrorInvalidValue;
-  const size_t smem = fixed + (size_t)g.stages * kv_stage;
-  auto kern = a.dh == 128 ? tree_attn_tc_kernel<128> : tree_attn_tc_kernel<64>;
+  if (!make_map3(&g.ttk, a.tk, a.dh, a.Hkv, nodes, 1, keys)) return cudaErrorInvalidValue;
+  if (!make_map3(&g.ttv, a.tv, a.dh, a.Hkv, nodes, 1, keys)) return cudaErrorInvalidValue;
+  void (*kern)(AttnTcArgs);
+  if (a.dh == 128) kern = keys == AT_KEYS1 ? tree_attn_tc_kernel<128, AT_KEYS1> : tree_attn_tc_kernel<128, AT_KEYS>;
+  else kern = keys == AT_KEYS1 ? tree_attn_tc_kernel<64, AT_KEYS1> : tree_attn_tc_kernel<64, AT_KEYS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.nsplit + 1, a.Hkv, a.B * a.nrb);
