@@ -326,6 +326,7 @@ medusa_status gather_impl(const medusa_plan* p, const medusa_weights* w, const i
   return MEDUSA_OK;
 }
 
+// q (fp32) may be null when only the bf16 copy for tensor-core attention is needed.
 medusa_status qkv_impl(const medusa_plan* p, const medusa_weights* w, const int32_t* pos, float* q,
                        void* tk, void* tv, void* ws, cudaStream_t st) {
   const medusa_dims& d = p->d;
@@ -352,7 +353,26 @@ medusa_status qkv_impl(const medusa_plan* p, const medusa_weights* w, const int3
     s.rows = rows[i];
     s.out_off = offs[i];
   }
-  LAUNCH(p, KN_QKV, st, p->tc_nodes ? launch_umma_gemm(a, p->d_status, st) : launch_rowdot(a, d.dtype, st));
+  if (p->tc_nodes) {
+    // rotary embedding and the q / k / v outputs in the projection's own epilogue
+    a.epi = EPI_ROPE;
+    a.rope_pos = pos;
+    a.rope_table = p->d_rope;
+    a.rope_rows = p->rope_rows;
+    a.rope_dh = d.dh;
+    a.rope_qcols = qd;
+    a.rope_kcols = kd;
+    a.rq = q;
+    a.rqb = p->tc_attn ? at<bf16>(ws, p->o_qb) : nullptr;
+    a.rk = tk;
+    a.rv = tv;
+    a.rkv_bf16 = d.dtype == MEDUSA_BF16;
+    a.rope_status = p->d_status;
+    LAUNCH(p, KN_QKV, st, launch_umma_gemm(a, p->d_status, st));
+    return MEDUSA_OK;
+  }
+  if (!q) return MEDUSA_ERR_INVALID;
+  LAUNCH(p, KN_QKV, st, launch_rowdot(a, d.dtype, st));
   LAUNCH(p, KN_ROPE, st, launch_rope_split(qkv, pos, p->M, d.Hq, d.Hkv, d.dh, p->d_rope, p->rope_rows,
                                            p->d_status, d.dtype, q,
                                            p->tc_attn ? at<bf16>(ws, p->o_qb) : nullptr, tk, tv, st));
@@ -958,7 +978,8 @@ medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* r
     LAUNCH(p, KN_SELECT, st, launch_heads_select(t, mg, tr, cnt, st));
   }
   if ((s = gather_impl(p, w, tok, ws, st)) != MEDUSA_OK) return s;
-  if ((s = qkv_impl(p, w, pos, q, tk, tv, ws, st)) != MEDUSA_OK) return s;
+  // tensor-core attention reads the bf16 copy of q only
+  if ((s = qkv_impl(p, w, pos, p->tc_attn && p->tc_nodes ? nullptr : q, tk, tv, ws, st)) != MEDUSA_OK) return s;
   if ((s = attn_impl(p, q, kv, tk, tv, p->d_mask, o, true, true, ws, st)) != MEDUSA_OK) return s;
   if ((s = out_impl(p, w, o, true, hp, true, ws, st)) != MEDUSA_OK) return s;
   float* vlog = at<float>(ws, p->o_vlog);

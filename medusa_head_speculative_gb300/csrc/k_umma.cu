@@ -107,6 +107,76 @@ __device__ __forceinline__ void epilogue4(const MatArgs& a, const MatSeg& s, int
   }
 }
 
+__device__ __forceinline__ void store4(float* p, const float (&y)[4]) {
+  if (aligned16(p)) *reinterpret_cast<float4*>(p) = make_float4(y[0], y[1], y[2], y[3]);
+  else for (int e = 0; e < 4; ++e) p[e] = y[e];
+}
+__device__ __forceinline__ void store4(bf16* p, const float (&y)[4]) {
+  if (aligned8(p)) {
+    __nv_bfloat162 t[2] = {__floats2bfloat162_rn(y[0], y[1]), __floats2bfloat162_rn(y[2], y[3])};
+    *reinterpret_cast<uint2*>(p) = *reinterpret_cast<const uint2*>(t);
+  } else {
+    for (int e = 0; e < 4; ++e) p[e] = __float2bfloat16_rn(y[e]);
+  }
+}
+
+// EPI_ROPE: outputs c0..c0+3 (x0) and c0+half..c0+half+3 (x1) of node row m, columns of
+// the stacked q | k | v projection with c0 % dh < dh / 2.  q and k are rotated in pairs
+// (i, i + dh/2) at the node's position (rotate-half form, cos | sin rows of the table):
+//   y_i = x_i cos - x_{i+dh/2} sin,   y_{i+dh/2} = x_{i+dh/2} cos + x_i sin;
+// v is passed through.  (Rotary position embedding as used by Llama, cited by "Medusa:
+// Simple LLM Inference Acceleration Framework with Multiple Decoding Heads" for the
+// position ids of the tree nodes.)
+__device__ void rope4(const MatArgs& a, int m, int c0, float4 v0, float4 v1) {
+  const int dh = a.rope_dh, half = dh / 2, qc = a.rope_qcols, kc = a.rope_kcols;
+  float x0[4] = {v0.x, v0.y, v0.z, v0.w}, x1[4] = {v1.x, v1.y, v1.z, v1.w};
+  if (c0 >= qc + kc) {                                  // v
+    const long o = (long)m * kc + (c0 - qc - kc);
+    if (a.rkv_bf16) {
+      store4(reinterpret_cast<bf16*>(a.rv) + o, x0);
+      store4(reinterpret_cast<bf16*>(a.rv) + o + half, x1);
+    } else {
+      store4(reinterpret_cast<float*>(a.rv) + o, x0);
+      store4(reinterpret_cast<float*>(a.rv) + o + half, x1);
+    }
+    return;
+  }
+  int p = a.rope_pos[m];
+  if (p < 0 || p >= a.rope_rows) {
+    set_flag(a.rope_status, MEDUSA_FLAG_KV_CAPACITY);
+    p = p < 0 ? 0 : a.rope_rows - 1;
+  }
+  const int i0 = c0 % dh;
+  const float* cs = a.rope_table + (long)p * dh;
+  float y0[4], y1[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float c = cs[i0 + e], sn = cs[half + i0 + e];
+    y0[e] = x0[e] * c - x1[e] * sn;
+    y1[e] = x1[e] * c + x0[e] * sn;
+  }
+  if (c0 < qc) {                                        // q
+    const long o = (long)m * qc + c0;
+    if (a.rq) {
+      store4(a.rq + o, y0);
+      store4(a.rq + o + half, y1);
+    }
+    if (a.rqb) {
+      store4(a.rqb + o, y0);
+      store4(a.rqb + o + half, y1);
+    }
+  } else {                                              // k
+    const long o = (long)m * kc + (c0 - qc);
+    if (a.rkv_bf16) {
+      store4(reinterpret_cast<bf16*>(a.rk) + o, y0);
+      store4(reinterpret_cast<bf16*>(a.rk) + o + half, y1);
+    } else {
+      store4(reinterpret_cast<float*>(a.rk) + o, y0);
+      store4(reinterpret_cast<float*>(a.rk) + o + half, y1);
+    }
+  }
+}
+
 // Epilogue of a CTA's accumulators through shared memory.  Thread = TMEM lane = weight
 // row, so reading TMEM gives each thread one output column for many activation rows;
 // written out directly, a warp's store covers only 128 bytes of 16 different rows.
@@ -131,12 +201,27 @@ __device__ void staged_epilogue(const MatArgs& a, const MatSeg& s, int rbase, in
       }
     }
     __syncthreads();
-    for (int i = tid; i < cm * q4; i += 128) {
-      const int ml = i / q4, q = i - ml * q4;
-      const int m = m0 + c0 + ml, r = rbase + 4 * q;
-      if (m < a.M && r < s.rows) {
-        const float4 v = *reinterpret_cast<const float4*>(stage + ml * rt + 4 * q);
-        epilogue4(a, s, m, r, v, kpart ? kpart + ((long)blockIdx.z * a.M + m) * a.ldo : nullptr);
+    if (a.epi == EPI_ROPE && !kpart) {
+      // weight tiles start on head boundaries: both halves of every head are in the stage
+      const int dh = a.rope_dh, half = dh / 2, gh = half / 4, heads = rt / dh;
+      for (int i = tid; i < cm * heads * gh; i += 128) {
+        const int ml = i / (heads * gh), rem = i - ml * heads * gh;
+        const int hh = rem / gh, rl = hh * dh + 4 * (rem - hh * gh);
+        const int m = m0 + c0 + ml, r = rbase + rl;
+        if (m < a.M && r < s.rows) {
+          const float4 v0 = *reinterpret_cast<const float4*>(stage + ml * rt + rl);
+          const float4 v1 = *reinterpret_cast<const float4*>(stage + ml * rt + rl + half);
+          rope4(a, m, s.out_off + r, v0, v1);
+        }
+      }
+    } else {
+      for (int i = tid; i < cm * q4; i += 128) {
+        const int ml = i / q4, q = i - ml * q4;
+        const int m = m0 + c0 + ml, r = rbase + 4 * q;
+        if (m < a.M && r < s.rows) {
+          const float4 v = *reinterpret_cast<const float4*>(stage + ml * rt + 4 * q);
+          epilogue4(a, s, m, r, v, kpart ? kpart + ((long)blockIdx.z * a.M + m) * a.ldo : nullptr);
+        }
       }
     }
     __syncthreads();
@@ -442,6 +527,31 @@ __global__ void splitk_reduce_kernel(const MatArgs a, const float* __restrict__ 
   constexpr int ZMAX = 8;
   pdl_trigger();
   pdl_wait();
+  if (a.epi == EPI_ROPE) {
+    // one item = 4 columns of the first half of a head and their partners dh/2 further on
+    const int dh = a.rope_dh, half = dh / 2, gh = half / 4;
+    const int per_row = (int)(a.ldo / dh) * gh;
+    const long n = (long)a.M * per_row;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+      const int m = (int)(i / per_row), rem = (int)(i - (long)m * per_row), hg = rem / gh;
+      const int c0 = hg * dh + 4 * (rem - hg * gh);
+      float4 v0[ZMAX], v1[ZMAX];
+#pragma unroll
+      for (int z = 0; z < ZMAX; ++z) {
+        const float* row = kpart + ((long)z * a.M + m) * a.ldo;
+        v0[z] = z < ksplit ? __ldcg(reinterpret_cast<const float4*>(row + c0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v1[z] = z < ksplit ? __ldcg(reinterpret_cast<const float4*>(row + c0 + half)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+#pragma unroll
+      for (int z = 0; z < ZMAX; ++z) {
+        s0.x += v0[z].x; s0.y += v0[z].y; s0.z += v0[z].z; s0.w += v0[z].w;
+        s1.x += v1[z].x; s1.y += v1[z].y; s1.z += v1[z].z; s1.w += v1[z].w;
+      }
+      rope4(a, m, c0, s0, s1);
+    }
+    return;
+  }
   const int c4 = cols / 4;
   const long n = (long)a.M * c4;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
@@ -510,7 +620,7 @@ static cudaError_t launch_splitk_reduce(const MatArgs& a, int ksplit, cudaStream
 // K ranges for a launch of `ctas` CTAs that leaves SMs idle (single-segment launches, or
 // plain stores): about two CTAs per SM, at least 4 K blocks each, partials within kpart.
 static int choose_ksplit(const MatArgs& a, long ctas, int nk, int num_sms) {
-  const bool splittable = a.nseg == 1 || (a.epi == EPI_STORE && !a.out_hi);
+  const bool splittable = a.nseg == 1 || (a.epi == EPI_STORE && !a.out_hi) || a.epi == EPI_ROPE;
   if (!splittable || !a.kpart || ctas >= num_sms || (a.nseg == 1 ? a.seg[0].rows : a.ldo) % 4 != 0)
     return 1;
   int ksplit = (int)(2L * num_sms / ctas);

@@ -15,7 +15,7 @@ constexpr int kMaxSeg = 10;     // LM head + up to 8 Medusa heads (+1 spare)
 constexpr int kTops = 16;       // candidates kept per head (MEDUSA_MAX_TOPS)
 constexpr int kMaskWords = 8;   // 256 nodes / 32
 
-enum Epi { EPI_STORE = 0, EPI_SILU_RES = 1, EPI_RES_ADD = 2 };
+enum Epi { EPI_STORE = 0, EPI_SILU_RES = 1, EPI_RES_ADD = 2, EPI_ROPE = 3 };
 
 // One row block of a stacked projection Y[m][out_off + r] = sum_k X[m][k] W[r][k].
 struct MatSeg {
@@ -43,6 +43,19 @@ struct MatArgs {
   __nv_bfloat16* out_lo;
   float* kpart;                  // tensor-core path: scratch for split-K partials, or null
   size_t kpart_bytes;
+  // EPI_ROPE (tensor-core path, segments q | k | v of one head size): rotary embedding of
+  // the q and k outputs at position rope_pos[m] (cos | sin rows of rope_table), then q to
+  // rq (fp32, optional) and rqb (bf16, optional), k to rk and v to rv in the cache dtype
+  // (bf16 when rkv_bf16, else fp32); `out` is not written.
+  const int32_t* rope_pos;
+  const float* rope_table;
+  int rope_rows, rope_dh, rope_qcols, rope_kcols;
+  float* rq;
+  __nv_bfloat16* rqb;
+  void* rk;
+  void* rv;
+  int rkv_bf16;
+  uint32_t* rope_status;
 };
 
 // CUDA-core row-dot projection: dtype 0 = f32 weights, 1 = bf16.
