@@ -44,6 +44,12 @@ Readings where the pages are silent or disagree (each also listed in the design 
       weight exceeds u_final times the remaining total); it is the next step's root.
       p = softmax(z / T); T = 0 is greedy.  Uniforms are inputs: uniforms[0] for the
       draw, uniforms[1 + (d - 1) * 16 + j] for the j-th child tried at depth d.
+  R9  A backbone of n synthetic layers (the multi-layer form of R0 for a real backbone's
+      per-layer calls): x_0 = E[tok]; layer l takes q, k, v from x_l with its own
+      projections (RoPE at the node position), attends over its own prefix cache plus
+      its own tree keys under the same mask, and x_{l+1} = x_l + Wo_l o_l; h' = x_n.
+      Compaction appends the kept nodes' layer-l keys/values to layer l's cache.  With
+      one layer this is R0.
 """
 from __future__ import annotations
 
@@ -542,7 +548,13 @@ def medusa_step(wts, h, kc, vc, spec, dims, accept, root=None, s=None):
                     for n in range(n1)])
     r.o = tree_attention(r.q, kc, vc, r.k, r.v, tree_mask(spec))
     r.hp = np.stack([layer_out(wts, X[n], r.o[n]) for n in range(n1)])
+    return _verify(r, wts, spec, accept)
 
+
+def _verify(r, wts, spec, accept):
+    """Steps (5)-(6) from the layer outputs r.hp: verification logits, acceptance, the
+    kept path, the next root / hidden state, and the kept nodes' keys/values (r.k, r.v)."""
+    n1 = spec.N + 1
     # verification logits ([MEDUSA] §3.4 Tree Attention, Step 6)
     r.zv = (np.asarray(wts["lm"], dtype=np.float64) @ r.hp.T).T   # z_n = LM h'_n
     r.am = np.empty(n1, dtype=np.int64)
@@ -618,3 +630,89 @@ def medusa_generate(wts, h, kc, vc, spec, dims, accept, n_steps):
         vc = np.concatenate([vc, r.kv_new[1]])
         h, root = r.h_next, r.root_next
     return tokens, steps, kc, vc
+
+
+# ============================================================ multi-layer backbone (R9)
+def medusa_step_layers(wts, layers, h, caches, spec, dims, accept, root=None, s=None):
+    """One decode step of one sequence through an n-layer backbone (R9).
+
+    layers: per layer a dict with wq, wk, wv, wo (layer 0's may be wts itself); caches:
+    per layer (kc, vc) post-RoPE prefix keys/values [L][Hkv][dh] (the same L in every
+    layer).  The result's k / v / q / o are layer 0's; layer_k / layer_v hold every
+    layer's tree keys/values and kv_new_layers the kept nodes' per layer.
+    """
+    Hq, Hkv, dh, base = dims["Hq"], dims["Hkv"], dims["dh"], dims["rope_base"]
+    h = f64(h)
+    L = f64(caches[0][0]).shape[0]
+    K = max(spec.depth)
+    s = s or [max(p[k] for p in spec.paths if len(p) > k) + 1 for k in range(K)]
+    r = heads_step(wts, h, max(s), s)
+    if root is not None:
+        r.root, r.root_margin = int(root), math.inf
+    n1 = spec.N + 1
+    r.tok = tree_tokens(spec, r.root, r.topk)
+    r.pos = tree_positions(spec, L)
+    M = tree_mask(spec)
+    X = np.stack([np.asarray(wts["emb"][int(t)], dtype=np.float64) for t in r.tok])
+    r.layer_k, r.layer_v = [], []
+    for li, lw in enumerate(layers):
+        kc, vc = f64(caches[li][0]), f64(caches[li][1])
+        Q = (X @ f64(lw["wq"]).T).reshape(n1, Hq, dh)
+        Kt = (X @ f64(lw["wk"]).T).reshape(n1, Hkv, dh)
+        Vt = (X @ f64(lw["wv"]).T).reshape(n1, Hkv, dh)
+        q = np.stack([[rope(Q[n, hh], r.pos[n], base) for hh in range(Hq)] for n in range(n1)])
+        k = np.stack([[rope(Kt[n, hh], r.pos[n], base) for hh in range(Hkv)] for n in range(n1)])
+        o = tree_attention(q, kc, vc, k, Vt, M)
+        X = np.stack([layer_out(lw, X[n], o[n]) for n in range(n1)])
+        r.layer_k.append(k)
+        r.layer_v.append(Vt)
+        if li == 0:
+            r.q, r.k, r.v, r.o = q, k, Vt, o
+    r.hp = X
+    r = _verify(r, wts, spec, accept)
+    r.kv_new_layers = [(k[r.path_nodes].copy(), v[r.path_nodes].copy())
+                       for k, v in zip(r.layer_k, r.layer_v)]
+    return r
+
+
+def sequential_greedy_layers(wts, layers, h, caches, dims, n_tokens):
+    """Plain greedy decoding through the n-layer backbone, one token per forward pass.
+    Returns (tokens, final caches as a list of (K, V))."""
+    Hq, Hkv, dh, base = dims["Hq"], dims["Hkv"], dims["dh"], dims["rope_base"]
+    G = Hq // Hkv
+    Ks = [list(f64(c[0])) for c in caches]
+    Vs = [list(f64(c[1])) for c in caches]
+    tok, _ = argmax_lowest(lm_head(wts["lm"], f64(h)))
+    out = []
+    while len(out) < n_tokens:
+        out.append(tok)
+        pos = len(Ks[0])
+        x = np.asarray(wts["emb"][tok], dtype=np.float64)
+        for li, lw in enumerate(layers):
+            q = np.stack([rope(qh, pos, base) for qh in matvec(lw["wq"], x).reshape(Hq, dh)])
+            k = np.stack([rope(kh, pos, base) for kh in matvec(lw["wk"], x).reshape(Hkv, dh)])
+            v = matvec(lw["wv"], x).reshape(Hkv, dh)
+            Ks[li].append(k)
+            Vs[li].append(v)
+            Ka, Va = np.stack(Ks[li]), np.stack(Vs[li])
+            o = np.stack([attend(q[hq], Ka[:, hq // G], Va[:, hq // G]) for hq in range(Hq)])
+            x = layer_out(lw, x, o)
+        tok, _ = argmax_lowest(lm_head(wts["lm"], x))
+    return out, [(np.stack(a), np.stack(b)) for a, b in zip(Ks, Vs)]
+
+
+def medusa_generate_layers(wts, layers, h, caches, spec, dims, accept, n_steps):
+    """Repeated n-layer decode steps carrying (h_next, root_next) and every layer's
+    compacted cache.  Returns (tokens, per-step results, final caches)."""
+    caches = [(f64(a), f64(b)) for a, b in caches]
+    h = f64(h)
+    root = None
+    tokens, steps = [], []
+    for _ in range(n_steps):
+        r = medusa_step_layers(wts, layers, h, caches, spec, dims, accept, root=root)
+        steps.append(r)
+        tokens += [int(t) for t in r.out_tok]
+        caches = [(np.concatenate([kc, kn]), np.concatenate([vc, vn]))
+                  for (kc, vc), (kn, vn) in zip(caches, r.kv_new_layers)]
+        h, root = r.h_next, r.root_next
+    return tokens, steps, caches

@@ -143,6 +143,23 @@ def weights(w: Workload) -> dict:
     }
 
 
+def layer_weights(w: Workload, layer: int, planted: bool = False) -> dict:
+    """Projections of backbone layer `layer` (0: the same tensors as `weights`), stored
+    [out][in]: wq, wk, wv, wo.  Layers past 0 draw from their own streams; `planted`
+    scales Wo by 0.1 as planted_weights does, so the residual stream stays dominant."""
+    d, qd, kd = w.d, w.Hq * w.dh, w.Hkv * w.dh
+    sd = 1.0 / math.sqrt(d)
+    lw = {
+        "wq": _normal(w, "wq", (qd, d), sd, layer),
+        "wk": _normal(w, "wk", (kd, d), sd, layer),
+        "wv": _normal(w, "wv", (kd, d), sd, layer),
+        "wo": _normal(w, "wo", (d, qd), 1.0 / math.sqrt(qd), layer),
+    }
+    if planted:
+        lw["wo"] = (lw["wo"].to(torch.float32) * 0.1).to(w.torch_dtype)
+    return lw
+
+
 def hidden(w: Workload) -> torch.Tensor:
     """Last hidden state h_t [B][d] as fp32 holding dtype-rounded N(0,1) values."""
     return _normal(w, "h", (w.B, w.d), 1.0).to(torch.float32)
@@ -156,10 +173,12 @@ def uniforms(w: Workload, step: int = 0) -> torch.Tensor:
     return torch.from_numpy(a)
 
 
-def kv_prefix(w: Workload, b: int):
-    """Post-RoPE prefix keys and values of sequence b: two [L_b][Hkv][dh] tensors."""
+def kv_prefix(w: Workload, b: int, layer: int = 0):
+    """Post-RoPE prefix keys and values of sequence b in backbone layer `layer`: two
+    [L_b][Hkv][dh] tensors."""
     shape = (w.lengths[b], w.Hkv, w.dh)
-    return _normal(w, "kc", shape, 1.0, b), _normal(w, "vc", shape, 1.0, b)
+    i = b + 100000 * layer
+    return _normal(w, "kc", shape, 1.0, i), _normal(w, "vc", shape, 1.0, i)
 
 
 def page_table(w: Workload) -> torch.Tensor:
@@ -169,8 +188,8 @@ def page_table(w: Workload) -> torch.Tensor:
     return torch.from_numpy(perm.reshape(w.B, P))
 
 
-def kv_cache(w: Workload):
-    """Device-layout KV cache holding every sequence's prefix.
+def kv_cache(w: Workload, layer: int = 0):
+    """Device-layout KV cache of backbone layer `layer` holding every sequence's prefix.
 
     Contiguous: K, V each [B][capacity][Hkv][dh].  Paged (page_size > 0): K, V each
     [B*pages_per_seq][page_size][Hkv][dh] plus the page table; logical slot t of
@@ -181,7 +200,7 @@ def kv_cache(w: Workload):
     kc = torch.zeros((w.B, cap, Hkv, dh), dtype=w.torch_dtype)
     vc = torch.zeros((w.B, cap, Hkv, dh), dtype=w.torch_dtype)
     for b in range(w.B):
-        k, v = kv_prefix(w, b)
+        k, v = kv_prefix(w, b, layer)
         kc[b, :w.lengths[b]] = k
         vc[b, :w.lengths[b]] = v
     if not w.page_size:

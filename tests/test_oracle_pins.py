@@ -439,3 +439,58 @@ def test_rejection_walk_at_low_temperature_is_the_greedy_walk():
         path, v, _ = O.rejection_walk(spec, tok, zv, 1e-4, rng.random(1 + 32) * 0.999 + 0.0005)
         assert list(path) == list(greedy_path)
         assert v == am[path[-1]]
+
+
+# ---------------------------------------------------------------- multi-layer backbone (R9)
+def _layers_setup(planted, n_layers):
+    w, ow, h, k, v, dims = _tiny_setup(planted)
+    layers = [ow] + [O.oracle_weights(S.layer_weights(w, l, planted=planted))
+                     for l in range(1, n_layers)]
+    caches = [(k, v)] + [S.kv_prefix(w, 0, l) for l in range(1, n_layers)]
+    return w, ow, h, layers, caches, dims
+
+
+def test_one_layer_backbone_is_the_single_layer_step():
+    """R9 with one layer is R0: the same tokens, layer outputs, logits and path."""
+    w, ow, h, layers, caches, dims = _layers_setup(True, 1)
+    h = torch.from_numpy(ow["emb"][7].astype(np.float32))
+    spec = O.cartesian_tree(w.s)
+    a = O.medusa_step(ow, h, caches[0][0], caches[0][1], spec, dims, {"mode": "greedy"})
+    b = O.medusa_step_layers(ow, layers, h, caches, spec, dims, {"mode": "greedy"})
+    assert list(a.tok) == list(b.tok) and list(a.path_nodes) == list(b.path_nodes)
+    np.testing.assert_array_equal(a.hp, b.hp)
+    np.testing.assert_array_equal(a.zv, b.zv)
+    np.testing.assert_array_equal(a.kv_new[0], b.kv_new_layers[0][0])
+
+
+def test_layers_differ_so_the_pins_below_see_every_layer():
+    """Layer 1's projections and cache are not layer 0's, and a second layer changes
+    h' (a dropped layer loop or a reused cache would fail the decoding pins)."""
+    w, ow, h, layers, caches, dims = _layers_setup(False, 2)
+    assert not np.array_equal(layers[0]["wq"], layers[1]["wq"])
+    assert not np.array_equal(O.f64(caches[0][0]), O.f64(caches[1][0]))
+    spec = O.cartesian_tree(w.s)
+    one = O.medusa_step_layers(ow, layers[:1], h, caches[:1], spec, dims, {"mode": "greedy"})
+    two = O.medusa_step_layers(ow, layers, h, caches, spec, dims, {"mode": "greedy"})
+    assert np.abs(one.hp - two.hp).max() > 1e-3
+    np.testing.assert_array_equal(one.layer_k[0], two.layer_k[0])   # layer 0 sees layer 0 only
+
+
+@pytest.mark.parametrize("planted,n_layers", [(False, 2), (True, 3)])
+def test_multi_layer_medusa_greedy_reproduces_sequential_greedy(planted, n_layers):
+    """Through an n-layer backbone, Medusa with greedy verification emits the plain greedy
+    continuation and leaves every layer's cache as sequential decoding does (MEDUSA 精读
+    section 4), so tree attention and compaction are right in every layer."""
+    w, ow, h, layers, caches, dims = _layers_setup(planted, n_layers)
+    if planted:
+        h = torch.from_numpy(ow["emb"][7].astype(np.float32))
+    spec = O.cartesian_tree(w.s)
+    toks, steps, fin = O.medusa_generate_layers(ow, layers, h, caches, spec, dims,
+                                                {"mode": "greedy"}, 5)
+    ref, ref_caches = O.sequential_greedy_layers(ow, layers, h, caches, dims, len(toks))
+    assert toks == ref
+    for (kc, vc), (kr, vr) in zip(fin, ref_caches):
+        np.testing.assert_allclose(kc, kr[:len(kc)], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(vc, vr[:len(vc)], rtol=1e-10, atol=1e-12)
+    if planted:
+        assert max(s.m for s in steps) >= 2
