@@ -47,6 +47,7 @@ extern "C" {
 #define MEDUSA_MAX_HEADS 8     /* K <= 8 Medusa heads ([MEDUSA] §3.4: five suffice) */
 #define MEDUSA_MAX_TOPS 16     /* s_k <= 16 candidates per head */
 #define MEDUSA_MAX_NODES 256   /* N + 1 <= 256 packed tree nodes (root included) */
+#define MEDUSA_MAX_LAYERS 1024 /* backbone layers of medusa_step_layers */
 
 typedef enum {
   MEDUSA_OK = 0,
@@ -178,6 +179,43 @@ medusa_status medusa_step(const medusa_plan* plan, const float* h, const int32_t
                           const medusa_weights* w, const medusa_kv* kv, medusa_accept acc,
                           const medusa_outputs* out, void* workspace, size_t ws_bytes,
                           void* stream);
+
+/* ---- multi-layer backbone
+ * The tree nodes pass through n synthetic layers instead of one, the way a real
+ * backbone's per-layer calls would ([MEDUSA] §3.4 Tree Attention: every layer attends
+ * over its own cache plus the tree under the same mask and position ids):
+ *   x_0 = E[tok];  layer l: q, k, v = Wq_l x_l, Wk_l x_l, Wv_l x_l (RoPE at the node
+ *   position), o_l = tree attention over layer l's prefix and the tree's layer-l keys,
+ *   x_{l+1} = x_l + Wo_l o_l;  h' = x_n  (verification, acceptance and h_next as in
+ *   medusa_step).  After acceptance the kept nodes' keys/values are appended to every
+ *   layer's cache.
+ * One medusa_layer per layer: its projections ([out][in] row-major, the plan's dtype,
+ * 16-byte aligned; shapes as in medusa_weights) and its KV cache (the layout medusa_kv
+ * describes; every layer shares the page table and the lengths). */
+typedef struct {
+  const void* wq;   /* [Hq*dh][d]  */
+  const void* wk;   /* [Hkv*dh][d] */
+  const void* wv;   /* [Hkv*dh][d] */
+  const void* wo;   /* [d][Hq*dh]  */
+  void* k;          /* this layer's cached keys   (device, caller-owned, updated) */
+  void* v;          /* this layer's cached values (device, caller-owned, updated) */
+} medusa_layer;
+
+/* Bytes of workspace medusa_step_layers needs for n_layers layers (the single-layer size
+ * plus each further layer's tree keys/values); 0 for n_layers outside 1..MEDUSA_MAX_LAYERS. */
+size_t medusa_workspace_size_layers(const medusa_plan* plan, int n_layers);
+
+/* One decode step through an n_layers-layer backbone.  h, root_in, acc, out, stream as
+ * in medusa_step; w supplies the heads, the LM head and the embedding (its wq..wo are not
+ * read); layers: host array of n_layers entries (read during the call only); kv supplies
+ * the page table, len and len_out (its k, v are not read; len_out may alias len).
+ * Errors: MEDUSA_ERR_INVALID for n_layers outside 1..MEDUSA_MAX_LAYERS, a NULL layer
+ * pointer or misaligned weights, plus medusa_step's conditions.  With n_layers = 1 the
+ * result equals medusa_step's with that layer's weights and cache. */
+medusa_status medusa_step_layers(const medusa_plan* plan, const float* h, const int32_t* root_in,
+                                 const medusa_weights* w, const medusa_layer* layers, int n_layers,
+                                 const medusa_kv* kv, medusa_accept acc, const medusa_outputs* out,
+                                 void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------ stages */
 /* (a) Heads ([MEDUSA] §3.4 MEDUSA Heads eq.; Tree Attention Step 1).  Writes the

@@ -44,6 +44,10 @@ class Weights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("w1", "w2", "lm", "emb", "wq", "wk", "wv", "wo")]
 
 
+class Layer(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("wq", "wk", "wv", "wo", "k", "v")]
+
+
 class KV(C.Structure):
     _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("page_table", C.c_void_p),
                 ("len", C.c_void_p), ("len_out", C.c_void_p)]
@@ -85,6 +89,9 @@ def lib():
         "medusa_get_status": (I, [P, P, C.POINTER(C.c_uint32)]),
         "medusa_step": (I, [P, P, P, C.POINTER(Weights), C.POINTER(KV), Accept,
                             C.POINTER(Outputs), P, SZ, P]),
+        "medusa_workspace_size_layers": (SZ, [P, I]),
+        "medusa_step_layers": (I, [P, P, P, C.POINTER(Weights), C.POINTER(Layer), I, C.POINTER(KV),
+                                   Accept, C.POINTER(Outputs), P, SZ, P]),
         "medusa_heads": (I, [P, P, P, C.POINTER(Weights), P, P, P, P, P, SZ, P]),
         "medusa_heads_noalloc": (I, [P, P, P, C.POINTER(Weights), P, P, P, P]),
         "medusa_tree_build": (I, [P, P, P, P, P, P, P, P, P]),
@@ -186,6 +193,9 @@ class Plan:
     def workspace_size(self):
         return lib().medusa_workspace_size(self.handle)
 
+    def workspace_size_layers(self, n_layers):
+        return lib().medusa_workspace_size_layers(self.handle, n_layers)
+
     def status(self, stream=None):
         flags = C.c_uint32(0)
         code = lib().medusa_get_status(self.handle, _stream(stream), C.byref(flags))
@@ -221,6 +231,14 @@ def weights_struct(w):
     return Weights(*(ptr(w.get(n)) for n in ("w1", "w2", "lm", "emb", "wq", "wk", "wv", "wo")))
 
 
+def layers_array(layers):
+    """ctypes array of Layer from dicts with wq, wk, wv, wo, k, v (device tensors)."""
+    arr = (Layer * len(layers))()
+    for i, L in enumerate(layers):
+        arr[i] = Layer(*(ptr(L[n]) for n in ("wq", "wk", "wv", "wo", "k", "v")))
+    return arr
+
+
 def kv_struct(k, v, length, len_out=None, page_table=None):
     return KV(ptr(k), ptr(v), ptr(page_table), ptr(length), ptr(len_out))
 
@@ -239,6 +257,14 @@ def step(plan, h, root_in, wts, kv, accept, outs, ws, stream=None):
     _check("medusa_step", lib().medusa_step(plan.handle, ptr(h), ptr(root_in), C.byref(wts),
                                             C.byref(kv), accept, C.byref(outs), ptr(ws),
                                             ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def step_layers(plan, h, root_in, wts, layers, kv, accept, outs, ws, stream=None):
+    """medusa_step_layers; `layers` from layers_array."""
+    _check("medusa_step_layers",
+           lib().medusa_step_layers(plan.handle, ptr(h), ptr(root_in), C.byref(wts), layers,
+                                    len(layers), C.byref(kv), accept, C.byref(outs), ptr(ws),
+                                    ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def heads(plan, h, root_in, wts, logits, topk_tok, topk_val, root, ws, stream=None):

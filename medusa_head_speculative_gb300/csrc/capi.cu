@@ -204,8 +204,9 @@ void layout(medusa_plan* p) {
   const size_t widest = std::max(std::max(D, qd), std::min<size_t>(V, 128 * 148));
   p->kpart_bytes = p->tc_nodes ? std::min<size_t>(8 * M * widest * 4, (size_t)64 << 20) : 0;
   p->o_kpart = take(p->kpart_bytes);
-  // counters: [0,B) selection, [B,2B) commit per sequence, then one per node row
-  p->o_cnt = take((2 * B + M) * 4);
+  // counters: [0,B) selection, [B,2B) commit per sequence, one per node row, then [B]
+  // for the multi-layer compaction
+  p->o_cnt = take((3 * B + M) * 4);
   p->o_vparts = take(M * 4 * 6 * 4);
   p->ws_bytes = off;
 }
@@ -327,8 +328,10 @@ medusa_status gather_impl(const medusa_plan* p, const medusa_weights* w, const i
 }
 
 // q (fp32) may be null when only the bf16 copy for tensor-core attention is needed.
+// x_in: the previous layer's h' (fp32; its bf16 hi/lo halves in the workspace) for backbone
+// layers past the first; null for the first layer, which reads x = E[tok].
 medusa_status qkv_impl(const medusa_plan* p, const medusa_weights* w, const int32_t* pos, float* q,
-                       void* tk, void* tv, void* ws, cudaStream_t st) {
+                       void* tk, void* tv, void* ws, cudaStream_t st, const float* x_in = nullptr) {
   const medusa_dims& d = p->d;
   const int qd = d.Hq * d.dh, kd = d.Hkv * d.dh;
   float* qkv = at<float>(ws, p->o_qkv);
@@ -346,9 +349,15 @@ medusa_status qkv_impl(const medusa_plan* p, const medusa_weights* w, const int3
   for (int i = 0; i < 3; ++i) {
     MatSeg& s = a.seg[i];
     s.w = ws_[i];
-    s.x = p->tc_nodes ? nullptr : at<float>(ws, p->o_x);
-    s.a_hi = p->tc_nodes ? at<bf16>(ws, p->o_x) : nullptr;
-    s.a_lo = nullptr;                         // embedding rows are exact in bf16
+    if (x_in) {                               // h' of the previous layer
+      s.x = p->tc_nodes ? nullptr : x_in;
+      s.a_hi = p->tc_nodes ? at<bf16>(ws, p->o_hphi) : nullptr;
+      s.a_lo = p->tc_nodes ? at<bf16>(ws, p->o_hplo) : nullptr;
+    } else {
+      s.x = p->tc_nodes ? nullptr : at<float>(ws, p->o_x);
+      s.a_hi = p->tc_nodes ? at<bf16>(ws, p->o_x) : nullptr;
+      s.a_lo = nullptr;                       // embedding rows are exact in bf16
+    }
     s.ldx = d.d;
     s.rows = rows[i];
     s.out_off = offs[i];
@@ -425,9 +434,11 @@ medusa_status attn_impl(const medusa_plan* p, const float* q, const medusa_kv* k
   return MEDUSA_OK;
 }
 
-// h' = x + Wo o ; x gathered by gather_impl, o split to bf16 hi/lo when split_ready
+// h' = x + Wo o ; x gathered by gather_impl (res_in null), or the previous layer's h'
+// (res_in, fp32, may be hp itself: each element is read and then written by one thread);
+// o split to bf16 hi/lo when split_ready
 medusa_status out_impl(const medusa_plan* p, const medusa_weights* w, const float* o, bool split_ready,
-                       float* hp, bool want_split, void* ws, cudaStream_t st) {
+                       float* hp, bool want_split, void* ws, cudaStream_t st, const float* res_in = nullptr) {
   const medusa_dims& d = p->d;
   const int qd = d.Hq * d.dh;
   MatArgs a{};
@@ -443,13 +454,14 @@ medusa_status out_impl(const medusa_plan* p, const medusa_weights* w, const floa
   if (p->tc_nodes) {
     if (!split_ready)
       LAUNCH(p, KN_O_SPLIT, st, launch_split(o, at<bf16>(ws, p->o_ohi), at<bf16>(ws, p->o_olo), (long)p->M * qd, st));
-    a.res_w = at<bf16>(ws, p->o_x);
+    if (res_in) a.res_f32 = res_in;
+    else a.res_w = at<bf16>(ws, p->o_x);
     if (want_split) {
       a.out_hi = at<bf16>(ws, p->o_hphi);
       a.out_lo = at<bf16>(ws, p->o_hplo);
     }
   } else {
-    a.res_f32 = at<float>(ws, p->o_x);
+    a.res_f32 = res_in ? res_in : at<float>(ws, p->o_x);
   }
   MatSeg& s = a.seg[0];
   s.w = w->wo;
@@ -936,27 +948,28 @@ medusa_status medusa_kv_compact(const medusa_plan* p, const medusa_kv* kv, const
   return compact_impl(p, kv, tk, tv, path_nodes, n_acc, S(stream));
 }
 
-medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* root_in,
-                          const medusa_weights* w, const medusa_kv* kv, medusa_accept acc,
-                          const medusa_outputs* out, void* ws, size_t ws_bytes, void* stream) {
-  EntryScope scope("medusa_step");
-  if (!p || !h || !out) return MEDUSA_ERR_INVALID;
-  if (!out->out_tok || !out->n_acc || !out->h_next || !out->root_next) return MEDUSA_ERR_INVALID;
-  medusa_status s = check_weights(p, w, true, true, true);
-  if (s != MEDUSA_OK) return s;
-  if ((s = check_kv(p, kv, true)) != MEDUSA_OK) return s;
-  if ((s = check_accept(acc)) != MEDUSA_OK) return s;
-  if ((s = check_ws(p, ws, ws_bytes)) != MEDUSA_OK) return s;
-  const cudaStream_t st = S(stream);
+namespace {
+
+// Tree keys/values of backbone layer l >= 1 live past the single-layer workspace.
+size_t layer_kv_bytes(const medusa_plan* p) {
+  return align_up((size_t)p->M * p->d.Hkv * p->d.dh * p->esize());
+}
+size_t layers_ws_bytes(const medusa_plan* p, int n_layers) {
+  return p->ws_bytes + (size_t)(n_layers - 1) * 2 * layer_kv_bytes(p);
+}
+
+// The decode step through nl backbone layers (nl = 1: medusa_step).  With one layer the
+// fused commit also compacts the cache; with more, it only accepts and kv_compact_layers
+// then appends the kept nodes to every layer's cache.
+medusa_status step_core(const medusa_plan* p, const float* h, const int32_t* root_in,
+                        const medusa_weights* w, const medusa_layer* layers, int nl, const medusa_kv* kv,
+                        medusa_accept acc, const medusa_outputs* out, void* ws, cudaStream_t st) {
+  medusa_status s = MEDUSA_OK;
   int32_t* ttok = at<int32_t>(ws, p->o_ttok);
   int32_t* root = at<int32_t>(ws, p->o_root);
   int32_t* tok = at<int32_t>(ws, p->o_tok);
   int32_t* pos = at<int32_t>(ws, p->o_pos);
-  uint32_t* mask = at<uint32_t>(ws, p->o_mask);
-  int32_t* retr = at<int32_t>(ws, p->o_retr);
   float* q = at<float>(ws, p->o_q);
-  void* tk = at<char>(ws, p->o_tk);
-  void* tv = at<char>(ws, p->o_tv);
   float* o = at<float>(ws, p->o_o);
   float* hp = at<float>(ws, p->o_hp);
   int32_t* am = at<int32_t>(ws, p->o_am);
@@ -964,9 +977,8 @@ medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* r
   int32_t* path = out->path_nodes ? out->path_nodes : at<int32_t>(ws, p->o_path);
   float* logits = at<float>(ws, p->o_logits);
   int32_t* cnt = at<int32_t>(ws, p->o_cnt);
-  (void)mask;
-  (void)retr;
-  MEDUSA_TRY(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * (2 * p->d.B + p->M), st));
+  const int B = p->d.B;
+  MEDUSA_TRY(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * (3 * B + p->M), st));
   if ((s = heads_impl(p, h, root_in, w, logits, ttok, at<float>(ws, p->o_tval), root, ws, st)) != MEDUSA_OK)
     return s;
   {   // fused: slice top-k, head merge and node tokens / positions
@@ -978,13 +990,37 @@ medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* r
     LAUNCH(p, KN_SELECT, st, launch_heads_select(t, mg, tr, cnt, st));
   }
   if ((s = gather_impl(p, w, tok, ws, st)) != MEDUSA_OK) return s;
-  // tensor-core attention reads the bf16 copy of q only
-  if ((s = qkv_impl(p, w, pos, p->tc_attn && p->tc_nodes ? nullptr : q, tk, tv, ws, st)) != MEDUSA_OK) return s;
-  if ((s = attn_impl(p, q, kv, tk, tv, p->d_mask, o, true, true, ws, st)) != MEDUSA_OK) return s;
-  if ((s = out_impl(p, w, o, true, hp, true, ws, st)) != MEDUSA_OK) return s;
+  auto tk_of = [&](int l) -> void* {
+    return l == 0 ? at<char>(ws, p->o_tk) : at<char>(ws, p->ws_bytes + (size_t)(l - 1) * 2 * layer_kv_bytes(p));
+  };
+  auto tv_of = [&](int l) -> void* {
+    return l == 0 ? at<char>(ws, p->o_tv)
+                  : at<char>(ws, p->ws_bytes + (size_t)(l - 1) * 2 * layer_kv_bytes(p) + layer_kv_bytes(p));
+  };
+  for (int l = 0; l < nl; ++l) {
+    medusa_weights wl = *w;
+    wl.wq = layers[l].wq;
+    wl.wk = layers[l].wk;
+    wl.wv = layers[l].wv;
+    wl.wo = layers[l].wo;
+    medusa_kv kl = *kv;
+    kl.k = layers[l].k;
+    kl.v = layers[l].v;
+    // tensor-core attention reads the bf16 copy of q only
+    if ((s = qkv_impl(p, &wl, pos, p->tc_attn && p->tc_nodes ? nullptr : q, tk_of(l), tv_of(l), ws, st,
+                      l == 0 ? nullptr : hp)) != MEDUSA_OK)
+      return s;
+    if ((s = attn_impl(p, q, &kl, tk_of(l), tv_of(l), p->d_mask, o, true, true, ws, st)) != MEDUSA_OK) return s;
+    if ((s = out_impl(p, &wl, o, true, hp, true, ws, st, l == 0 ? nullptr : hp)) != MEDUSA_OK) return s;
+  }
   float* vlog = at<float>(ws, p->o_vlog);
   if ((s = vlogits_impl(p, w, hp, true, tok, acc, vlog, am, stats, ws, st, false)) != MEDUSA_OK) return s;
-  {   // fused: per-row statistics, acceptance and KV compaction
+  medusa_kv k0 = *kv;
+  k0.k = layers[0].k;
+  k0.v = layers[0].v;
+  CompactArgs c = compact_args(p, &k0, tk_of(0), tv_of(0), path, out->n_acc);
+  c.no_copy = nl > 1;
+  {   // fused: per-row statistics, acceptance and (one layer) KV compaction
     VerifyArgs v = verify_args(p, tok, acc);
     v.logits = vlog;
     v.am = am;
@@ -996,12 +1032,70 @@ medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* r
     v.path_nodes = path;
     v.h_next = out->h_next;
     v.root_next = out->root_next;
-    const CompactArgs c = compact_args(p, kv, tk, tv, path, out->n_acc);
     LAUNCH(p, KN_COMMIT, st,
-           launch_verify_commit(v, c, cnt + 2 * p->d.B, cnt + p->d.B,
-                                at<float>(ws, p->o_vparts), st));
+           launch_verify_commit(v, c, cnt + 2 * B, cnt + B, at<float>(ws, p->o_vparts), st));
+  }
+  for (int l0 = 0; nl > 1 && l0 < nl; l0 += kLayersPerLaunch) {
+    CompactLayersArgs g{};
+    g.base = c;
+    g.base.no_copy = 0;
+    g.nl = std::min(kLayersPerLaunch, nl - l0);
+    g.write_len = l0 + g.nl == nl;              // the last launch sets len_out
+    g.cnt = cnt + 2 * B + p->M;
+    for (int i = 0; i < g.nl; ++i) {
+      g.kc[i] = layers[l0 + i].k;
+      g.vc[i] = layers[l0 + i].v;
+      g.tk[i] = tk_of(l0 + i);
+      g.tv[i] = tv_of(l0 + i);
+    }
+    LAUNCH(p, KN_COMPACT, st, launch_kv_compact_layers(g, st));
   }
   return MEDUSA_OK;
+}
+
+}  // namespace
+
+medusa_status medusa_step(const medusa_plan* p, const float* h, const int32_t* root_in,
+                          const medusa_weights* w, const medusa_kv* kv, medusa_accept acc,
+                          const medusa_outputs* out, void* ws, size_t ws_bytes, void* stream) {
+  EntryScope scope("medusa_step");
+  if (!p || !h || !out) return MEDUSA_ERR_INVALID;
+  if (!out->out_tok || !out->n_acc || !out->h_next || !out->root_next) return MEDUSA_ERR_INVALID;
+  medusa_status s = check_weights(p, w, true, true, true);
+  if (s != MEDUSA_OK) return s;
+  if ((s = check_kv(p, kv, true)) != MEDUSA_OK) return s;
+  if ((s = check_accept(acc)) != MEDUSA_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MEDUSA_OK) return s;
+  const medusa_layer one{w->wq, w->wk, w->wv, w->wo, kv->k, kv->v};
+  return step_core(p, h, root_in, w, &one, 1, kv, acc, out, ws, S(stream));
+}
+
+size_t medusa_workspace_size_layers(const medusa_plan* p, int n_layers) {
+  if (!p || n_layers < 1 || n_layers > MEDUSA_MAX_LAYERS) return 0;
+  return layers_ws_bytes(p, n_layers);
+}
+
+medusa_status medusa_step_layers(const medusa_plan* p, const float* h, const int32_t* root_in,
+                                 const medusa_weights* w, const medusa_layer* layers, int n_layers,
+                                 const medusa_kv* kv, medusa_accept acc, const medusa_outputs* out,
+                                 void* ws, size_t ws_bytes, void* stream) {
+  EntryScope scope("medusa_step_layers");
+  if (!p || !h || !out || !layers || n_layers < 1 || n_layers > MEDUSA_MAX_LAYERS) return MEDUSA_ERR_INVALID;
+  if (!out->out_tok || !out->n_acc || !out->h_next || !out->root_next) return MEDUSA_ERR_INVALID;
+  medusa_status s = check_weights(p, w, true, false, true);
+  if (s != MEDUSA_OK) return s;
+  if (!w->emb || !aligned16(w->emb)) return MEDUSA_ERR_INVALID;
+  for (int l = 0; l < n_layers; ++l) {
+    const medusa_layer& L = layers[l];
+    if (!L.wq || !L.wk || !L.wv || !L.wo || !L.k || !L.v) return MEDUSA_ERR_INVALID;
+    if (!aligned16(L.wq) || !aligned16(L.wk) || !aligned16(L.wv) || !aligned16(L.wo)) return MEDUSA_ERR_INVALID;
+  }
+  if (!kv || !kv->len || !kv->len_out) return MEDUSA_ERR_INVALID;
+  if (p->d.page_size > 0 && !kv->page_table) return MEDUSA_ERR_INVALID;
+  if ((s = check_accept(acc)) != MEDUSA_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MEDUSA_OK) return s;
+  if (ws_bytes < layers_ws_bytes(p, n_layers)) return MEDUSA_ERR_WORKSPACE;
+  return step_core(p, h, root_in, w, layers, n_layers, kv, acc, out, ws, S(stream));
 }
 
 // ------------------------------------------------------------------ decode loop

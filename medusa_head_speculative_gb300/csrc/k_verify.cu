@@ -404,9 +404,11 @@ cudaError_t launch_verify_accept(const VerifyArgs& a, cudaStream_t st) {
 }
 
 // One CTA per sequence: slot len + l <- tree node path_nodes[l], l < n_acc, in 16-byte
-// pieces spread over all threads.
+// pieces spread over all threads, for the cache (kc, vc) and tree K/V (tk, tv) given.
+// Returns the new length in thread 0 (len_out is written by the caller).
 template <typename T>
-__device__ void compact_seq(const CompactArgs& a, int b) {
+__device__ int compact_copy(const CompactArgs& a, int b, void* kcache, void* vcache, const void* tkeys,
+                            const void* tvals) {
   __shared__ int s_len, s_n;
   __shared__ long s_dst[MEDUSA_MAX_HEADS + 1], s_src[MEDUSA_MAX_HEADS + 1];
   const long row = (long)a.Hkv * a.dh;                // elements per cached token
@@ -445,10 +447,10 @@ __device__ void compact_seq(const CompactArgs& a, int b) {
   __syncthreads();
   const int n = s_n;
   const int per = (int)(row * sizeof(T) / 16);         // 16-byte pieces per token row
-  uint4* kc = reinterpret_cast<uint4*>(a.kc);
-  uint4* vc = reinterpret_cast<uint4*>(a.vc);
-  const uint4* tk = reinterpret_cast<const uint4*>(a.tk);
-  const uint4* tv = reinterpret_cast<const uint4*>(a.tv);
+  uint4* kc = reinterpret_cast<uint4*>(kcache);
+  uint4* vc = reinterpret_cast<uint4*>(vcache);
+  const uint4* tk = reinterpret_cast<const uint4*>(tkeys);
+  const uint4* tv = reinterpret_cast<const uint4*>(tvals);
   constexpr int EPV = 16 / sizeof(T);                   // elements per piece
   constexpr int BATCH = 4;                              // loads in flight before the stores
   const int total = n * per, step = blockDim.x;
@@ -477,7 +479,42 @@ __device__ void compact_seq(const CompactArgs& a, int b) {
       }
   }
   __syncthreads();
-  if (threadIdx.x == 0) a.len_out[b] = s_len + n;
+  return s_len + n;
+}
+
+template <typename T>
+__device__ void compact_seq(const CompactArgs& a, int b) {
+  if (a.no_copy) return;
+  const int len = compact_copy<T>(a, b, a.kc, a.vc, a.tk, a.tv);
+  if (threadIdx.x == 0) a.len_out[b] = len;
+}
+
+// Multi-layer compaction: block (b, l) handles layer l of sequence b; the lengths before
+// the step are read by every block before the last one of the sequence (atomic counter)
+// writes len_out, so len_out may alias len.
+template <typename T>
+__global__ void __launch_bounds__(256) kv_compact_layers_kernel(const __grid_constant__ CompactLayersArgs a) {
+  __shared__ int s_last;
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x, l = blockIdx.y;
+  const int len = compact_copy<T>(a.base, b, a.kc[l], a.vc[l], a.tk[l], a.tv[l]);
+  if (!a.write_len) return;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(a.cnt + b, 1) == a.nl - 1;
+    if (s_last) {
+      a.base.len_out[b] = len;
+      a.cnt[b] = 0;
+    }
+  }
+}
+
+cudaError_t launch_kv_compact_layers(const CompactLayersArgs& a, cudaStream_t st) {
+  if (a.nl < 1 || a.nl > kLayersPerLaunch) return cudaErrorInvalidValue;
+  const dim3 grid(a.base.B, a.nl);
+  if (a.base.dtype == 0) return launch_kernel(kv_compact_layers_kernel<float>, grid, dim3(256), 0, st, 1, a);
+  return launch_kernel(kv_compact_layers_kernel<bf16>, grid, dim3(256), 0, st, 1, a);
 }
 
 template <typename T>

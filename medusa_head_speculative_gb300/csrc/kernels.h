@@ -167,8 +167,24 @@ struct CompactArgs {
   const int32_t* path_nodes; const int32_t* n_acc;
   int B, n1, Hkv, dh, K, dtype;
   uint32_t* status;
+  int no_copy;              // fused commit: acceptance only (a multi-layer step compacts after)
 };
 cudaError_t launch_kv_compact(const CompactArgs& a, cudaStream_t st);
+// Compaction of up to kLayersPerLaunch backbone layers: grid (B, nl), block (b, l) copies
+// sequence b's kept nodes from layer l's tree K/V into layer l's cache (base.len: the
+// lengths before the step).  With write_len, the last block of a sequence (counter cnt[b],
+// zero on entry, left zero) writes base.len_out[b], so len_out may alias len.
+constexpr int kLayersPerLaunch = 16;
+struct CompactLayersArgs {
+  CompactArgs base;
+  int nl, write_len;
+  int32_t* cnt;
+  void* kc[kLayersPerLaunch];
+  void* vc[kLayersPerLaunch];
+  const void* tk[kLayersPerLaunch];
+  const void* tv[kLayersPerLaunch];
+};
+cudaError_t launch_kv_compact_layers(const CompactLayersArgs& a, cudaStream_t st);
 // Fused per-row statistics + acceptance + KV compaction.  row_cnt [B*n1] and seq_cnt [B]
 // zero on entry (left zero); parts: [B*n1][4][6] float scratch.
 cudaError_t launch_verify_commit(const VerifyArgs& v, const CompactArgs& c, int32_t* row_cnt,
