@@ -44,7 +44,7 @@ Readings where the pages are silent or disagree (each also listed in the design 
       weight exceeds u_final times the remaining total); it is the next step's root.
       p = softmax(z / T); T = 0 is greedy.  Uniforms are inputs: uniforms[0] for the
       draw, uniforms[1 + (d - 1) * 16 + j] for the j-th child tried at depth d.
-  R9  A backbone of n synthetic layers (the multi-layer form of R0 for a real backbone's
+  R14 A backbone of n synthetic layers (the multi-layer form of R0 for a real backbone's
       per-layer calls): x_0 = E[tok]; layer l takes q, k, v from x_l with its own
       projections (RoPE at the node position), attends over its own prefix cache plus
       its own tree keys under the same mask, and x_{l+1} = x_l + Wo_l o_l; h' = x_n.
@@ -632,9 +632,9 @@ def medusa_generate(wts, h, kc, vc, spec, dims, accept, n_steps):
     return tokens, steps, kc, vc
 
 
-# ============================================================ multi-layer backbone (R9)
+# ============================================================ multi-layer backbone (R14)
 def medusa_step_layers(wts, layers, h, caches, spec, dims, accept, root=None, s=None):
-    """One decode step of one sequence through an n-layer backbone (R9).
+    """One decode step of one sequence through an n-layer backbone (R14).
 
     layers: per layer a dict with wq, wk, wv, wo (layer 0's may be wts itself); caches:
     per layer (kc, vc) post-RoPE prefix keys/values [L][Hkv][dh] (the same L in every

@@ -1,4 +1,4 @@
-"""The multi-layer backbone (medusa_step_layers) against the oracle's n-layer step (R9):
+"""The multi-layer backbone (medusa_step_layers) against the oracle's n-layer step (R14):
 accepted tokens, path, next root and hidden state, and every layer's compacted cache; one
 layer equals medusa_step bit for bit; on the planted tiny model a multi-step loop through
 several layers emits the plain greedy continuation."""

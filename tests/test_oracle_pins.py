@@ -441,7 +441,7 @@ def test_rejection_walk_at_low_temperature_is_the_greedy_walk():
         assert v == am[path[-1]]
 
 
-# ---------------------------------------------------------------- multi-layer backbone (R9)
+# ---------------------------------------------------------------- multi-layer backbone (R14)
 def _layers_setup(planted, n_layers):
     w, ow, h, k, v, dims = _tiny_setup(planted)
     layers = [ow] + [O.oracle_weights(S.layer_weights(w, l, planted=planted))
@@ -451,7 +451,7 @@ def _layers_setup(planted, n_layers):
 
 
 def test_one_layer_backbone_is_the_single_layer_step():
-    """R9 with one layer is R0: the same tokens, layer outputs, logits and path."""
+    """R14 with one layer is R0: the same tokens, layer outputs, logits and path."""
     w, ow, h, layers, caches, dims = _layers_setup(True, 1)
     h = torch.from_numpy(ow["emb"][7].astype(np.float32))
     spec = O.cartesian_tree(w.s)
