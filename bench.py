@@ -182,6 +182,67 @@ def steady_state(args, w: S.Workload, st, stream, barrier):
                     "once per step; prefix length held fixed"}
 
 
+def layers_bytes(w: S.Workload, n1: int, n_layers: int):
+    """step_bytes through an n-layer backbone: every further layer adds its projections,
+    its KV prefix, its tree K/V written and read, and the node activations."""
+    es = 4 if w.dtype == "f32" else 2
+    qd, kd = w.Hq * w.dh, w.Hkv * w.dh
+    per = ((qd + 2 * kd + qd) * w.d * es + w.B * n1 * w.d * es
+           + sum(w.lengths) * 2 * kd * es + w.B * n1 * 2 * kd * es * 2)
+    return step_bytes(w, n1) + (n_layers - 1) * per
+
+
+def multi_layer(args, w: S.Workload, st, device, stream, barrier):
+    """medusa_step_layers through args.layers backbone layers (layer 0 = the workload's
+    projections and cache, further layers seeded on their own), prefix held fixed, as a
+    CUDA graph replayed back to back."""
+    from medusa_head_speculative_gb300 import binding as Bnd
+    n = args.layers
+    plan = st["plan"]
+    layers = [dict(wq=st["wts"]["wq"], wk=st["wts"]["wk"], wv=st["wts"]["wv"], wo=st["wts"]["wo"],
+                   k=st["kc"], v=st["vc"])]
+    for l in range(1, n):
+        lw = S.layer_weights(w, l)
+        kc, vc, _ = S.kv_cache(w, l)
+        layers.append(dict(**{k: t.to(device) for k, t in lw.items()}, k=kc.to(device), v=vc.to(device)))
+    arr = Bnd.layers_array(layers)
+    ws = torch.empty(plan.workspace_size_layers(n), dtype=torch.uint8, device=device)
+    kv = Bnd.kv_struct(None, None, st["length"], st["len_out"], st["pt"])
+
+    def one():
+        Bnd.step_layers(plan, st["h"], None, st["wstruct"], arr, kv, st["acc"], st["outs"], ws)
+
+    for _ in range(3):
+        one()
+    run, mode = one, "direct"
+    if not args.no_graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                one()
+            g.replay()
+            run, mode = g.replay, "cuda_graph"
+        except Exception as exc:                        # noqa: BLE001
+            mode = f"direct (graph capture failed: {exc})"[:160]
+    reps = max(1, min(args.steps, 1000))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(reps):
+        run()
+    e1.record(stream)
+    barrier()
+    ms = e0.elapsed_time(e1) / reps
+    assert plan.status() == 0, "device status word set during the multi-layer region"
+    sb = layers_bytes(w, plan.n1, n)
+    hbm, _ = peaks()
+    return {"value": round(1e3 / ms, 2), "unit": "steps/s", "n_layers": n, "ms_per_step": round(ms, 5),
+            "steps": reps, "launch": mode, "step_bytes": sb,
+            "step_hbm_frac": round(sb / (ms * 1e-3) / 1e9 / hbm, 4),
+            "note": "medusa_step_layers: every layer's projections, KV prefix and compaction; "
+                    "prefix length held fixed"}
+
+
 def decode_loop(args, w: S.Workload, st, device):
     """The library's decode loop (medusa_loop_*): one captured step with root, h and the
     cache lengths carried in place, replayed back to back from the workload's prefix while
@@ -410,6 +471,7 @@ def run_ours(args, w: S.Workload):
     n_acc_mean = float(st["out"]["n_acc"].float().mean())
     steady = steady_state(args, w, st, stream, barrier)
     loop = decode_loop(args, w, st, device)
+    mlayer = multi_layer(args, w, st, device, stream, barrier) if args.layers > 1 else None
 
     # end to end: h_t from pinned host memory, result (tokens, counts) back, every step
     ke = min(K, 500)
@@ -502,6 +564,7 @@ def run_ours(args, w: S.Workload):
             steady_bytes(w, n1) / (steady["ms_per_step"] * 1e-3) / 1e9 / hbm, 4),
             step_bytes=steady_bytes(w, n1)),
         "decode_loop": loop,
+        "multi_layer": mlayer,
         "gpu_launches": int(launches),
         "launch": launch_mode,
     }
@@ -712,6 +775,8 @@ def main():
     ap.add_argument("--workload", default="vicuna7b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct calls, not a CUDA graph")
+    ap.add_argument("--layers", type=int, default=4,
+                    help="backbone layers of the multi_layer measurement (1: skip it)")
     ap.add_argument("--planted", action="store_true",
                     help="planted weights whose heads are often right (long accepted paths)")
     ap.add_argument("--sweep", action="store_true",
