@@ -358,6 +358,31 @@ int medusa_tree_cartesian(int K, const int* s, int max_nodes, int32_t* parent, i
 int medusa_tree_greedy(int K, const int* s, int smax, const double* a, int N, int32_t* parent,
                        int32_t* rank);
 
+/* ---- optimized tree on the device, and the tree size
+ * The same construction as medusa_tree_greedy, on the GPU from a device table: one CTA
+ * repeatedly takes the frontier node with the largest path product (formed root to leaf in
+ * double precision, as the host builder forms it; ties to the smaller rank path) and adds
+ * its children to the frontier, then packs the N chosen nodes canonically.
+ *   a:        device [K][smax] doubles, a[k*smax + i] = head k+1's marginal accuracy at
+ *             rank i (values in [0, 1]); s: host [K], 1 <= s[k] <= smax <= MEDUSA_MAX_TOPS
+ *   N:        candidates, 1 <= N <= MEDUSA_MAX_NODES - 1 and at most the Cartesian tree's size
+ *   parent, rank: device [N+1] outputs in canonical packing (parent[0] = -1, rank[0] = 0)
+ *   expected: device [N+1] output or NULL: expected[n] = the expected number of accepted
+ *             candidates of the tree of the first n nodes added (sum of their path
+ *             products), so one call gives the curve for every size up to N
+ * Asynchronous on `stream`.  MEDUSA_ERR_INVALID on a bad size or NULL pointer. */
+medusa_status medusa_tree_greedy_device(int K, const int* s, int smax, const double* a, int N,
+                                        int32_t* parent, int32_t* rank, double* expected,
+                                        void* stream);
+/* Tree size for the current batch and context ([MEDUSA] §6 Limitations and Trade-offs: the
+ * best tree size depends on the context length; "Follow-Up Research": dynamic candidate
+ * counts for batched inference): among n candidate sizes with measured (or modelled) step
+ * times step_ms[i], the index maximising the expected tokens per unit time
+ * (1 + expected[sizes[i]]) / step_ms[i], ties to the smaller size.  expected: host
+ * [max_n + 1] as from medusa_tree_greedy_device.  Returns the index or a negative status. */
+int medusa_tree_size_choose(const double* expected, int max_n, const int* sizes,
+                            const double* step_ms, int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -107,6 +107,9 @@ def lib():
                                       C.POINTER(C.c_int32)]),
         "medusa_tree_greedy": (I, [I, C.POINTER(C.c_int), I, C.POINTER(C.c_double), I,
                                    C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
+        "medusa_tree_greedy_device": (I, [I, C.POINTER(C.c_int), I, P, I, P, P, P, P]),
+        "medusa_tree_size_choose": (I, [C.POINTER(C.c_double), I, C.POINTER(C.c_int),
+                                        C.POINTER(C.c_double), I]),
         "medusa_loop_create": (I, [P, C.POINTER(Weights), C.POINTER(KV), Accept, P, P, P, P, I, P,
                                    SZ, C.POINTER(P)]),
         "medusa_loop_run": (I, [P, I, P]),
@@ -161,6 +164,28 @@ def tree_greedy(s, a, N):
     if n1 < 0:
         raise MedusaError("medusa_tree_greedy", n1)
     return np.array(parent[:n1], dtype=np.int32), np.array(rank[:n1], dtype=np.int32)
+
+
+def tree_greedy_device(s, a_dev, N, parent, rank, expected=None, stream=None):
+    """medusa_tree_greedy_device: a_dev a [K][smax] float64 CUDA tensor; parent, rank int32
+    CUDA tensors of N+1 entries, expected float64 (N+1) or None."""
+    K, smax = a_dev.shape
+    sa = (C.c_int * K)(*s)
+    _check("medusa_tree_greedy_device",
+           lib().medusa_tree_greedy_device(K, sa, smax, ptr(a_dev), N, ptr(parent), ptr(rank),
+                                           ptr(expected), _stream(stream)))
+
+
+def tree_size_choose(expected, sizes, step_ms):
+    """medusa_tree_size_choose: index into sizes of the best expected tokens per time."""
+    e = np.ascontiguousarray(expected, dtype=np.float64)
+    sz = (C.c_int * len(sizes))(*sizes)
+    ms = np.ascontiguousarray(step_ms, dtype=np.float64)
+    i = lib().medusa_tree_size_choose(e.ctypes.data_as(C.POINTER(C.c_double)), len(e) - 1, sz,
+                                      ms.ctypes.data_as(C.POINTER(C.c_double)), len(sizes))
+    if i < 0:
+        raise MedusaError("medusa_tree_size_choose", i)
+    return i
 
 
 # ------------------------------------------------------------------ plan

@@ -1189,3 +1189,31 @@ medusa_status medusa_loop_steps(const medusa_loop* L, void* stream, long long* s
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ optimized tree on the device
+extern "C" medusa_status medusa_tree_greedy_device(int K, const int* s, int smax, const double* a, int N,
+                                                   int32_t* parent, int32_t* rank, double* expected,
+                                                   void* stream) {
+  EntryScope scope("medusa_tree_greedy_device");
+  if (K < 1 || K > MEDUSA_MAX_HEADS || !s || !a || !parent || !rank) return MEDUSA_ERR_INVALID;
+  if (smax < 1 || smax > MEDUSA_MAX_TOPS || N < 1 || N > MEDUSA_MAX_NODES - 1) return MEDUSA_ERR_INVALID;
+  long cart = 0, level = 1;                      // nodes of the Cartesian tree (root excluded)
+  for (int k = 0; k < K; ++k) {
+    if (s[k] < 1 || s[k] > smax) return MEDUSA_ERR_INVALID;
+    level = std::min<long>(level * s[k], 1L << 20);
+    cart += level;
+  }
+  if (cart < N) return MEDUSA_ERR_INVALID;
+  medusa::TreeGreedyArgs g{};
+  g.acc = a;
+  g.K = K;
+  g.smax = smax;
+  g.N = N;
+  g.fmax = N * smax + smax;
+  for (int k = 0; k < K; ++k) g.s[k] = s[k];
+  g.parent = parent;
+  g.rank = rank;
+  g.expected = expected;
+  if (medusa::launch_tree_greedy(g, S(stream)) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  return MEDUSA_OK;
+}

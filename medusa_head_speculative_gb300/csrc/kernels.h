@@ -185,6 +185,20 @@ struct CompactLayersArgs {
   const void* tv[kLayersPerLaunch];
 };
 cudaError_t launch_kv_compact_layers(const CompactLayersArgs& a, cudaStream_t st);
+
+// ---- optimized tree on the device (one CTA): acc [K][smax] doubles; fmax = N*smax + smax
+// frontier entries; parent / rank [N+1] in canonical packing; expected [N+1] (optional):
+// expected[n] = sum of the path products of the first n nodes added.
+struct TreeGreedyArgs {
+  const double* acc;
+  int K, smax, N, fmax;
+  int s[MEDUSA_MAX_HEADS];
+  int32_t* parent;
+  int32_t* rank;
+  double* expected;
+};
+size_t tree_greedy_smem(int N, int smax);
+cudaError_t launch_tree_greedy(const TreeGreedyArgs& a, cudaStream_t st);
 // Fused per-row statistics + acceptance + KV compaction.  row_cnt [B*n1] and seq_cnt [B]
 // zero on entry (left zero); parts: [B*n1][4][6] float scratch.
 cudaError_t launch_verify_commit(const VerifyArgs& v, const CompactArgs& c, int32_t* row_cnt,

@@ -99,3 +99,19 @@ extern "C" int medusa_tree_greedy(int K, const int* s, int smax, const double* a
   }
   return pack(chosen, N + 1, parent, rank);
 }
+
+extern "C" int medusa_tree_size_choose(const double* expected, int max_n, const int* sizes,
+                                       const double* step_ms, int n) {
+  if (!expected || !sizes || !step_ms || n < 1 || max_n < 0) return MEDUSA_ERR_INVALID;
+  int best = -1;
+  double best_rate = 0.0;
+  for (int i = 0; i < n; ++i) {
+    if (sizes[i] < 0 || sizes[i] > max_n || !(step_ms[i] > 0.0)) return MEDUSA_ERR_INVALID;
+    const double rate = (1.0 + expected[sizes[i]]) / step_ms[i];     // tokens per ms
+    if (best < 0 || rate > best_rate || (rate == best_rate && sizes[i] < sizes[best])) {
+      best = i;
+      best_rate = rate;
+    }
+  }
+  return best;
+}
