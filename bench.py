@@ -243,6 +243,66 @@ def multi_layer(args, w: S.Workload, st, device, stream, barrier):
                     "prefix length held fixed"}
 
 
+def tree_size(args, w: S.Workload, st, device, stream):
+    """The tree size for this batch and context: trees of several sizes from the score table,
+    built on the device (medusa_tree_greedy_device), each timed as a whole step (CUDA graph,
+    prefix held fixed), and the size with the most expected tokens per unit time chosen
+    (medusa_tree_size_choose) from the table's expected accepted length."""
+    from medusa_head_speculative_gb300 import binding as Bnd
+    sizes = [16, 32, 64, 128]
+    smax = max(w.s)
+    a = torch.from_numpy(S.score_table(w.K, smax)).to(device)
+    nmax = max(sizes)
+    par = torch.empty(nmax + 1, dtype=torch.int32, device=device)
+    rnk = torch.empty_like(par)
+    exp = torch.empty(nmax + 1, dtype=torch.float64, device=device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    Bnd.tree_greedy_device(list(w.s), a, nmax, par, rnk, exp)      # warm-up
+    e0.record(stream)
+    Bnd.tree_greedy_device(list(w.s), a, nmax, par, rnk, exp)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    build_us = e0.elapsed_time(e1) * 1e3
+    expected = exp.cpu().numpy()
+    dtype = Bnd.F32 if w.dtype == "f32" else Bnd.BF16
+    ms_sizes = []
+    for N in sizes:
+        Bnd.tree_greedy_device(list(w.s), a, N, par, rnk)
+        parent = par[:N + 1].cpu().numpy().astype(np.int32)
+        rank = rnk[:N + 1].cpu().numpy().astype(np.int32)
+        plan = Bnd.Plan(w.B, w.d, w.V, w.K, w.Hq, w.Hkv, w.dh, dtype, w.capacity, w.s, parent, rank,
+                        rope_base=w.rope_base, page_size=w.page_size,
+                        num_pages=w.B * w.pages_per_seq if w.page_size else 0)
+        ws = torch.empty(plan.workspace_size, dtype=torch.uint8, device=device)
+
+        def one():
+            Bnd.step(plan, st["h"], None, st["wstruct"], st["kv"], st["acc"], st["outs"], ws)
+
+        for _ in range(3):
+            one()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            one()
+        reps = max(1, min(args.steps, 200))
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert plan.status() == 0, "device status word set during the tree-size region"
+        ms_sizes.append(e0.elapsed_time(e1) / reps)
+        del g, ws
+        plan.close()
+    best = Bnd.tree_size_choose(expected, sizes, ms_sizes)
+    return {"sizes": sizes, "ms_per_step": [round(x, 5) for x in ms_sizes],
+            "expected_accepted": [round(float(expected[n]), 4) for n in sizes],
+            "expected_tokens_per_s": [round(w.B * (1 + float(expected[n])) / (m * 1e-3), 1)
+                                      for n, m in zip(sizes, ms_sizes)],
+            "chosen": sizes[best], "builder_us": round(build_us, 1),
+            "note": "trees built on the device from the fixed score table; expected tokens "
+                    "per step = 1 + E[L] of the table (trained heads' accuracies would replace it)"}
+
+
 def decode_loop(args, w: S.Workload, st, device):
     """The library's decode loop (medusa_loop_*): one captured step with root, h and the
     cache lengths carried in place, replayed back to back from the workload's prefix while
@@ -472,6 +532,7 @@ def run_ours(args, w: S.Workload):
     steady = steady_state(args, w, st, stream, barrier)
     loop = decode_loop(args, w, st, device)
     mlayer = multi_layer(args, w, st, device, stream, barrier) if args.layers > 1 else None
+    tsize = tree_size(args, w, st, device, stream) if not args.no_tree_size else None
 
     # end to end: h_t from pinned host memory, result (tokens, counts) back, every step
     ke = min(K, 500)
@@ -565,6 +626,7 @@ def run_ours(args, w: S.Workload):
             step_bytes=steady_bytes(w, n1)),
         "decode_loop": loop,
         "multi_layer": mlayer,
+        "tree_size": tsize,
         "gpu_launches": int(launches),
         "launch": launch_mode,
     }
@@ -775,6 +837,7 @@ def main():
     ap.add_argument("--workload", default="vicuna7b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct calls, not a CUDA graph")
+    ap.add_argument("--no-tree-size", action="store_true", help="skip the tree-size measurement")
     ap.add_argument("--layers", type=int, default=4,
                     help="backbone layers of the multi_layer measurement (1: skip it)")
     ap.add_argument("--planted", action="store_true",
