@@ -151,10 +151,13 @@ __global__ void __launch_bounds__(256) tree_attn_kernel(AttnArgs a) {
 
 // One warp per (sequence, kv head, query row): o = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s
 // over the prefix splits and the tree split, M = max_s m_s.  Lane j holds the VPL
-// consecutive columns [j*VPL, (j+1)*VPL) of the head (dh = 32 * VPL); the splits' (m, l)
-// pairs are read once per lane and reduced across the warp.
+// consecutive columns [j*VPL, (j+1)*VPL) of the head (dh = 32 * VPL).  Splits go in batches
+// of 8: every lane loads the batch's (m, l) pairs (the same addresses across the warp) and
+// its columns of the batch's outputs in one round trip, and the running maximum moves
+// once per batch (the sums are rescaled when it rises).
 template <int VPL>
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
+  constexpr int SB = 8;
   pdl_trigger();
   pdl_wait();
   const int R = a.n1 * a.G, S = a.nsplit + 1;
@@ -165,32 +168,50 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
   const long bg = wg / R;                            // b * Hkv + g
   const int g = (int)(bg % a.Hkv), b = (int)(bg / a.Hkv);
   const long base = bg * S * R + r;                  // partial row of split s: base + s * R
-  float M = -INFINITY;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, a.part_ml[(base + (long)s * R) * 2]);
-  M = warp_max(M);
-  float Lsum = 0.f;
-  for (int s = lane; s < S; s += 32) {
-    const float m = a.part_ml[(base + (long)s * R) * 2];
-    if (m != -INFINITY) Lsum += __expf(m - M) * a.part_ml[(base + (long)s * R) * 2 + 1];
-  }
-  Lsum = warp_sum(Lsum);
+  float M = -INFINITY, Lsum = 0.f;
   float acc[VPL];
 #pragma unroll
   for (int c = 0; c < VPL; ++c) acc[c] = 0.f;
-#pragma unroll 4
-  for (int s = 0; s < S; ++s) {
-    const float m = a.part_ml[(base + (long)s * R) * 2];
-    const float w = m == -INFINITY ? 0.f : __expf(m - M);
-    const float* src = a.part_o + (base + (long)s * R) * a.dh + lane * VPL;
-    if (VPL == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src);
-      acc[0] += w * v.x; acc[VPL > 1 ? 1 : 0] += w * v.y;
-      acc[VPL > 2 ? 2 : 0] += w * v.z; acc[VPL > 3 ? 3 : 0] += w * v.w;
-    } else if (VPL == 2) {
-      const float2 v = *reinterpret_cast<const float2*>(src);
-      acc[0] += w * v.x; acc[VPL > 1 ? 1 : 0] += w * v.y;
-    } else {
-      acc[0] += w * src[0];
+  for (int s0 = 0; s0 < S; s0 += SB) {
+    float m[SB], l[SB], v[SB][VPL];
+#pragma unroll
+    for (int u = 0; u < SB; ++u) {
+      m[u] = -INFINITY;
+      l[u] = 0.f;
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) v[u][c] = 0.f;
+      if (s0 + u < S) {
+        const long pr = base + (long)(s0 + u) * R;
+        const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + pr * 2);
+        m[u] = ml.x;
+        l[u] = ml.y;
+        const float* src = a.part_o + pr * a.dh + lane * VPL;
+        if (VPL == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(src);
+          v[u][0] = t.x; v[u][VPL > 1 ? 1 : 0] = t.y; v[u][VPL > 2 ? 2 : 0] = t.z; v[u][VPL > 3 ? 3 : 0] = t.w;
+        } else if (VPL == 2) {
+          const float2 t = *reinterpret_cast<const float2*>(src);
+          v[u][0] = t.x; v[u][VPL > 1 ? 1 : 0] = t.y;
+        } else {
+          v[u][0] = src[0];
+        }
+      }
+    }
+    float mb = M;
+#pragma unroll
+    for (int u = 0; u < SB; ++u) mb = fmaxf(mb, m[u]);
+    if (mb == -INFINITY) continue;                   // no keys in any split so far
+    const float scale = M == -INFINITY ? 0.f : __expf(M - mb);
+    Lsum *= scale;
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) acc[c] *= scale;
+    M = mb;
+#pragma unroll
+    for (int u = 0; u < SB; ++u) {
+      const float w = m[u] == -INFINITY ? 0.f : __expf(m[u] - M);
+      Lsum += w * l[u];
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) acc[c] += w * v[u][c];
     }
   }
   const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
