@@ -57,9 +57,11 @@ struct AttnTcArgs {
 // done (BOF), P written (BPR).  One P-written barrier per P buffer: the softmax warps can
 // finish chunk i + 1 before the MMA thread has waited for chunk i, but never chunk i + 2
 // (that needs the P V of chunk i), so no barrier runs two phases ahead of its waiter.
+// With 128-key chunks (one tile) each row's keys are split over two softmax warps; BMX
+// (two, by chunk parity) collects the 256 half-row maxima before either half forms P.
 enum {
   BQ = 0, BKVF = 1, BKVE = BKVF + AT_STAGES, BSF = BKVE + AT_STAGES,
-  BOF = BSF + 2 * AT_TILES, BPR = BOF + 2 * AT_TILES, BCOUNT = BPR + 2 * AT_TILES
+  BOF = BSF + 2 * AT_TILES, BPR = BOF + 2 * AT_TILES, BMX = BPR + 2 * AT_TILES, BCOUNT = BMX + 2
 };
 
 // A bounded wait whose outcome is the same in every lane (the TMEM accesses that follow
@@ -114,8 +116,10 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
     for (int i = 0; i < 2 * AT_TILES; ++i) {
       mbar_init(bar(BSF + i), 1);
       mbar_init(bar(BOF + i), 1);
-      mbar_init(bar(BPR + i), AT_ROWS);
+      mbar_init(bar(BPR + i), KEYS == 128 ? 2 * AT_ROWS : AT_ROWS);   // every softmax thread
     }
+    mbar_init(bar(BMX), 2 * AT_ROWS);
+    mbar_init(bar(BMX + 1), 2 * AT_ROWS);
     s_issued = 0;
     s_waited = 0;
     s_qok = 0;
@@ -270,7 +274,180 @@ tree_attn_tc_kernel(const __grid_constant__ AttnTcArgs g) {
       }
       s_waited = waited;
     }
-  } else if (warp < 4 * nta) {
+  } else if (KEYS == 128 && warp < 8) {
+    // ------------------------------------------------------------ softmax, split rows
+    // One tile: warps q and q + 4 share TMEM lanes 32q.. (row r); warp hf = warp / 4 takes
+    // keys [64 hf, 64 hf + 64) of every chunk, writes that 64-key atom of P, rescales and
+    // reads back O's columns [hf DH/2, (hf + 1) DH/2).  Per chunk the two halves swap their
+    // maxima through spare TMEM columns of their row's lane (BMX orders the store before the
+    // partner's load), so both form P against the same m_use.
+    const int q = warp & 3, hf = warp >> 2;
+    const int r = q * 32 + lane;
+    const int gr = row0 + r;
+    const int node = gr / G;
+    const bool row_ok = gr < R;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t xcol = lane_base + OCOL + DH;    // [parity][half] maxima, then the sum
+    uint8_t* pgen = smem_raw + (ps - sraw) + (size_t)hf * PA;
+    const float sl2 = a.scale * 1.4426950408889634f;
+    float m_use = -INFINITY, l_acc = 0.f;
+    const bool live = row0 + q * 32 < R;
+    for (int i = 0; i < nch; ++i) {
+      const int bm = BMX + (i & 1);
+      const uint32_t pmx = (uint32_t)(i >> 1) & 1u;
+      if (!live) {                                  // keep pace and keep every barrier's count
+        if (i >= 2 && !warp_wait(bar(BOF + (i & 1)), ((i - 2) >> 1) & 1)) { timed_out = true; break; }
+        tc_fence_before();
+        mbar_arrive(bar(bm));
+        if (!warp_wait(bar(bm), pmx)) { timed_out = true; break; }
+        mbar_arrive(bar(BPR + (i & 1)));
+        continue;
+      }
+      if (!warp_wait(bar(BSF + (i & 1)), (i >> 1) & 1)) { timed_out = true; break; }
+      tc_fence_after();
+      float s[64];
+      tmem_ld64(lane_base + (uint32_t)(i & 1) * KEYS + 64 * hf, s);
+      const int t0 = kbeg + i * KEYS + 64 * hf;     // this half's first key
+      const bool full = !tree && t0 + 64 <= kend;
+      float mx;
+      if (full) {
+        float q0 = s[0], q1 = s[1], q2 = s[2], q3 = s[3];
+#pragma unroll
+        for (int j = 4; j < 64; j += 4) {
+          q0 = fmaxf(q0, s[j]);
+          q1 = fmaxf(q1, s[j + 1]);
+          q2 = fmaxf(q2, s[j + 2]);
+          q3 = fmaxf(q3, s[j + 3]);
+        }
+        mx = fmaxf(fmaxf(q0, q1), fmaxf(q2, q3)) * sl2;
+      } else {
+        uint32_t w[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int wi = (t0 >> 5) + u;
+          w[u] = !tree ? 0xffffffffu
+                       : (row_ok && wi < kMaskWords ? a.mask[(long)node * kMaskWords + wi] : 0u);
+        }
+        mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const bool bit = (w[j >> 5] >> (j & 31)) & 1u;
+          const bool valid = (t0 + j < kend) && bit;
+          s[j] = valid ? s[j] * sl2 : -INFINITY;
+          mx = fmaxf(mx, s[j]);
+        }
+      }
+      tmem_st1(xcol + 2 * (i & 1) + hf, mx);       // swap half-row maxima
+      tc_fence_before();
+      mbar_arrive(bar(bm));
+      if (!warp_wait(bar(bm), pmx)) { timed_out = true; break; }
+      tc_fence_after();
+      mx = fmaxf(mx, tmem_ld1(xcol + 2 * (i & 1) + (hf ^ 1)));
+      // this chunk's P buffer was last read by the P V of chunk i - 2
+      if (i >= 2 && !warp_wait(bar(BOF + (i & 1)), ((i - 2) >> 1) & 1)) { timed_out = true; break; }
+      const bool raise = m_use != -INFINITY && mx > m_use + AT_LAZY;
+      if (__any_sync(0xffffffffu, raise)) {
+        if (!warp_wait(bar(BOF + ((i - 1) & 1)), ((i - 1) >> 1) & 1)) { timed_out = true; break; }
+        tc_fence_after();
+        const float f = raise ? ex2_approx(m_use - mx) : 1.f;
+#pragma unroll
+        for (int c = 0; c < DH / 2; c += 16) {
+          float v[16];
+          tmem_ld16(lane_base + OCOL + hf * (DH / 2) + c, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] *= f;
+          tmem_st16(lane_base + OCOL + hf * (DH / 2) + c, v);
+        }
+        if (raise) {
+          l_acc *= f;
+          m_use = mx;
+        }
+      }
+      if (m_use == -INFINITY) m_use = mx;
+      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+      if (full) {
+        const float nm = -m_use;
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+          s[j] = ex2_approx(fmaf(s[j], sl2, nm));
+          s[j + 1] = ex2_approx(fmaf(s[j + 1], sl2, nm));
+          s[j + 2] = ex2_approx(fmaf(s[j + 2], sl2, nm));
+          s[j + 3] = ex2_approx(fmaf(s[j + 3], sl2, nm));
+          l0 += s[j];
+          l1 += s[j + 1];
+          l2 += s[j + 2];
+          l3 += s[j + 3];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            s[j + e] = s[j + e] == -INFINITY ? 0.f : ex2_approx(s[j + e] - m_use);
+          l0 += s[j];
+          l1 += s[j + 1];
+          l2 += s[j + 2];
+          l3 += s[j + 3];
+        }
+      }
+      l_acc += (l0 + l1) + (l2 + l3);
+      uint8_t* prow = pgen + (size_t)(i & 1) * PT + r * 128;   // this half's 64-key atom
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 u;
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(s[8 * c + 0], s[8 * c + 1]);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(s[8 * c + 2], s[8 * c + 3]);
+        __nv_bfloat162 p2 = __floats2bfloat162_rn(s[8 * c + 4], s[8 * c + 5]);
+        __nv_bfloat162 p3 = __floats2bfloat162_rn(s[8 * c + 6], s[8 * c + 7]);
+        u.x = *reinterpret_cast<uint32_t*>(&p0);
+        u.y = *reinterpret_cast<uint32_t*>(&p1);
+        u.z = *reinterpret_cast<uint32_t*>(&p2);
+        u.w = *reinterpret_cast<uint32_t*>(&p3);
+        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = u;
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(bar(BPR + (i & 1)));
+    }
+    // the row's sum is the two halves' sums (the same m_use), exchanged through BMX once more
+    const int bm = BMX + (nch & 1);
+    float l_other = 0.f;
+    if (!timed_out) {
+      if (hf == 1) tmem_st1(xcol + 4, l_acc);
+      tc_fence_before();
+      mbar_arrive(bar(bm));
+      if (!warp_wait(bar(bm), (uint32_t)(nch >> 1) & 1u)) timed_out = true;
+      tc_fence_after();
+      if (!timed_out && hf == 0) l_other = tmem_ld1(xcol + 4);
+    }
+    float o[DH / 2];
+#pragma unroll
+    for (int c = 0; c < DH / 2; ++c) o[c] = 0.f;
+    if (!timed_out && nch > 0 && live) {
+      if (!warp_wait(bar(BOF + ((nch - 1) & 1)), ((nch - 1) >> 1) & 1)) {
+        timed_out = true;
+      } else {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < DH / 2; c += 16) {
+          float v[16];
+          tmem_ld16(lane_base + OCOL + hf * (DH / 2) + c, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[c + e] = v[e];
+        }
+      }
+    }
+    if (row_ok && !timed_out) {
+      const long pr = (((long)b * a.Hkv + gk) * (a.nsplit + 1) + split) * R + gr;
+      float4* dst = reinterpret_cast<float4*>(a.part_o + pr * DH + hf * (DH / 2));
+#pragma unroll
+      for (int c = 0; c < DH / 2; c += 4) dst[c / 4] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+      if (hf == 0) {
+        a.part_ml[pr * 2] = m_use * 0.6931471805599453f;     // back to natural-log units
+        a.part_ml[pr * 2 + 1] = l_acc + l_other;
+      }
+    }
+  } else if (KEYS == 64 && warp < 4 * nta) {
     // ------------------------------------------------------------ softmax rows
     const int t = warp >> 2, wl = warp & 3;
     const int r = wl * 32 + lane;                   // row within the tile = TMEM lane
@@ -479,11 +656,23 @@ cudaError_t launch_tree_attention_tc(const AttnArgs& a, const void* q_bf16, cuda
   if (a.rows_per_block != AT_ROWS && a.rows_per_block != AT_ROWS * AT_TILES) return cudaErrorInvalidValue;
   g.nt = a.rows_per_block / AT_ROWS;
   const int H = a.dh / 64;
-  // shared memory: Q tiles, two P buffers per tile, then as many K/V stages as fit (227 KB)
+  // shared memory: Q tiles, two P buffers per tile, then as many K/V stages as fit in the
+  // per-CTA maximum less the kernel's own static shared memory
+  int optin = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    optin = 227 * 1024;
+  auto kernel_for = [&](int keys) -> void (*)(AttnTcArgs) {
+    if (a.dh == 128) return keys == AT_KEYS1 ? tree_attn_tc_kernel<128, AT_KEYS1> : tree_attn_tc_kernel<128, AT_KEYS>;
+    return keys == AT_KEYS1 ? tree_attn_tc_kernel<64, AT_KEYS1> : tree_attn_tc_kernel<64, AT_KEYS>;
+  };
   auto plan = [&](int keys, size_t& smem) {
+    cudaFuncAttributes fa{};
+    const size_t stat = cudaFuncGetAttributes(&fa, kernel_for(keys)) == cudaSuccess ? fa.sharedSizeBytes : 4096;
+    const size_t budget = (size_t)optin > stat ? (size_t)optin - stat : 0;
     const size_t fixed = 1024 + (size_t)g.nt * H * AT_ROWS * 128 + (size_t)g.nt * 2 * AT_ROWS * keys * 2;
     const size_t kv_stage = (size_t)2 * H * keys * 128;
-    const int stages = fixed < 226u * 1024u ? (int)std::min<size_t>(AT_STAGES, (226u * 1024u - fixed) / kv_stage) : 0;
+    const int stages = fixed < budget ? (int)std::min<size_t>(AT_STAGES, (budget - fixed) / kv_stage) : 0;
     smem = fixed + (size_t)stages * kv_stage;
     return stages;
   };
@@ -513,9 +702,7 @@ cudaError_t launch_tree_attention_tc(const AttnArgs& a, const void* q_bf16, cuda
   }
   if (!make_map3(&g.ttk, a.tk, a.dh, a.Hkv, nodes, 1, keys)) return cudaErrorInvalidValue;
   if (!make_map3(&g.ttv, a.tv, a.dh, a.Hkv, nodes, 1, keys)) return cudaErrorInvalidValue;
-  void (*kern)(AttnTcArgs);
-  if (a.dh == 128) kern = keys == AT_KEYS1 ? tree_attn_tc_kernel<128, AT_KEYS1> : tree_attn_tc_kernel<128, AT_KEYS>;
-  else kern = keys == AT_KEYS1 ? tree_attn_tc_kernel<64, AT_KEYS1> : tree_attn_tc_kernel<64, AT_KEYS>;
+  void (*kern)(AttnTcArgs) = kernel_for(keys);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.nsplit + 1, a.Hkv, a.B * a.nrb);
