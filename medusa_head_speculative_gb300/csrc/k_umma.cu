@@ -618,12 +618,14 @@ static cudaError_t launch_splitk_reduce(const MatArgs& a, int ksplit, cudaStream
 }
 
 // K ranges for a launch of `ctas` CTAs that leaves SMs idle (single-segment launches, or
-// plain stores): about two CTAs per SM, at least 4 K blocks each, partials within kpart.
-static int choose_ksplit(const MatArgs& a, long ctas, int nk, int num_sms) {
+// plain stores): about per_sm resident CTAs per SM (two for the narrow kernel, one for the
+// wide one: a second wave of split CTAs costs more than the idle SMs it would fill), at
+// least 4 K blocks each, partials within kpart.
+static int choose_ksplit(const MatArgs& a, long ctas, int nk, int num_sms, int per_sm) {
   const bool splittable = a.nseg == 1 || (a.epi == EPI_STORE && !a.out_hi) || a.epi == EPI_ROPE;
   if (!splittable || !a.kpart || ctas >= num_sms || (a.nseg == 1 ? a.seg[0].rows : a.ldo) % 4 != 0)
     return 1;
-  int ksplit = (int)(2L * num_sms / ctas);
+  int ksplit = (int)((long)per_sm * num_sms / ctas);
   ksplit = ksplit > 8 ? 8 : ksplit;
   ksplit = ksplit > nk / 4 ? nk / 4 : ksplit;
   while (ksplit > 1 && (size_t)ksplit * a.M * a.ldo * sizeof(float) > a.kpart_bytes) --ksplit;
@@ -651,7 +653,7 @@ static cudaError_t launch_umma_wide(const MatArgs& m, uint32_t* status, int num_
   g.status = status;
   const int nk = (a.k + UM_K - 1) / UM_K;
   const int ytiles = (g.wtiles + 1) / 2 * 2;
-  g.ksplit = choose_ksplit(a, (long)nct * ytiles, nk, num_sms);
+  g.ksplit = choose_ksplit(a, (long)nct * ytiles, nk, num_sms, 1);
   g.kpart = a.kpart;
   for (int i = 0; i < a.nseg; ++i)
     if (!make_map(&g.tw[i], a.seg[i].w, a.k, a.seg[i].rows, a.k, UW_R)) return cudaErrorInvalidValue;
@@ -718,7 +720,7 @@ cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st
   // split K when the tiles alone cannot cover the SMs
   const int nk = (a.k + UM_K - 1) / UM_K;
   const int mchunks = (a.M + nbox - 1) / nbox;
-  const int ksplit = choose_ksplit(a, (long)mchunks * a.tile_off[a.nseg], nk, num_sms);
+  const int ksplit = choose_ksplit(a, (long)mchunks * a.tile_off[a.nseg], nk, num_sms, 2);
   g.ksplit = ksplit;
   g.kpart = a.kpart;
   for (int i = 0; i < a.nseg; ++i) {
