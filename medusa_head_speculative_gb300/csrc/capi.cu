@@ -687,8 +687,16 @@ medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) == cudaSuccess && sms > 0)
     p->num_sms = sms;
-  // vocab slices for the top-k pass: <= 32 per head, at least 1024 logits each
+  // vocab slices for the top-k pass: <= 32 per head, at least 1024 logits each, and no
+  // more than fit one resident wave of the selection's 256-thread CTAs (8 per SM), but
+  // at most 12 logits per thread
   p->topk_splits = std::max(1, std::min(32, (dims->V + 1023) / 1024));
+  {
+    const long pairs = (long)dims->B * (p->K + 1), wave = 8L * p->num_sms;
+    const int fit = (int)std::max(1L, wave / pairs);
+    const int floor12 = (dims->V + 12 * 256 - 1) / (12 * 256);
+    p->topk_splits = std::max(std::min(p->topk_splits, fit), std::min(floor12, p->topk_splits));
+  }
   p->topk_chunk = (dims->V + p->topk_splits - 1) / p->topk_splits;
   // attention: query-row blocks and prefix splits so the grid covers the SMs ~2x
   const int G = dims->Hq / dims->Hkv;

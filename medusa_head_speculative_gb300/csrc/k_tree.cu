@@ -93,15 +93,28 @@ __device__ void slice_topk(const TopkArgs& a, int sp, int k, int b) {
   const float* z = a.logits + ((long)b * a.nh + k) * a.V;
   const int lo = sp * a.chunk, hi = min(a.V, lo + a.chunk);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (hi - lo <= 4 * (int)blockDim.x) {
-    TopListN<4> L;
+  auto local = [&](auto L) {                            // N logits per thread, loads first
+    constexpr int N = sizeof(L.v) / sizeof(float);
     L.init();
+    float x[N];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < N; ++u) {
       const int v = lo + threadIdx.x + u * blockDim.x;
-      if (v < hi) L.insert(z[v], v);
+      x[u] = v < hi ? z[v] : NEG_INF;
+    }
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+      const int v = lo + threadIdx.x + u * blockDim.x;
+      if (v < hi) L.insert(x[u], v);
     }
     warp_merge(L, sv[warp], si[warp], a.rounds[k]);
+  };
+  if (hi - lo <= 4 * (int)blockDim.x) {
+    local(TopListN<4>{});
+  } else if (hi - lo <= 8 * (int)blockDim.x) {
+    local(TopListN<8>{});
+  } else if (hi - lo <= 12 * (int)blockDim.x) {
+    local(TopListN<12>{});
   } else {
     TopList L;
     L.init();
