@@ -207,7 +207,7 @@ void layout(medusa_plan* p) {
   // counters: [0,B) selection, [B,2B) commit per sequence, one per node row, then [B]
   // for the multi-layer compaction
   p->o_cnt = take((3 * B + M) * 4);
-  p->o_vparts = take(M * 4 * 6 * 4);
+  p->o_vparts = take(M * kVerifySlicesMax * 6 * 4);
   p->ws_bytes = off;
 }
 

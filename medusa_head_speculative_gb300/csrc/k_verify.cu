@@ -525,22 +525,21 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(CompactArgs a) {
 }
 
 // Fused verification for the whole step.  Each node row's vocabulary is split over
-// kVerifySlices CTAs; the last slice CTA of a row (per-row counter) merges the partials and
-// finishes the row; the last row of a sequence (per-sequence counter) runs that sequence's
-// acceptance and KV compaction.  Nothing waits; every counter is reset after use.
-constexpr int kVerifySlices = 4;
-
+// `slices` CTAs (gridDim.y: about one resident wave of CTAs in all, 1..4);
+// the last slice CTA of a row (per-row counter) merges the partials and finishes the row;
+// the last row of a sequence (per-sequence counter) runs that sequence's acceptance and KV
+// compaction.  Nothing waits; every counter is reset after use.
 template <typename T>
 __global__ void __launch_bounds__(256, 4) verify_commit_kernel(VerifyArgs v, CompactArgs c, int32_t* row_cnt,
                                                             int32_t* seq_cnt, float* parts) {
   __shared__ int s_last;
   pdl_trigger();
   pdl_wait();
-  const int row = blockIdx.x, sl = blockIdx.y, b = row / v.n1;
-  const int per = ((v.V + kVerifySlices - 1) / kVerifySlices + 3) / 4 * 4;
+  const int row = blockIdx.x, sl = blockIdx.y, b = row / v.n1, slices = gridDim.y;
+  const int per = ((v.V + slices - 1) / slices + 3) / 4 * 4;
   const int v0 = min(v.V, sl * per), v1 = min(v.V, v0 + per);
   RowPart r = row_part(v, row, v0, v1);
-  float* pp = parts + ((long)row * kVerifySlices + sl) * 6;
+  float* pp = parts + ((long)row * kVerifySlicesMax + sl) * 6;
   if (threadIdx.x == 0) {
     pp[0] = r.bv;
     pp[1] = __int_as_float(r.bi);
@@ -549,15 +548,15 @@ __global__ void __launch_bounds__(256, 4) verify_commit_kernel(VerifyArgs v, Com
     pp[4] = r.st.U;
     pp[5] = r.nonfinite ? 1.f : 0.f;
     __threadfence();
-    s_last = atomicAdd(row_cnt + row, 1) == kVerifySlices - 1;
+    s_last = atomicAdd(row_cnt + row, 1) == slices - 1;
   }
   __syncthreads();
   if (!s_last) return;
   if (threadIdx.x == 0) {                         // merge the row's slices
     __threadfence();
     RowPart m{-INFINITY, 0x7fffffff, SoftStat{-INFINITY, 0.f, 0.f}, false};
-    for (int q = 0; q < kVerifySlices; ++q) {
-      const float* x = parts + ((long)row * kVerifySlices + q) * 6;
+    for (int q = 0; q < slices; ++q) {
+      const float* x = parts + ((long)row * kVerifySlicesMax + q) * 6;
       const float bv = __ldcg(x), m0 = __ldcg(x + 2), S = __ldcg(x + 3), U = __ldcg(x + 4);
       const int bi = __float_as_int(__ldcg(x + 1));
       if (better(bv, bi, m.bv, m.bi)) { m.bv = bv; m.bi = bi; }
@@ -579,7 +578,18 @@ __global__ void __launch_bounds__(256, 4) verify_commit_kernel(VerifyArgs v, Com
 
 cudaError_t launch_verify_commit(const VerifyArgs& v, const CompactArgs& c, int32_t* row_cnt,
                                  int32_t* seq_cnt, float* parts, cudaStream_t st) {
-  dim3 grid(v.B * v.n1, kVerifySlices);
+  static int num_sms = 0;
+  if (!num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      num_sms = 148;
+  }
+  const int rows = v.B * v.n1;
+  // about one resident wave (4 CTAs per SM), at most 4 slices: more made the per-row merge
+  // cost more than the shorter slices saved
+  const int slices = std::max(1, std::min(4, 4 * num_sms / rows));
+  dim3 grid(rows, slices);
   if (c.dtype == 0)
     return launch_kernel(verify_commit_kernel<float>, grid, dim3(256), 0, st, 1, v, c, row_cnt, seq_cnt, parts);
   return launch_kernel(verify_commit_kernel<bf16>, grid, dim3(256), 0, st, 1, v, c, row_cnt, seq_cnt, parts);

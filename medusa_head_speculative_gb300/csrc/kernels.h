@@ -200,7 +200,8 @@ struct TreeGreedyArgs {
 size_t tree_greedy_smem(int N, int smax);
 cudaError_t launch_tree_greedy(const TreeGreedyArgs& a, cudaStream_t st);
 // Fused per-row statistics + acceptance + KV compaction.  row_cnt [B*n1] and seq_cnt [B]
-// zero on entry (left zero); parts: [B*n1][4][6] float scratch.
+// zero on entry (left zero); parts: [B*n1][kVerifySlicesMax][6] float scratch.
+constexpr int kVerifySlicesMax = 8;
 cudaError_t launch_verify_commit(const VerifyArgs& v, const CompactArgs& c, int32_t* row_cnt,
                                  int32_t* seq_cnt, float* parts, cudaStream_t st);
 
