@@ -687,17 +687,19 @@ medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) == cudaSuccess && sms > 0)
     p->num_sms = sms;
-  // vocab slices for the top-k pass: <= 32 per head, at least 1024 logits each, and no
-  // more than fit one resident wave of the selection's 256-thread CTAs (8 per SM), but
-  // at most 12 logits per thread
-  p->topk_splits = std::max(1, std::min(32, (dims->V + 1023) / 1024));
+  // vocab slices for the top-k pass: as many as one resident wave of the selection's
+  // 256-thread CTAs holds, but no fewer than one per 4096 logits (at most 16 per thread)
+  // and no more than one per 1024 logits or 32 per head; slices start on 16-byte
+  // boundaries when V allows (the selection then loads float4)
   {
-    const long pairs = (long)dims->B * (p->K + 1), wave = 8L * p->num_sms;
-    const int fit = (int)std::max(1L, wave / pairs);
-    const int floor12 = (dims->V + 12 * 256 - 1) / (12 * 256);
-    p->topk_splits = std::max(std::min(p->topk_splits, fit), std::min(floor12, p->topk_splits));
+    const long pairs = (long)dims->B * (p->K + 1);
+    const long wave = (long)std::max(1, heads_select_ctas_per_sm()) * p->num_sms;
+    const long lo = (dims->V + 4095) / 4096, hi = std::max(1, std::min(32, (dims->V + 1023) / 1024));
+    const long sp = std::min<long>(32, std::max(lo, std::min(hi, wave / pairs)));
+    p->topk_splits = (int)std::max(1L, sp);
   }
   p->topk_chunk = (dims->V + p->topk_splits - 1) / p->topk_splits;
+  if (dims->V % 4 == 0) p->topk_chunk = (p->topk_chunk + 3) / 4 * 4;
   // attention: query-row blocks and prefix splits so the grid covers the SMs ~2x
   const int G = dims->Hq / dims->Hkv;
   const int R = p->n1 * G;

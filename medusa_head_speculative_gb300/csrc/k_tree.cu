@@ -8,6 +8,7 @@
 // ids, flatten/restore indices).  Order of candidates: larger logit first, lower token id
 // on equal logits.
 #include <cmath>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -83,10 +84,35 @@ __device__ __forceinline__ void warp_merge(TopListN<N>& L, float* ov, int* oi, i
   }
 }
 
+// Sorts N (value, token) pairs into descending `better` order with a bitonic sorting
+// network (N a power of two); every comparator index is a compile-time constant, so the
+// pairs stay in registers.
+template <int N>
+__device__ __forceinline__ void bitonic_sort_desc(float (&v)[N], int (&ix)[N]) {
+#pragma unroll
+  for (int k = 2; k <= N; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+      for (int x = 0; x < N; ++x) {
+        const int y = x ^ j;
+        if (y <= x) continue;
+        // blocks of k with bit k clear end descending, the others ascending: each pair of
+        // neighbouring blocks is then a bitonic sequence for the next merge
+        const bool sw = (x & k) == 0 ? better(v[y], ix[y], v[x], ix[x]) : better(v[x], ix[x], v[y], ix[y]);
+        if (sw) {
+          const float tv = v[x]; v[x] = v[y]; v[y] = tv;
+          const int ti = ix[x]; ix[x] = ix[y]; ix[y] = ti;
+        }
+      }
+}
+
 // The 16 best (logit, token) pairs of one vocab slice of one head, by a 256-thread CTA.
-// Slices of up to 1024 logits leave each thread at most 4 of them, so the per-thread and
-// per-warp lists are 4 deep; the 8 warps' lists (one run of up to 16 per warp) are then
-// spread 4 entries per lane over warp 0 and merged the same way.
+// When the slice starts on a 16-byte boundary each thread loads F float4 of it (4F <= 16
+// logits, all loads issued first), sorts them with a network and the warp merges the 32
+// sorted lists; otherwise per-thread lists are filled by insertion.  The 8 warps' lists
+// (one run of up to 16 per warp) are then spread 4 entries per lane over warp 0 and merged
+// the same way.  NaN logits never enter a list.
 __device__ void slice_topk(const TopkArgs& a, int sp, int k, int b) {
   __shared__ float sv[8][kTops];
   __shared__ int si[8][kTops];
@@ -109,7 +135,46 @@ __device__ void slice_topk(const TopkArgs& a, int sp, int k, int b) {
     }
     warp_merge(L, sv[warp], si[warp], a.rounds[k]);
   };
-  if (hi - lo <= 4 * (int)blockDim.x) {
+  // F float4 per thread (loads first), sorted into a list of NP = 4, 8 or 16 entries
+  auto local_vec = [&](auto L, auto f) {
+    constexpr int NP = sizeof(L.v) / sizeof(float);
+    constexpr int F = decltype(f)::value;
+    const float4* z4 = reinterpret_cast<const float4*>(z);
+    const int q0 = lo >> 2, q1 = hi >> 2;
+    float4 x[F];
+#pragma unroll
+    for (int u = 0; u < F; ++u) {
+      const int q = q0 + threadIdx.x + u * blockDim.x;
+      x[u] = q < q1 ? z4[q] : make_float4(NEG_INF, NEG_INF, NEG_INF, NEG_INF);
+    }
+#pragma unroll
+    for (int u = 0; u < F; ++u) {
+      const int q = q0 + threadIdx.x + u * blockDim.x;
+      const float e[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const bool ok = q < q1 && !(e[c] != e[c]);
+        L.v[4 * u + c] = ok ? e[c] : NEG_INF;
+        L.i[4 * u + c] = ok ? 4 * q + c : NO_IDX;
+      }
+    }
+#pragma unroll
+    for (int t = 4 * F; t < NP; ++t) { L.v[t] = NEG_INF; L.i[t] = NO_IDX; }
+    bitonic_sort_desc(L.v, L.i);
+    warp_merge(L, sv[warp], si[warp], a.rounds[k]);
+  };
+  const int bd = (int)blockDim.x;
+  const bool vec = (a.V & 3) == 0 && (a.chunk & 3) == 0;   // slices start on 16 bytes
+  const int n4 = (hi - lo + 3) >> 2;
+  if (vec && n4 <= bd) {
+    local_vec(TopListN<4>{}, std::integral_constant<int, 1>{});
+  } else if (vec && n4 <= 2 * bd) {
+    local_vec(TopListN<8>{}, std::integral_constant<int, 2>{});
+  } else if (vec && n4 <= 3 * bd) {
+    local_vec(TopListN<16>{}, std::integral_constant<int, 3>{});
+  } else if (vec && n4 <= 4 * bd) {
+    local_vec(TopListN<16>{}, std::integral_constant<int, 4>{});
+  } else if (hi - lo <= 4 * bd) {
     local(TopListN<4>{});
   } else if (hi - lo <= 8 * (int)blockDim.x) {
     local(TopListN<8>{});
@@ -213,15 +278,22 @@ __global__ void __launch_bounds__(256) heads_select_kernel(TopkArgs t, MergeArgs
   pdl_wait();
   const int b = blockIdx.z;
   slice_topk(t, blockIdx.x, blockIdx.y + t.k0, b);
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(counter + b, 1) == t.splits * (t.nh - t.k0) - 1;
+  if (threadIdx.x == 0) {          // thread 0 wrote this slice's candidates
+    __threadfence();
+    s_last = atomicAdd(counter + b, 1) == t.splits * (t.nh - t.k0) - 1;
+  }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
   merge_heads(m, b, tv, ti, &s_root);
   node_tokens(tr, b, ti, s_root);
   if (threadIdx.x == 0) counter[b] = 0;
+}
+
+int heads_select_ctas_per_sm() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, heads_select_kernel, 256, 0) != cudaSuccess) n = 0;
+  return n;
 }
 
 cudaError_t launch_heads_select(const TopkArgs& t, const MergeArgs& m, const TreeArgs& tr,

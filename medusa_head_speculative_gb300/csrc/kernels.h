@@ -108,6 +108,8 @@ cudaError_t launch_tree_build(const TreeArgs& a, cudaStream_t st);
 // counter: [B] zeros on entry; left at zero on exit.
 cudaError_t launch_heads_select(const TopkArgs& t, const MergeArgs& m, const TreeArgs& tr,
                                 int32_t* counter, cudaStream_t st);
+// Resident 256-thread selection CTAs per SM (0 when the query fails).
+int heads_select_ctas_per_sm();
 
 // qkv [M][(Hq+2Hkv)*dh] fp32 -> q [M][Hq][dh] fp32 (RoPE; also as bf16 into qb when
 // non-null), tree k (RoPE) / v in dtype.
