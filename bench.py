@@ -77,9 +77,12 @@ def kernel_bytes(w: S.Workload, n1: int, tc_heads: bool):
     qd, kd = w.Hq * w.dh, w.Hkv * w.dh
     act = 4 if tc_heads else 0          # bf16 hi + lo copies written next to fp32
     kv_prefix = sum(w.lengths) * 2 * kd * es
+    # CUDA-core heads (batch 1): the LM head's root pass shares the first launch
+    lm = (V * d * es + B * V * 4) if not tc_heads else 0
     return {
-        "heads_w1": K * d * d * es + B * d * 4 + B * K * d * (4 + act),
-        "heads_vocab": (K + 1) * V * d * es + B * (K + 1) * d * 4 + B * (K + 1) * V * 4,
+        "heads_w1": K * d * d * es + B * d * 4 + B * K * d * (4 + act) + lm,
+        "heads_vocab": (K + 1) * V * d * es + B * (K + 1) * d * 4 + B * (K + 1) * V * 4
+                       - (lm + (B * d * 4 if lm else 0)),
         "layer_qkv": (qd + 2 * kd) * d * es + M * d * 2 + M * (qd + 2 * kd) * 4,
         "tree_attention": kv_prefix + M * (qd * 4 + 2 * kd * es),
         "layer_out": d * qd * es + M * qd * 4 + M * d * (2 + 4 + 4),
@@ -87,16 +90,17 @@ def kernel_bytes(w: S.Workload, n1: int, tc_heads: bool):
     }
 
 
-def kernel_flops(w: S.Workload, n1: int):
+def kernel_flops(w: S.Workload, n1: int, tc_heads: bool = True):
     """Algorithmic FLOPs per launch of the contractions (the method's products, counted
     once: the hi/lo activation halves that double the tensor-core work are not counted)."""
     B, d, V, K = w.B, w.d, w.V, w.K
     M = B * n1
     qd, kd = w.Hq * w.dh, w.Hkv * w.dh
     prefix = sum(w.lengths)
+    lm = 0 if tc_heads else 2 * B * V * d
     return {
-        "heads_w1": 2 * B * K * d * d,
-        "heads_vocab": 2 * B * (K + 1) * V * d,
+        "heads_w1": 2 * B * K * d * d + lm,
+        "heads_vocab": 2 * B * (K + 1) * V * d - lm,
         "layer_qkv": 2 * M * (qd + 2 * kd) * d,
         "tree_attention": 4 * n1 * w.Hq * w.dh * prefix + 4 * B * n1 * n1 * w.Hq * w.dh // 2,
         "layer_out": 2 * M * d * qd,
@@ -591,7 +595,7 @@ def run_ours(args, w: S.Workload):
         if name in kb:
             row["gbs"] = round(kb[name] / (us * 1e-6) / 1e9, 1)
         ktab[name] = row
-    kf = kernel_flops(w, n1)
+    kf = kernel_flops(w, n1, plan_tc_heads(w))
     tflops, tflops_kind = tensor_peak()
     ridge = tflops * 1e12 / (hbm * 1e9)                 # FLOP per byte where the bounds meet
     dom = max((n for n in kernels if n in kb), key=lambda n: kernels[n][1])

@@ -252,9 +252,23 @@ medusa_status heads_impl(const medusa_plan* p, const float* h, const int32_t* ro
     s.rows = D;
     s.out_off = k * D;
   }
+  // z_0 = LM h (only when the root is not given) reads h, not u: on the CUDA-core path it
+  // joins this launch, whose few rows per warp otherwise leave the warps unevenly loaded
+  const bool lm_first = !p->tc_heads && !root_in;
+  if (lm_first) {
+    MatSeg& s = a.seg[K];
+    s.w = w->lm;
+    s.x = h; s.ldx = D;
+    s.rows = V;
+    s.out_off = 0;
+    a.nseg = K + 1;
+    a.alt_from = K;
+    a.out_alt = logits;
+    a.ldo_alt = (long)(K + 1) * V;
+  }
   LAUNCH(p, KN_H_W1, st, p->tc_heads ? launch_umma_gemm(a, p->d_status, st) : launch_rowdot(a, d.dtype, st));
-  // z_0 = LM h (only when the root is not given), z_k = W2_k u_k
-  const int k0 = root_in ? 1 : 0;
+  // z_k = W2_k u_k (and z_0 here when it did not join the first launch)
+  const int k0 = root_in || lm_first ? 1 : 0;
   MatArgs b{};
   b.nseg = K + 1 - k0;
   b.M = B;
@@ -262,7 +276,7 @@ medusa_status heads_impl(const medusa_plan* p, const float* h, const int32_t* ro
   b.out = logits;
   b.ldo = (long)(K + 1) * V;
   b.epi = EPI_STORE;
-  if (!root_in) {
+  if (k0 == 0) {
     b.seg[0].w = w->lm;
     b.seg[0].x = h; b.seg[0].a_hi = hhi; b.seg[0].a_lo = hlo; b.seg[0].ldx = D;
     b.seg[0].rows = V;

@@ -13,8 +13,12 @@
 
 namespace medusa {
 
-__device__ __forceinline__ void epilogue_store(const MatArgs& a, const MatSeg& s, int m, int r,
+__device__ __forceinline__ void epilogue_store(const MatArgs& a, const MatSeg& s, int si, int m, int r,
                                                float acc) {
+  if (a.out_alt && si >= a.alt_from) {
+    a.out_alt[(long)m * a.ldo_alt + s.out_off + r] = acc;
+    return;
+  }
   float y = acc;
   if (a.epi == EPI_SILU_RES) {
     y = silu(acc) + a.res_f32[(long)m * a.ldr + r];
@@ -128,7 +132,7 @@ __global__ void __launch_bounds__(256) rowdot_kernel(MatArgs a, long total_rows)
           for (int m = 0; m < MT; ++m) acc[m] = warp_sum(acc[m]);
 #pragma unroll
           for (int m = 0; m < MT; ++m)
-            if (lane == m && m < mt) epilogue_store(a, s, m0 + m, r, acc[m]);
+            if (lane == m && m < mt) epilogue_store(a, s, si, m0 + m, r, acc[m]);
         }
       }
     }

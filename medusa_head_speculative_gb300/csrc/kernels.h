@@ -56,6 +56,12 @@ struct MatArgs {
   void* rv;
   int rkv_bf16;
   uint32_t* rope_status;
+  // CUDA-core row-dot only: when out_alt is set, segments from alt_from on store their
+  // raw sums to out_alt[m * ldo_alt + out_off + r] instead (no epilogue), so the heads'
+  // first projection and the LM head can share one launch.
+  int alt_from;
+  float* out_alt;
+  long ldo_alt;
 };
 
 // CUDA-core row-dot projection: dtype 0 = f32 weights, 1 = bf16.
