@@ -606,6 +606,10 @@ def run_ours(args, w: S.Workload):
                 "peak": tflops, "unit": "TFLOP/s",
                 "frac": round(kf[dom] / (dom_us * 1e-6) / 1e12 / tflops, 4), "traffic": traffic,
                 "algorithmic_flops": kf[dom],
+                # fp32 activations enter the tensor cores as bf16 hi + lo halves: two MMAs
+                # per product, of which only the method's one is counted above
+                "issued_per_algorithmic": 2 if (dom in ("verify_logits", "layer_out")
+                                                or (dom.startswith("heads") and plan_tc_heads(w))) else 1,
                 "peak_source": f"{tflops_kind} (MEASURED_PEAKS.json bf16_tflops_sustained)"
                 if tflops_kind == "measured" else "fallback 1.7 PFLOP/s sustained"}
     else:
