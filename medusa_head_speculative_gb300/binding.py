@@ -19,7 +19,7 @@ MEDUSA_ERR_CUDA, MEDUSA_ERR_DEVICE, MEDUSA_ERR_WORKSPACE = -3, -4, -6
 F32, BF16 = 0, 1
 GREEDY, TYPICAL, REJECT = 0, 1, 2
 MAX_HEADS, MAX_TOPS, MAX_NODES = 8, 16, 256
-FLAG_TOKEN_RANGE, FLAG_KV_CAPACITY, FLAG_PAGE_RANGE, FLAG_NONFINITE = 1, 2, 4, 8
+FLAG_TOKEN_RANGE, FLAG_KV_CAPACITY, FLAG_PAGE_RANGE, FLAG_NONFINITE, FLAG_TIMEOUT = 1, 2, 4, 8, 16
 STATUS_NAMES = {0: "OK", -1: "INVALID", -2: "UNSUPPORTED", -3: "CUDA", -4: "DEVICE", -6: "WORKSPACE"}
 
 
@@ -115,6 +115,7 @@ def lib():
         "medusa_loop_run": (I, [P, I, P]),
         "medusa_loop_steps": (I, [P, P, C.POINTER(C.c_longlong)]),
         "medusa_loop_destroy": (None, [P]),
+        "medusa_plan_expire_wait_once": (I, [P, C.c_ulonglong]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -227,6 +228,10 @@ class Plan:
         if code not in (MEDUSA_OK, MEDUSA_ERR_DEVICE):
             raise MedusaError("medusa_get_status", code)
         return flags.value
+
+    def expire_wait_once(self, ns):
+        """Failure-path testing: the next verification-logit GEMM's wait runs out after ns."""
+        _check("medusa_plan_expire_wait_once", lib().medusa_plan_expire_wait_once(self.handle, int(ns)))
 
     def profile_start(self, max_launches):
         _check("medusa_profile_start", lib().medusa_profile_start(self.handle, max_launches))

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <queue>
 #include <cmath>
 #include <cstdint>
@@ -73,6 +74,8 @@ struct medusa_plan {
   uint32_t* d_mask = nullptr;            // device [n1][8] ancestor bitmask of the tree
   int32_t* d_retr = nullptr;             // device [n1][K+1] root->leaf paths
   int device = 0, num_sms = 148;
+  // failure-path tests: one-shot wait limit for the next verification-logit GEMM
+  mutable std::atomic<unsigned long long> test_wait_ns{0};
   bool tc_heads = false, tc_nodes = false;   // tensor-core projections
   bool tc_attn = false;                      // tensor-core tree attention
   int M;                                     // node rows B * n1
@@ -535,6 +538,7 @@ medusa_status vlogits_impl(const medusa_plan* p, const medusa_weights* w, const 
   s.ldx = d.d;
   s.rows = d.V;
   s.out_off = 0;
+  if (p->tc_nodes) a.test_wait_ns = p->test_wait_ns.exchange(0);
   LAUNCH(p, KN_VLOGITS, st, p->tc_nodes ? launch_umma_gemm(a, p->d_status, st) : launch_rowdot(a, d.dtype, st));
   if (!with_stats) return MEDUSA_OK;
   VerifyArgs v = verify_args(p, tok, acc);
@@ -866,6 +870,13 @@ medusa_status medusa_profile_stop(medusa_plan* p, void* stream, medusa_kernel_ti
   }
   *n = m;
   p->prof.release();
+  return MEDUSA_OK;
+}
+
+medusa_status medusa_plan_expire_wait_once(medusa_plan* p, unsigned long long ns) {
+  if (!p || ns == 0 || ns > 10000000000ull) return MEDUSA_ERR_INVALID;
+  if (!p->tc_nodes) return MEDUSA_ERR_UNSUPPORTED;
+  p->test_wait_ns.store(ns);
   return MEDUSA_OK;
 }
 

@@ -231,7 +231,7 @@ __device__ void staged_epilogue(const MatArgs& a, const MatSeg& s, int rbase, in
 template <bool HAS_LO>
 __global__ void __launch_bounds__(128, 2) umma_gemm_kernel(const __grid_constant__ UmmaArgs g) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bars[2 * 8 + 1];
+  __shared__ uint64_t bars[2 * 8 + 2];
   __shared__ uint32_t tmem_slot;
   __shared__ int s_issued, s_consumed, s_bad;
   const MatArgs& a = g.m;
@@ -252,6 +252,7 @@ __global__ void __launch_bounds__(128, 2) umma_gemm_kernel(const __grid_constant
   auto full = [&](int i) { return bar0 + 8u * i; };
   auto empty = [&](int i) { return bar0 + 8u * (8 + i); };
   const uint32_t accb = bar0 + 8u * 16;
+  const uint32_t never = bar0 + 8u * 17;               // nothing arrives on it (test hook)
 
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
@@ -259,6 +260,7 @@ __global__ void __launch_bounds__(128, 2) umma_gemm_kernel(const __grid_constant
       mbar_init(empty(i), 1);
     }
     mbar_init(accb, 1);
+    mbar_init(never, 1);
     s_issued = 0;
     s_consumed = 0;
     s_bad = 0;
@@ -312,7 +314,9 @@ __global__ void __launch_bounds__(128, 2) umma_gemm_kernel(const __grid_constant
     int j = 0, st = 0;
     uint32_t ph = 0;
     uint64_t off = 0;
-    for (; j < nkl; ++j) {
+    // failure-path test hook: a wait that runs out, as one on a copy that never lands
+    if (a.test_wait_ns && !mbar_wait(never, 0, a.test_wait_ns)) timed_out = true;
+    for (; j < nkl && !timed_out; ++j) {
       if (!mbar_wait(full(st), ph, TC_TIMEOUT_NS)) { timed_out = true; break; }
       tc_fence_after();
       const uint64_t ad = ad0 + off, bd = bd0 + off, ld = ld0 + off;
@@ -354,21 +358,17 @@ __global__ void __launch_bounds__(128, 2) umma_gemm_kernel(const __grid_constant
 // For hundreds to thousands of activation rows (the node projections at batch > 1) the
 // 128 x nbox tiles above re-read their operands from L2 faster than the tensor cores use
 // them.  Here a CTA owns 256 weight rows (two 128-row accumulators in TMEM) against up to
-// 256 activation rows, and the two CTAs of a cluster (consecutive weight tiles, the same
-// activation rows) split each activation tile: each loads half and multicasts it to both.
-// Per stage a CTA then reads 32 KB of weights and half of the activation bytes for twice
-// the MMA work of a 128-row tile.  The stage ring is shared across the pair: a stage is
-// refilled only after both CTAs' MMAs have read it (each MMA thread's commit arrives on
-// the empty barriers of both CTAs).
+// 256 activation rows: per stage it reads 32 KB of weights and the activation tile for
+// twice the MMA work of a 128-row tile.  CTAs of neighbouring weight tiles read the same
+// activation tiles, which L2 serves after the first read.
 constexpr int UW_R = 256;                    // weight rows per CTA
 constexpr uint32_t UW_W_BYTES = UW_R * 128;  // one 64-column stage of them
-constexpr uint16_t UW_PAIR = 0x3;            // both CTAs of the cluster
 
 struct UmmaWideArgs {
   CUtensorMap tw[kMaxSeg];   // weights of each segment: dims {k, rows}, box {64, 256}
-  CUtensorMap ta, tl;        // activations (hi, lo), shared by all segments: box {64, nbox/2}
+  CUtensorMap ta, tl;        // activations (hi, lo), shared by all segments: box {64, nbox}
   MatArgs m;                 // tile_off counts 256-row tiles
-  int wtiles;                // weight tiles; grid.y is this rounded up to even
+  int wtiles;                // weight tiles (grid.y)
   int nbox, stages, ksplit;
   float* kpart;
   uint32_t tmem_cols, acc_stride;
@@ -378,20 +378,18 @@ struct UmmaWideArgs {
 template <bool HAS_LO>
 __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant__ UmmaWideArgs g) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bars[2 * 8 + 1];
+  __shared__ uint64_t bars[2 * 8 + 2];
   __shared__ uint32_t tmem_slot;
   __shared__ int s_issued, s_consumed, s_bad;
   const MatArgs& a = g.m;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = cluster_rank();
-  const bool has_w = (int)blockIdx.y < g.wtiles;
   int si = 0;
-  while (has_w && si + 1 < a.nseg && (int)blockIdx.y >= a.tile_off[si + 1]) ++si;
+  while (si + 1 < a.nseg && (int)blockIdx.y >= a.tile_off[si + 1]) ++si;
   const MatSeg& s = a.seg[si];
-  const int rbase = has_w ? ((int)blockIdx.y - a.tile_off[si]) * UW_R : 0;
-  const int rows_here = has_w ? min(UW_R, s.rows - rbase) : 0;
-  const int nacc = rows_here > 128 ? 2 : (rows_here > 0 ? 1 : 0);
-  const int m0 = (int)blockIdx.x * g.nbox, half = g.nbox / 2;
+  const int rbase = ((int)blockIdx.y - a.tile_off[si]) * UW_R;
+  const int rows_here = min(UW_R, s.rows - rbase);
+  const int nacc = rows_here > 128 ? 2 : 1;
+  const int m0 = (int)blockIdx.x * g.nbox;
   const int nk = (a.k + UM_K - 1) / UM_K;
   const int kt0 = (int)((long)blockIdx.z * nk / g.ksplit);
   const int nkl = (int)((long)(blockIdx.z + 1) * nk / g.ksplit) - kt0;
@@ -403,13 +401,15 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
   auto full = [&](int i) { return bar0 + 8u * i; };
   auto empty = [&](int i) { return bar0 + 8u * (8 + i); };
   const uint32_t accb = bar0 + 8u * 16;
+  const uint32_t never = bar0 + 8u * 17;               // nothing arrives on it (test hook)
 
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(full(i), 1);
-      mbar_init(empty(i), 2);                           // one commit from each CTA's MMA
+      mbar_init(empty(i), 1);
     }
     mbar_init(accb, 1);
+    mbar_init(never, 1);
     s_issued = 0;
     s_consumed = 0;
     s_bad = 0;
@@ -418,7 +418,6 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
   if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), g.tmem_cols);
   tc_fence_before();
   __syncthreads();
-  cluster_sync();                       // the peer's barriers exist before any copy or arrive
   tc_fence_after();
   pdl_trigger();                        // after the TMEM allocation, as above
   const uint32_t tmem = tmem_slot;
@@ -426,17 +425,15 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
 
   if (warp == 0 && lane == 0) {                         // ---- TMA producer
     const uint64_t pw = policy_evict_first(), pa = policy_evict_last();
-    const uint32_t stage_tx = (has_w ? UW_W_BYTES : 0u) + A_BYTES * (HAS_LO ? 2 : 1);
+    const uint32_t stage_tx = STAGE;
     // weights of the first S stages before the wait for earlier kernels, as above
     const int pre = nkl < S ? nkl : S;
     for (int j = 0; j < pre; ++j) {
       mbar_expect_tx(full(j), stage_tx);
-      if (has_w) tma_load_2d(base + j * STAGE, &g.tw[si], (kt0 + j) * UM_K, rbase, full(j), pw);
+      tma_load_2d(base + j * STAGE, &g.tw[si], (kt0 + j) * UM_K, rbase, full(j), pw);
     }
     pdl_wait();
     const CUtensorMap* tw = &g.tw[si];
-    const uint32_t aoff = UW_W_BYTES + rank * (uint32_t)half * 128;
-    const int arow = m0 + (int)rank * half;
     int j = 0, st = 0;
     uint32_t ph = 0;                                    // phase of the ring's current pass
     for (; j < nkl; ++j) {
@@ -445,10 +442,10 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
       if (j >= pre) {
         if (!mbar_wait(empty(st), ph ^ 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
         mbar_expect_tx(full(st), stage_tx);
-        if (has_w) tma_load_2d(ws, tw, kx, rbase, full(st), pw);
+        tma_load_2d(ws, tw, kx, rbase, full(st), pw);
       }
-      tma_load_2d_mc(ws + aoff, &g.ta, kx, arow, full(st), UW_PAIR, pa);
-      if (HAS_LO) tma_load_2d_mc(ws + aoff + A_BYTES, &g.tl, kx, arow, full(st), UW_PAIR, pa);
+      tma_load_2d(ws + UW_W_BYTES, &g.ta, kx, m0, full(st), pa);
+      if (HAS_LO) tma_load_2d(ws + UW_W_BYTES + A_BYTES, &g.tl, kx, m0, full(st), pa);
       if (++st == S) { st = 0; ph ^= 1; }
     }
     s_issued = j;
@@ -463,11 +460,13 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
     int j = 0, st = 0;
     uint32_t ph = 0;
     uint64_t off = 0;
-    for (; j < nkl; ++j) {
+    // failure-path test hook: a wait that runs out, as one on a copy that never lands
+    if (a.test_wait_ns && !mbar_wait(never, 0, a.test_wait_ns)) timed_out = true;
+    for (; j < nkl && !timed_out; ++j) {
       if (!mbar_wait(full(st), ph, TC_TIMEOUT_NS)) { timed_out = true; break; }
       tc_fence_after();
       const uint64_t bd = b0 + off, ld = l0 + off;
-      if (nacc > 0) {
+      {
         const uint64_t ad = a0 + off;
 #pragma unroll
         for (int ks = 0; ks < UM_K / 16; ++ks) {
@@ -483,7 +482,7 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
           if (HAS_LO) umma_bf16(d1, ad + 2 * ks, ld + 2 * ks, idesc, 1);
         }
       }
-      umma_commit_mc(empty(st), UW_PAIR);               // frees the stage in both CTAs
+      umma_commit(empty(st));                           // frees the stage
       if (++st == S) { st = 0; ph ^= 1; off = 0; } else { off += dstep; }
     }
     s_consumed = j;
@@ -494,9 +493,9 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
   pdl_wait();
   const bool acc_ok = mbar_wait(accb, 0, TC_TIMEOUT_NS);
   tc_fence_after();
-  // every MMA has read its stage and every copy (ours and the peer's multicast halves)
-  // has landed in this CTA's ring unless a wait expired: the ring is free for staging
-  const bool run = __syncthreads_and(acc_ok) && !s_bad && nkl > 0 && nacc > 0;
+  // every MMA has read its stage and every copy has landed unless a wait expired: the
+  // ring is free for staging
+  const bool run = __syncthreads_and(acc_ok) && !s_bad && nkl > 0;
   if (run) {
     float* stage = reinterpret_cast<float*>(smem_raw + (base - smem_u32(smem_raw)));
     staged_epilogue(a, s, rbase, nacc, m0, g.nbox, tmem, g.acc_stride, stage,
@@ -505,18 +504,11 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
   if (timed_out || !acc_ok) set_flag(g.status, MEDUSA_FLAG_TIMEOUT);
   tc_fence_before();
   __syncthreads();
-  if (tid == 0) {
-    // copies issued but not consumed (bounded), then the last use of every stage: both
-    // CTAs' commits must have landed on this CTA's empty barriers before it may exit
+  if (tid == 0) {                                       // drain copies issued but not consumed
     for (int j = s_consumed; j < s_issued; ++j)
       mbar_wait(full(j % S), (j / S) & 1, TC_TIMEOUT_NS / 16);
-    for (int st = 0; st < S && st < nkl; ++st) {
-      const int uses = (nkl - st + S - 1) / S;
-      mbar_wait(empty(st), (uses - 1) & 1, TC_TIMEOUT_NS / 16);
-    }
   }
   __syncthreads();
-  cluster_sync();                       // nothing more arrives from the peer after this
   if (warp == 1) tmem_dealloc(tmem, g.tmem_cols);
 }
 
@@ -652,21 +644,20 @@ static cudaError_t launch_umma_wide(const MatArgs& m, uint32_t* status, int num_
   if (g.stages < 2) return cudaErrorInvalidValue;
   g.status = status;
   const int nk = (a.k + UM_K - 1) / UM_K;
-  const int ytiles = (g.wtiles + 1) / 2 * 2;
-  g.ksplit = choose_ksplit(a, (long)nct * ytiles, nk, num_sms, 1);
+  g.ksplit = choose_ksplit(a, (long)nct * g.wtiles, nk, num_sms, 1);
   g.kpart = a.kpart;
   for (int i = 0; i < a.nseg; ++i)
     if (!make_map(&g.tw[i], a.seg[i].w, a.k, a.seg[i].rows, a.k, UW_R)) return cudaErrorInvalidValue;
-  if (!make_map(&g.ta, a.seg[0].a_hi, a.k, a.M, a.seg[0].ldx, g.nbox / 2)) return cudaErrorInvalidValue;
-  if (has_lo && !make_map(&g.tl, a.seg[0].a_lo, a.k, a.M, a.seg[0].ldx, g.nbox / 2)) return cudaErrorInvalidValue;
+  if (!make_map(&g.ta, a.seg[0].a_hi, a.k, a.M, a.seg[0].ldx, g.nbox)) return cudaErrorInvalidValue;
+  if (has_lo && !make_map(&g.tl, a.seg[0].a_lo, a.k, a.M, a.seg[0].ldx, g.nbox)) return cudaErrorInvalidValue;
   // at least 116 KB of shared memory keeps one CTA per SM, so the 512-column TMEM
-  // allocations of co-scheduled clusters never wait on each other
+  // allocations of co-resident CTAs never wait on each other
   size_t smem = (size_t)g.stages * stage + 1024;
   if (smem < 116u * 1024u) smem = 116u * 1024u;
   auto kern = has_lo ? umma_wide_kernel<true> : umma_wide_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = launch_kernel(kern, dim3(nct, ytiles, g.ksplit), dim3(128), smem, st, 2, g);
+  e = launch_kernel(kern, dim3(nct, g.wtiles, g.ksplit), dim3(128), smem, st, 1, g);
   if (e != cudaSuccess || g.ksplit == 1) return e;
   return launch_splitk_reduce(a, g.ksplit, st);
 }

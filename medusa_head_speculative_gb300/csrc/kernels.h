@@ -62,6 +62,10 @@ struct MatArgs {
   int alt_from;
   float* out_alt;
   long ldo_alt;
+  // Tensor-core path, failure-path tests only (0 otherwise): the MMA thread first waits
+  // on a barrier that nothing arrives on, for at most this many nanoseconds, and then
+  // takes the expired-wait path.
+  unsigned long long test_wait_ns;
 };
 
 // CUDA-core row-dot projection: dtype 0 = f32 weights, 1 = bf16.

@@ -58,27 +58,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
 }
-// The same load delivered to every CTA of the cluster in cta_mask: the box lands at offset
-// dst of each CTA's shared memory and completes its bytes on the mbarrier at offset bar
-// of each of them.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                               uint32_t bar, uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask), "l"(policy)
-      : "memory");
-}
-// Rank of this CTA in its cluster, and a full cluster barrier (all threads of all CTAs).
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -121,14 +100,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
-// Arrive on the mbarrier at offset bar of every CTA in cta_mask once this thread's
-// earlier tcgen05 operations have completed.
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(cta_mask)
-      : "memory");
-}
 // 16 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
@@ -158,8 +129,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Warp-collective store of 16 consecutive 32-bit columns of this warp's 32 TMEM lanes
-// (one lane per thread); returns after the store has completed.
 // One fp32 column of this thread's TMEM lane (store completes before returning).
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(__float_as_uint(v))
@@ -172,6 +141,7 @@ __device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
   return __uint_as_float(r);
 }
+// 16 consecutive fp32 columns of this thread's TMEM lane (store completes before returning).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
