@@ -166,6 +166,17 @@ size_t medusa_workspace_size(const medusa_plan* plan);
 /* Synchronises `stream`, returns the device status word in *flags and clears it.
  * MEDUSA_ERR_DEVICE when a flag was set, MEDUSA_OK otherwise. */
 medusa_status medusa_get_status(const medusa_plan* plan, void* stream, uint32_t* flags);
+/* Failure-path testing (the pages have no counterpart): the next verification-logit GEMM
+ * this plan launches (in medusa_step, medusa_step_layers, medusa_verify_logits or a
+ * decode loop captured after this call) has its MMA thread first wait, for at most `ns`
+ * nanoseconds, on a barrier that nothing arrives on.  The wait runs out and the kernel
+ * takes the path of a wait on a copy that never landed: it sets MEDUSA_FLAG_TIMEOUT,
+ * lets its other waits run to their own ~1 s limits, drains its copies in flight, frees
+ * its tensor memory and returns, so the call's outputs are meaningless but the CUDA
+ * context stays usable.  One-shot: the setting is cleared when that GEMM is launched.
+ * MEDUSA_ERR_INVALID for ns = 0 or above 10 s; MEDUSA_ERR_UNSUPPORTED for plans without
+ * the tensor-core projections (fp32). */
+medusa_status medusa_plan_expire_wait_once(medusa_plan* plan, unsigned long long ns);
 
 /* ------------------------------------------------------------------ full step */
 /* One decode step ([MEDUSA] §3.2 information flow, steps (2)-(6); [READING] section 3).
@@ -240,7 +251,9 @@ medusa_status medusa_heads(const medusa_plan* plan, const float* h, const int32_
  *   - Plans whose heads scratch exceeds the array (about B*(K+1)*V*4 bytes of logits plus
  *     small extras) get MEDUSA_ERR_UNSUPPORTED and nothing is launched.
  *   - The first call on a device looks up the array's address with that device current;
- *     make that first call before any stream capture begins.
+ *     make that first call before any stream capture begins.  The address is kept per
+ *     device and context; the first call after a cudaDeviceReset looks it up again and
+ *     must likewise come before any capture.
  *   - All calls share the array and it keeps the last call's contents (nothing in it
  *     needs to start at zero).  Calls whose GPU work overlaps race on it: order them on
  *     one stream. */

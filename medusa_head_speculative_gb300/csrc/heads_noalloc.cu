@@ -15,11 +15,14 @@
 //     MEDUSA_ERR_UNSUPPORTED before anything is launched.
 //   * The first call on a device looks up the array's device address (a CUDA runtime
 //     symbol lookup, no allocation) with that device current; make that first call
-//     before starting any stream capture.
+//     before starting any stream capture.  The address is kept per device and CUDA
+//     context: after cudaDeviceReset the next call looks it up again, so that call too
+//     should come before any capture.
 //   * Every call shares the one array and leaves its last contents there; nothing in it
 //     has to start at zero, since each call overwrites everything it reads.  Calls whose
 //     GPU work overlaps (different streams, or different plans at the same time) race on
 //     the array: order them on one stream.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -37,21 +40,49 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};     // device address of g_heads_scratch, per device
+struct ScratchAddr {
+  CUcontext ctx;      // the context the address was looked up in
+  void* ptr;          // device address of g_heads_scratch in that context
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
+
+// The calling thread's current CUDA context (null before the runtime has made one
+// current), through the driver entry point the runtime hands out.
+CUcontext current_context() {
+  using Fn = CUresult (*)(CUcontext*);
+  static Fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(p);
+  });
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
 
 // Host code must not use g_heads_scratch's name as an address: it is only a host-side
-// stand-in for the device symbol.  Look the real address up once per device.
+// stand-in for the device symbol.  The real address is looked up once per device and
+// context, and again when the current context is not the one it was found in (after a
+// cudaDeviceReset the runtime loads the module into a new primary context).
 medusa_status scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return MEDUSA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MEDUSA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  ScratchAddr& e = g_scratch[dev];
+  const CUcontext ctx = current_context();
+  if (!e.ptr || !ctx || ctx != e.ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_heads_scratch) != cudaSuccess || !p) return MEDUSA_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    e.ptr = p;
+    e.ctx = current_context();          // current now: the lookup made it so
   }
-  *out = g_scratch_ptr[dev];
+  *out = e.ptr;
   return MEDUSA_OK;
 }
 
