@@ -400,20 +400,22 @@ def rejection_walk(spec, tok, zv, T, uniforms):
 
     tok: [N+1] node tokens; zv: [N+1][V] verification logits; uniforms: [1 + 16 K].
     Returns (packed indices of the kept nodes root..last, the drawn next token, the
-    smallest decision margin in probability units)."""
+    decision margins in probability units: entry i is the smallest margin of the choice
+    made at kept node i, i.e. its children's tries and, at the last node, the draw)."""
     path = [0]
     u = 0
-    margin = math.inf
+    margins = []
     while True:
         p = softmax_T(zv[u], T)
         R = 1.0
         excluded = []
         nxt = None
+        here = math.inf
         d = len(path)                                  # depth of the children tried
         for j, c in enumerate(children(spec, u)):
             x = int(tok[c])
             uu = float(uniforms[1 + (d - 1) * 16 + j])
-            margin = min(margin, abs(uu * R - p[x]))
+            here = min(here, abs(uu * R - p[x]))
             if uu * R < p[x]:
                 nxt = c
                 break
@@ -423,7 +425,9 @@ def rejection_walk(spec, tok, zv, T, uniforms):
             w = p.copy()
             w[excluded] = 0.0
             v, mar = inverse_cdf_draw(w, float(uniforms[0]))
-            return np.array(path, dtype=np.int64), v, min(margin, mar)
+            margins.append(min(here, mar))
+            return np.array(path, dtype=np.int64), v, np.array(margins)
+        margins.append(here)
         path.append(nxt)
         u = nxt
 
@@ -459,6 +463,7 @@ class StepResult:
     root: int = 0
     root_margin: float = math.inf
     rs_margin: float = math.inf    # rejection sampling: smallest decision margin (R8)
+    rs_margins: np.ndarray = None  # rejection sampling: margin of the choice at each kept node
     tok: np.ndarray = None         # [N+1]
     pos: np.ndarray = None         # [N+1]
     q: np.ndarray = None           # [N+1][Hq][dh]
@@ -551,6 +556,19 @@ def medusa_step(wts, h, kc, vc, spec, dims, accept, root=None, s=None):
     return _verify(r, wts, spec, accept)
 
 
+def verify_only(wts, hp, tok, spec, accept):
+    """Steps (5)-(6) alone, from given layer outputs hp [N+1][d] and node tokens tok
+    [N+1]: the verification logits LM hp_n, acceptance, the kept path and the next root /
+    hidden state ([MEDUSA] §3.4 Tree Attention Step 6 and Typical Acceptance Scheme)."""
+    n1 = spec.N + 1
+    r = StepResult()
+    r.tok = np.asarray(tok, dtype=np.int64)
+    r.hp = f64(hp)
+    r.k = np.zeros((n1, 1))
+    r.v = np.zeros((n1, 1))
+    return _verify(r, wts, spec, accept)
+
+
 def _verify(r, wts, spec, accept):
     """Steps (5)-(6) from the layer outputs r.hp: verification logits, acceptance, the
     kept path, the next root / hidden state, and the kept nodes' keys/values (r.k, r.v)."""
@@ -566,8 +584,9 @@ def _verify(r, wts, spec, accept):
     T = accept.get("temperature", 0.0)
     if accept["mode"] == "reject" and T > 0.0:
         # R8: rejection sampling walks the tree with the given uniforms
-        r.path_nodes, r.root_next, r.rs_margin = rejection_walk(spec, r.tok, r.zv, T,
-                                                                accept["uniforms"])
+        r.path_nodes, r.root_next, r.rs_margins = rejection_walk(spec, r.tok, r.zv, T,
+                                                                 accept["uniforms"])
+        r.rs_margin = float(np.min(r.rs_margins))
         r.m = len(r.path_nodes) - 1
         r.acc = np.zeros(n1, dtype=np.int64)
         r.acc[r.path_nodes] = 1

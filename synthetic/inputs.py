@@ -215,6 +215,31 @@ def kv_cache(w: Workload, layer: int = 0):
     return kp, vp, pt
 
 
+def kv_cache_device(w: Workload, host_seqs, device):
+    """kv_cache built on `device` for caches too large to draw on the host in a test:
+    the sequences in host_seqs get their prefixes from the host streams (the values
+    kv_prefix gives the oracle); every other sequence's prefix is N(0, 1) drawn on the
+    device from a generator seeded with the workload's seed.  Contiguous layout only."""
+    if w.page_size:
+        raise ValueError("kv_cache_device: contiguous caches only")
+    cap, Hkv, dh = w.capacity, w.Hkv, w.dh
+    kc = torch.zeros((w.B, cap, Hkv, dh), dtype=w.torch_dtype, device=device)
+    vc = torch.zeros_like(kc)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed * 1000003 + _TAGS["kc"])
+    for b in range(w.B):
+        L = w.lengths[b]
+        if b in host_seqs:
+            k, v = kv_prefix(w, b)
+            kc[b, :L] = k.to(device)
+            vc[b, :L] = v.to(device)
+        else:
+            for t in (kc, vc):
+                t[b, :L] = torch.randn((L, Hkv, dh), generator=gen, device=device,
+                                       dtype=torch.float32).to(w.torch_dtype)
+    return kc, vc, None
+
+
 def score_table(K: int, smax: int) -> np.ndarray:
     """Fixed node-score table a_k^(i) (marginal top-i accuracy of head k), [K][smax].
 

@@ -10,7 +10,8 @@ import oracle as O
 import synthetic as S
 from medusa_head_speculative_gb300 import binding as Bnd
 
-from harness import NEAR, accept_of, close, oracle_accept, run_step, setup
+from harness import (NEAR, accept_of, affected_nodes, close, explain_by_flips, oracle_accept, record,
+                     run_step, setup)
 
 pytestmark = pytest.mark.gpu
 
@@ -66,15 +67,38 @@ def _cache_rows(w, kc, pt, b, t0, n):
     return torch.stack(rows).double().cpu().numpy()
 
 
-def _flagged(r, w, root_given):
-    """True when a decision the outputs depend on is a near tie in the oracle: the root,
-    a used top-s rank, a node's acceptance, or the greedy token at the last kept node."""
-    if not root_given and r.root_margin < NEAR:
+def _excusable(r, spec):
+    """Nodes whose accept flag may differ from the oracle's through a near tie (margin
+    below NEAR): a near-tie acceptance decision (in greedy mode: the parent's greedy
+    token), or a token that comes from a near-tie top-s rank, and every descendant of such
+    a node.  Returns a boolean mask over the packed nodes."""
+    bad_ranks = {(k, rk) for k in range(r.topk_margin.shape[0])
+                 for rk in range(r.topk_margin.shape[1]) if r.topk_margin[k, rk] < NEAR}
+    aff = affected_nodes(spec, bad_ranks)
+    return aff | (r.acc_margin < NEAR), aff
+
+
+def _compare_layers(g, r, b, spec):
+    """Outputs of sequence b against the oracle's n-layer step.  Returns True when compared
+    in full; False when the GPU's path differs from the oracle's only through near-tie
+    decisions (the path must then be the longest-path choice for flags that differ from
+    the oracle's at excusable nodes alone); AssertionError otherwise."""
+    n = int(g["n_acc"][b])
+    g_path = [int(x) for x in g["path"][b, :n]]
+    if g_path == [int(x) for x in r.path_nodes]:
+        assert list(g["out_tok"][b, :n]) == [int(t) for t in r.out_tok]
+        assert int(g["root_next"][b]) == r.root_next or r.am_margin[g_path[-1]] < NEAR
+        assert close(g["h_next"][b].cpu().numpy(), r.h_next) <= 0, "h_next"
         return True
-    if np.min(r.topk_margin[np.isfinite(r.topk_margin)], initial=np.inf) < NEAR:
-        return True
-    if np.min(r.acc_margin) < NEAR or r.am_margin[int(r.path_nodes[-1])] < NEAR:
-        return True
+    if g["out_tok"][b, 0] != r.out_tok[0]:
+        assert r.root_margin < NEAR, f"root {g['out_tok'][b, 0]} != {r.out_tok[0]}"
+        return False
+    exc, aff = _excusable(r, spec)
+    for l, node in enumerate(g_path):
+        if not aff[node]:
+            assert g["out_tok"][b, l] == r.tok[node], f"token of kept node {node}"
+    assert explain_by_flips(spec, r, g_path, exc), \
+        f"path {g_path} != {list(r.path_nodes)} and not explained by near-tie decisions"
     return False
 
 
@@ -94,20 +118,16 @@ def test_layers_step_matches_oracle(w, n_layers):
     olayers = [O.oracle_weights(c) for c in cpu]
     dims = {"Hq": w.Hq, "Hkv": w.Hkv, "dh": w.dh, "rope_base": w.rope_base}
     new_len = dev.length.cpu().numpy()
-    compared = 0
+    compared, flagged = 0, []
     for b in range(w.B):
         caches = [S.kv_prefix(w, b, l) for l in range(n_layers)]
         r = O.medusa_step_layers(ow, olayers, dev.cpu["h"][b], caches, dev.spec, dims,
                                  oracle_accept(w, b), s=list(w.s))
-        if _flagged(r, w, False):
-            continue
-        n = r.m + 1
-        assert g["n_acc"][b] == n
-        assert list(g["out_tok"][b, :n]) == [int(t) for t in r.out_tok]
-        assert list(g["path"][b, :n]) == [int(t) for t in r.path_nodes]
-        assert int(g["root_next"][b]) == r.root_next
-        assert close(g["h_next"][b].cpu().numpy(), r.h_next) <= 0, "h_next"
+        n = int(g["n_acc"][b])
         assert new_len[b] == lengths[b] + n
+        if not _compare_layers(g, r, b, dev.spec):
+            flagged.append((b, "near-tie decision"))
+            continue
         for l in range(n_layers):
             kn, vn = r.kv_new_layers[l]
             kg = _cache_rows(w, layers[l]["k"], dev.pt, b, lengths[b], n).reshape(kn.shape)
@@ -115,7 +135,8 @@ def test_layers_step_matches_oracle(w, n_layers):
             assert close(kg, kn) <= 0, f"layer {l} keys"
             assert close(vg, vn) <= 0, f"layer {l} values"
         compared += 1
-    assert compared >= 1
+    record(f"layers_{w.name}_{n_layers}", compared, flagged)
+    assert compared >= max(1, w.B - 1), flagged
 
 
 def test_one_layer_equals_medusa_step():

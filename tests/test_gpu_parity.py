@@ -12,7 +12,8 @@ import oracle as O
 import synthetic as S
 from medusa_head_speculative_gb300 import binding as Bnd
 
-from harness import (Flagged, close, compare_sequence, oracle_step, run_stages, run_step, setup)
+from harness import (Flagged, close, compare_sequence, oracle_step, record, run_stages, run_step,
+                     setup)
 
 pytestmark = pytest.mark.gpu
 
@@ -25,6 +26,12 @@ def _mid(**kw):
     return S.Workload(**base)
 
 
+_L13 = S.workload("vicuna13b").lengths
+_SHORT13, _LONG13 = int(np.argmin(_L13)), int(np.argmax(_L13))
+
+# name -> (workload, sampled sequences or None for all).  A sampled workload's other
+# sequences still run on the GPU (and the fused step must equal the stages on them); the
+# largest ones get their unsampled prefixes drawn on the device.
 CASES = {
     "tiny": (S.workload("tiny"), None),
     "mid_greedy": (_mid(), None),
@@ -45,29 +52,59 @@ CASES = {
     # rejection sampling with seeded uniforms (mostly draws at the root on random weights)
     "mid_reject": (_mid(mode="reject", temperature=0.8), None),
     "vicuna7b_reject": (S.workload("vicuna7b", mode="reject", temperature=0.7), None),
-    "vicuna13b": (S.workload("vicuna13b"), (0, 5)),
-    "zephyr7b": (S.workload("zephyr7b"), (3, 12)),
-    "vicuna33b_b4_l1024_n16": (S.vicuna33b(4, 1024, 16), (2,)),
-    # 2064 node rows: the clustered wide projections over many activation tiles, and
-    # two 128-row attention tiles (129 nodes x 1 query head per KV head)
-    "vicuna33b_b16_l1024_n128": (S.vicuna33b(16, 1024, 128), (5,)),
+    # four sampled sequences each, the 13B ones including its shortest and longest prefix
+    "vicuna13b": (S.workload("vicuna13b"), tuple(sorted({0, 5, _SHORT13, _LONG13}))),
+    "zephyr7b": (S.workload("zephyr7b"), (0, 3, 12, 15)),
+    # the Vicuna-33B-shaped sweep: two sampled sequences per point, from the smallest to
+    # the extreme corners (64 x 16K-token prefixes: the largest split counts and the
+    # longest TMA walks; 64 x 129 nodes = 8256 node rows over many activation tiles)
+    "vicuna33b_b4_l1024_n16": (S.vicuna33b(4, 1024, 16), (1, 2)),
+    "vicuna33b_b16_l1024_n128": (S.vicuna33b(16, 1024, 128), (5, 11)),
+    "vicuna33b_b64_l16384_n16": (S.vicuna33b(64, 16384, 16), (0, 63)),
+    "vicuna33b_b64_l1024_n128": (S.vicuna33b(64, 1024, 128), (7, 40)),
 }
+
+# KV caches above this many bytes get only the sampled sequences' prefixes from the host
+# streams; the rest are drawn on the device (sequences are independent, so they do not
+# change the sampled sequences' outputs)
+HOST_KV_LIMIT = 4 << 30
+
+
+def _kv_bytes(w):
+    return 2 * w.B * w.capacity * w.Hkv * w.dh * (4 if w.dtype == "f32" else 2)
+
+
+def _compare(dev, g, seqs, root=None):
+    """Compare the sampled sequences with the oracle; returns (compared, flagged)."""
+    ow = O.oracle_weights(dev.cpu["wts"])
+    compared, flagged = 0, []
+    for b in seqs:
+        r = oracle_step(dev, b, ow, root=None if root is None else int(root[b]))
+        try:
+            compare_sequence(g, r, b, dev.spec, dev.w, {}, root_given=root is not None)
+            compared += 1
+        except Flagged as e:
+            flagged.append((b, str(e)))
+    return compared, flagged
 
 
 def _check(name):
     w, sample = CASES[name]
-    dev = setup(w)
-    g = run_stages(dev)
-    ow = O.oracle_weights(dev.cpu["wts"])
     seqs = list(sample) if sample else list(range(w.B))
-    report, flagged = {}, []
-    for b in seqs:
-        r = oracle_step(dev, b, ow)
-        try:
-            compare_sequence(g, r, b, dev.spec, w, report)
-        except Flagged as e:
-            flagged.append((b, str(e)))
-    assert len(flagged) <= max(1, len(seqs) // 2), flagged
+    host_seqs = seqs if _kv_bytes(w) > HOST_KV_LIMIT else None
+    dev = setup(w, host_seqs=host_seqs)
+    g = run_stages(dev)
+    compared, flagged = _compare(dev, g, seqs)
+    if w.B == 1 and compared == 0:
+        # the only sequence hit a near tie: a second seed, so that one is compared in full
+        w2 = dataclasses.replace(w, seed=w.seed + 1)
+        dev2 = setup(w2)
+        c2, f2 = _compare(dev2, run_stages(dev2), seqs)
+        compared += c2
+        flagged += [(f"seed {w2.seed}", why) for _, why in f2]
+        del dev2
+    record(name, compared, flagged)
+    assert compared >= max(1, len(seqs) - 1), flagged
     # the fused step equals the chained stages exactly, and compacts the cache
     len_out = torch.empty_like(dev.length)
     s = run_step(dev, len_out=len_out)
@@ -78,28 +115,37 @@ def _check(name):
     np.testing.assert_array_equal(s["h_next"].cpu().numpy(), g["h_next"])
     np.testing.assert_array_equal(s["len_out"], np.array(w.lengths) + g["n_acc"])
     assert dev.plan.status() == 0
-    kc = _logical_cache(dev, dev.kc)
-    vc = _logical_cache(dev, dev.vc)
     for b in range(w.B):
         L, n = w.lengths[b], int(g["n_acc"][b])
+        kc = _seq_cache(dev, dev.kc, b, L, L + n)
+        vc = _seq_cache(dev, dev.vc, b, L, L + n)
         for l in range(n):
             node = g["path"][b, l]
-            np.testing.assert_array_equal(kc[b, L + l], g["tk"][b, node])
-            np.testing.assert_array_equal(vc[b, L + l], g["tv"][b, node])
-        k0, v0 = S.kv_prefix(w, b)
-        np.testing.assert_array_equal(kc[b, :L], k0.float().numpy())   # prefix untouched
-        assert not kc[b, L + n:].any()                                # nothing past the path
-    return g, report, flagged
+            np.testing.assert_array_equal(kc[l], g["tk"][b, node])
+            np.testing.assert_array_equal(vc[l], g["tv"][b, node])
+        if host_seqs is None or b in host_seqs:
+            k0, _ = S.kv_prefix(w, b)                                   # prefix untouched
+            np.testing.assert_array_equal(_seq_cache(dev, dev.kc, b, 0, L), k0.float().numpy())
+        assert not _seq_cache_any(dev, dev.kc, b, L + n)                 # nothing past the path
+    return g, flagged
 
 
-def _logical_cache(dev, t):
-    """[B][capacity][Hkv][dh] float view of the device cache (pages unscrambled)."""
+def _seq_rows(dev, t, b, t0, t1):
+    """Logical cache rows t0..t1-1 of sequence b as a device tensor (pages resolved)."""
     w = dev.w
-    x = t.float().cpu()
     if not w.page_size:
-        return x.numpy()
-    pt = dev.pt.cpu().long()
-    return x[pt].reshape(w.B, w.capacity, w.Hkv, w.dh).numpy()
+        return t[b, t0:t1]
+    slots = torch.arange(t0, t1, device=t.device)
+    pages = dev.pt[b].long()[slots // w.page_size]
+    return t[pages, slots % w.page_size]
+
+
+def _seq_cache(dev, t, b, t0, t1):
+    return _seq_rows(dev, t, b, t0, t1).float().cpu().numpy()
+
+
+def _seq_cache_any(dev, t, b, t0):
+    return bool(_seq_rows(dev, t, b, t0, dev.w.capacity).any())
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -118,16 +164,16 @@ def test_step_with_given_root(name):
     root_in = torch.from_numpy(roots).cuda()
     g = run_stages(dev, root_in=root_in)
     np.testing.assert_array_equal(g["root"], roots)
-    ow = O.oracle_weights(dev.cpu["wts"])
     seqs = list(sample) if sample else list(range(w.B))
-    report, flagged = {}, []
-    for b in seqs:
-        r = oracle_step(dev, b, ow, root=int(roots[b]))
-        try:
-            compare_sequence(g, r, b, dev.spec, w, report, root_given=True)
-        except Flagged as e:
-            flagged.append((b, str(e)))
-    assert len(flagged) <= max(1, len(seqs) // 2), flagged
+    compared, flagged = _compare(dev, g, seqs, root=roots)
+    if w.B == 1 and compared == 0:
+        dev2 = setup(dataclasses.replace(w, seed=w.seed + 1))
+        c2, f2 = _compare(dev2, run_stages(dev2, root_in=root_in), seqs, root=roots)
+        compared += c2
+        flagged += [(f"seed {w.seed + 1}", why) for _, why in f2]
+        del dev2
+    record(f"given_root_{name}", compared, flagged)
+    assert compared >= max(1, len(seqs) - 1), flagged
     s = run_step(dev, root_in=root_in, len_out=torch.empty_like(dev.length))
     np.testing.assert_array_equal(s["out_tok"], g["out_tok"])
     np.testing.assert_array_equal(s["path"], g["path"])

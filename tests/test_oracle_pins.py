@@ -494,3 +494,20 @@ def test_multi_layer_medusa_greedy_reproduces_sequential_greedy(planted, n_layer
         np.testing.assert_allclose(vc, vr[:len(vc)], rtol=1e-10, atol=1e-12)
     if planted:
         assert max(s.m for s in steps) >= 2
+
+
+def test_verify_only_equals_the_steps_verification():
+    """verify_only on a step's own layer outputs and tokens reproduces that step's
+    acceptance, path, next root and hidden state."""
+    w = S.workload("tiny", mode="typical", temperature=0.7)
+    wts = S.weights(w)
+    ow = O.oracle_weights(wts)
+    spec = O.cartesian_tree(w.s)
+    k, v = S.kv_prefix(w, 0)
+    dims = {"Hq": w.Hq, "Hkv": w.Hkv, "dh": w.dh, "rope_base": w.rope_base}
+    acc = {"mode": "typical", "temperature": 0.7, "eps": w.eps, "delta": w.delta}
+    r = O.medusa_step(ow, S.hidden(w)[0], k, v, spec, dims, acc, s=list(w.s))
+    q = O.verify_only(ow, r.hp, r.tok, spec, acc)
+    assert list(q.acc) == list(r.acc) and list(q.path_nodes) == list(r.path_nodes)
+    assert q.root_next == r.root_next and np.array_equal(q.h_next, r.h_next)
+    np.testing.assert_array_equal(q.zv, r.zv)
