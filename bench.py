@@ -1,12 +1,14 @@
 """Benchmark of one Medusa decode step (heads + top-s, tree build, tree attention through the
-synthetic layer, verification, acceptance, KV compaction) on the Vicuna-7B-shaped workload.
+synthetic layer, verification, acceptance, KV compaction) on the Vicuna-13B-shaped batch of 8
+(the headline), with the Vicuna-7B-shaped step and the Zephyr-7B-shaped GQA batch of 16
+measured into the same line under "workloads".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME]
+                    [--workload NAME] [--also NAME,NAME]
 
 Prints one JSON line.  `value` is whole-job decode steps per second with inputs resident in
 HBM; `e2e` is the same metric through the C ABI with the step's input copied from pinned
-host memory and its result read back every step.  Each step streams ~2.1 GB of weights,
+host memory and its result read back every step.  Each step streams > 1.8 GB of weights,
 far more than the 129 MB L2, so no L2 flush is needed between steps.  Under torchrun every
 rank runs an independent replica of the workload (sequences are independent: no
 collective on the data path); timing is the max over ranks.  `--impl reference` times the
@@ -461,7 +463,9 @@ def setup(w: S.Workload, device, planted: bool = False):
 
 
 def run_ours(args, w: S.Workload):
-    from medusa_head_speculative_gb300 import binding as Bnd
+    """The headline workload with every measurement, then the other workloads of
+    args.also (the step, its kernels, roofline, steady state, e2e and CPU baseline) as
+    sub-objects of the same line under "workloads"."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -471,6 +475,27 @@ def run_ours(args, w: S.Workload):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
+    res = measure(args, w, device, dist, world, rank, local, full=True)
+    torch.cuda.empty_cache()
+    subs = {}
+    for name in [x for x in args.also.split(",") if x and x != w.name]:
+        sub = measure(args, S.workload(name), device, dist, world, rank, local, full=False)
+        torch.cuda.empty_cache()
+        if sub is not None:
+            subs[name] = {k: v for k, v in sub.items()
+                          if k not in ("metric", "n_gpus", "higher_is_better", "scaling",
+                                       "vs_baseline", "data", "launch")}
+    if dist is not None:
+        dist.destroy_process_group()
+    if res is not None and subs:
+        res["workloads"] = subs
+    return res
+
+
+def measure(args, w: S.Workload, device, dist, world: int, rank: int, local: int, full: bool):
+    """One workload on this rank's GPU; the result dict on rank 0, None elsewhere.  With
+    full, also the decode loop, the multi-layer step and the tree-size measurement."""
+    from medusa_head_speculative_gb300 import binding as Bnd
     st = setup(w, device, planted=args.planted)
     plan = st["plan"]
     stream = torch.cuda.current_stream(device)
@@ -534,9 +559,9 @@ def run_ours(args, w: S.Workload):
     assert plan.status() == 0, "device status word set during the timed region"
     n_acc_mean = float(st["out"]["n_acc"].float().mean())
     steady = steady_state(args, w, st, stream, barrier)
-    loop = decode_loop(args, w, st, device)
-    mlayer = multi_layer(args, w, st, device, stream, barrier) if args.layers > 1 else None
-    tsize = tree_size(args, w, st, device, stream) if not args.no_tree_size else None
+    loop = decode_loop(args, w, st, device) if full else None
+    mlayer = multi_layer(args, w, st, device, stream, barrier) if full and args.layers > 1 else None
+    tsize = tree_size(args, w, st, device, stream) if full and not args.no_tree_size else None
 
     # end to end: h_t from pinned host memory, result (tokens, counts) back, every step
     ke = min(K, 500)
@@ -580,8 +605,6 @@ def run_ours(args, w: S.Workload):
                   tokens_per_s=round(whole_job_rate(world, steady["mean_tokens_per_step"] * w.B, steady_ms), 1))
 
     if rank != 0:
-        if dist is not None:
-            dist.destroy_process_group()
         return None
 
     n1 = plan.n1
@@ -656,10 +679,11 @@ def run_ours(args, w: S.Workload):
         "gpu_launches": int(launches),
         "launch": launch_mode,
     }
+    for k in ("decode_loop", "multi_layer", "tree_size"):
+        if res[k] is None:
+            del res[k]
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, st, plan_spec=(st["parent"], st["rank"]))
-    if dist is not None:
-        dist.destroy_process_group()
     return res
 
 
@@ -860,7 +884,10 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="vicuna7b")
+    ap.add_argument("--workload", default="vicuna13b",
+                    help="headline workload (default: the Vicuna-13B-shaped batch of 8)")
+    ap.add_argument("--also", default="vicuna7b,zephyr7b",
+                    help="further workloads measured into the same line ('' for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct calls, not a CUDA graph")
     ap.add_argument("--no-tree-size", action="store_true", help="skip the tree-size measurement")
