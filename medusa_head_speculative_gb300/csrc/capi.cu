@@ -443,7 +443,7 @@ medusa_status attn_impl(const medusa_plan* p, const float* q, const medusa_kv* k
   if (p->tc_attn) {
     bf16* qb = at<bf16>(ws, p->o_qb);
     if (!q_ready) LAUNCH(p, KN_QCAST, st, launch_to_bf16(q, qb, (long)p->M * d.Hq * d.dh, st));
-    LAUNCH(p, KN_ATTN, st, launch_tree_attention_tc(a, qb, st));
+    LAUNCH(p, KN_ATTN, st, launch_tree_attention_pp(a, qb, p->num_sms, st));
   } else {
     LAUNCH(p, KN_ATTN, st, launch_tree_attention(a, d.dtype, st));
   }
@@ -721,47 +721,38 @@ medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec
   // attention: query-row blocks and prefix splits so the grid covers the SMs ~2x
   const int G = dims->Hq / dims->Hkv;
   const int R = p->n1 * G;
-  p->tc_attn = tree_attention_tc_supported(dims->dtype, dims->dh, G, dims->page_size);
+  p->tc_attn = tree_attention_pp_supported(dims->dtype, dims->dh, G, dims->page_size);
   p->rpw = R <= 32 ? 4 : (R <= 72 ? 9 : 12);
   p->rows_per_block = p->tc_attn ? (R > 128 ? 256 : 128) : 8 * p->rpw;
   p->nrb = (R + p->rows_per_block - 1) / p->rows_per_block;
   const int base = dims->B * dims->Hkv * p->nrb;
   const int want = std::max(1, (2 * p->num_sms + base - 1) / base);
-  const int gran = p->tc_attn ? 64 : 32;              // keys per chunk of the kernel
+  const int gran = p->tc_attn ? 128 : 32;             // keys per chunk of the kernel
   const int max_splits = std::max(1, (dims->capacity + gran - 1) / gran);
   p->nsplit = std::min(want, max_splits);
   if (p->tc_attn) {
-    // One resident CTA per SM.  Cost in key-loads of one SM: the busiest SM's keys (each
-    // CTA also pays a fixed start-up of about three chunks), plus the partials that the
-    // splits write and the combine reads back, in the same units.  The busiest SM comes
-    // from assigning the CTAs, in launch order, to the SM that frees first; for grids of
-    // many rounds the even spread of the work is close enough.
+    // One persistent CTA per SM, CTA c taking units c, c + grid, ... (units split-major, the
+    // tree units last).  Cost in key loads of one SM: the busiest CTA's chunks (a unit also
+    // pays about four chunks' time for its query tile, the pipeline refill and its partial:
+    // measured at the 13B, Zephyr and 7B shapes), plus the partials that the splits write
+    // and the combine reads back, in the same units.
     const double key_bytes = 2.0 * dims->dh * 2;                 // one key's K and V
     const double part_bytes = 2.0 * dims->B * dims->Hq * p->n1 * (dims->dh * 4 + 8);
-    const long tree_keys = ((p->n1 + gran - 1) / gran + 3) * (long)gran;
+    const long tree_chunks = (p->n1 + gran - 1) / gran;
     double best = -1;
+    std::vector<long> load;
     for (int ns = 1; ns <= std::min(max_splits, 64); ++ns) {
       const long chunk = ((dims->capacity + ns - 1) / ns + gran - 1) / gran * gran;
-      const long keys = chunk + 3 * gran;
-      const long ctas = (long)base * (ns + 1);
-      double busiest;
-      if (ctas <= 16L * p->num_sms) {
-        std::priority_queue<long, std::vector<long>, std::greater<long>> free_at;
-        for (int i = 0; i < p->num_sms; ++i) free_at.push(0);
-        long end = 0;
-        for (long c = 0; c < ctas; ++c) {
-          const int split = (int)(c % (ns + 1));
-          const long start = free_at.top();
-          free_at.pop();
-          const long done = start + (split == ns ? tree_keys : keys);
-          end = std::max(end, done);
-          free_at.push(done);
-        }
-        busiest = (double)end;
-      } else {
-        busiest = std::max(((double)base * ns * keys + (double)base * tree_keys) / p->num_sms,
-                           (double)keys);
+      const long nsp = (dims->capacity + chunk - 1) / chunk;      // splits that exist
+      if (nsp != ns) continue;
+      const long units = (long)base * (ns + 1);
+      const long grid = std::min<long>(units, p->num_sms);
+      load.assign(grid, 0);
+      for (long u = 0; u < units; ++u) {
+        const bool tree = u / base == ns;
+        load[u % grid] += (tree ? tree_chunks : chunk / gran) + 4;
       }
+      const double busiest = (double)*std::max_element(load.begin(), load.end()) * gran;
       const double cost = busiest + (ns + 1) * part_bytes / (p->num_sms * key_bytes);
       if (best < 0 || cost < best) { best = cost; p->nsplit = ns; }
     }

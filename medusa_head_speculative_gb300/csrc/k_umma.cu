@@ -358,11 +358,13 @@ __global__ void __launch_bounds__(128, 2) umma_gemm_kernel(const __grid_constant
 // For hundreds to thousands of activation rows (the node projections at batch > 1) the
 // 128 x nbox tiles above re-read their operands from L2 faster than the tensor cores use
 // them.  Here a CTA owns 256 weight rows (two 128-row accumulators in TMEM) against up to
-// 256 activation rows: per stage it reads 32 KB of weights and the activation tile for
-// twice the MMA work of a 128-row tile.  CTAs of neighbouring weight tiles read the same
-// activation tiles, which L2 serves after the first read.
+// 256 activation rows, for twice the MMA work of a 128-row tile per operand byte.  With
+// fp32 activations (bf16 hi + lo tiles) a stage is 32 columns of K with the 64-byte
+// swizzle, so the ring holds 4-5 stages instead of 2 and the tensor cores do not wait on
+// L2; with bf16 activations it stays at 64 columns with the 128-byte swizzle (3-4 stages,
+// and half as many ring hand-offs per MMA).  CTAs of neighbouring weight tiles read the
+// same activation tiles, which L2 serves after the first read.
 constexpr int UW_R = 256;                    // weight rows per CTA
-constexpr uint32_t UW_W_BYTES = UW_R * 128;  // one 64-column stage of them
 
 struct UmmaWideArgs {
   CUtensorMap tw[kMaxSeg];   // weights of each segment: dims {k, rows}, box {64, 256}
@@ -375,12 +377,13 @@ struct UmmaWideArgs {
   uint32_t* status;
 };
 
-template <bool HAS_LO>
+template <bool HAS_LO, int UW_K>
 __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant__ UmmaWideArgs g) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[2 * 8 + 2];
   __shared__ uint32_t tmem_slot;
   __shared__ int s_issued, s_consumed, s_bad;
+  constexpr uint32_t UW_W_BYTES = UW_R * UW_K * 2;    // one stage of weights
   const MatArgs& a = g.m;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int si = 0;
@@ -390,11 +393,11 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
   const int rows_here = min(UW_R, s.rows - rbase);
   const int nacc = rows_here > 128 ? 2 : 1;
   const int m0 = (int)blockIdx.x * g.nbox;
-  const int nk = (a.k + UM_K - 1) / UM_K;
+  const int nk = (a.k + UW_K - 1) / UW_K;
   const int kt0 = (int)((long)blockIdx.z * nk / g.ksplit);
   const int nkl = (int)((long)(blockIdx.z + 1) * nk / g.ksplit) - kt0;
   const int S = g.stages;
-  const uint32_t A_BYTES = (uint32_t)g.nbox * 128;
+  const uint32_t A_BYTES = (uint32_t)g.nbox * UW_K * 2;
   const uint32_t STAGE = UW_W_BYTES + A_BYTES * (HAS_LO ? 2 : 1);
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t bar0 = smem_u32(bars);
@@ -430,14 +433,14 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
     const int pre = nkl < S ? nkl : S;
     for (int j = 0; j < pre; ++j) {
       mbar_expect_tx(full(j), stage_tx);
-      tma_load_2d(base + j * STAGE, &g.tw[si], (kt0 + j) * UM_K, rbase, full(j), pw);
+      tma_load_2d(base + j * STAGE, &g.tw[si], (kt0 + j) * UW_K, rbase, full(j), pw);
     }
     pdl_wait();
     const CUtensorMap* tw = &g.tw[si];
     int j = 0, st = 0;
     uint32_t ph = 0;                                    // phase of the ring's current pass
     for (; j < nkl; ++j) {
-      const int kx = (kt0 + j) * UM_K;
+      const int kx = (kt0 + j) * UW_K;
       const uint32_t ws = base + st * STAGE;
       if (j >= pre) {
         if (!mbar_wait(empty(st), ph ^ 1, TC_TIMEOUT_NS)) { timed_out = true; break; }
@@ -453,8 +456,9 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
   } else if (warp == 1 && lane == 0) {                  // ---- MMA issuer
     const uint32_t idesc = idesc_bf16(128, g.nbox);
     // descriptors of stage 0; stage st adds st * STAGE bytes to the start address field
-    const uint64_t a0 = sw128_desc(base), a1 = sw128_desc(base + UM_W_BYTES);
-    const uint64_t b0 = sw128_desc(base + UW_W_BYTES), l0 = sw128_desc(base + UW_W_BYTES + A_BYTES);
+    auto desc = [](uint32_t at) { return UW_K == 32 ? sw64_desc(at) : sw128_desc(at); };
+    const uint64_t a0 = desc(base), a1 = desc(base + UW_W_BYTES / 2);
+    const uint64_t b0 = desc(base + UW_W_BYTES), l0 = desc(base + UW_W_BYTES + A_BYTES);
     const uint64_t dstep = STAGE >> 4;
     const uint32_t d1 = tmem + g.acc_stride;
     int j = 0, st = 0;
@@ -469,7 +473,7 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
       {
         const uint64_t ad = a0 + off;
 #pragma unroll
-        for (int ks = 0; ks < UM_K / 16; ++ks) {
+        for (int ks = 0; ks < UW_K / 16; ++ks) {
           umma_bf16(tmem, ad + 2 * ks, bd + 2 * ks, idesc, (j | ks) != 0);
           if (HAS_LO) umma_bf16(tmem, ad + 2 * ks, ld + 2 * ks, idesc, 1);
         }
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
       if (nacc > 1) {
         const uint64_t ad = a1 + off;
 #pragma unroll
-        for (int ks = 0; ks < UM_K / 16; ++ks) {
+        for (int ks = 0; ks < UW_K / 16; ++ks) {
           umma_bf16(d1, ad + 2 * ks, bd + 2 * ks, idesc, (j | ks) != 0);
           if (HAS_LO) umma_bf16(d1, ad + 2 * ks, ld + 2 * ks, idesc, 1);
         }
@@ -588,16 +592,19 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D bf16 tensor map: `rows` rows of `cols` elements at `ld` elements apart; box
-// {64, box_rows}, 128-byte swizzle, zero fill out of bounds.
-static bool make_map(CUtensorMap* map, const void* ptr, long cols, long rows, long ld, int box_rows) {
+// {64, box_rows} with the 128-byte swizzle (box_cols 64) or {32, box_rows} with the
+// 64-byte swizzle (box_cols 32), zero fill out of bounds.
+static bool make_map(CUtensorMap* map, const void* ptr, long cols, long rows, long ld, int box_rows,
+                     int box_cols = UM_K) {
   auto fn = encode_fn();
   if (!fn || !ptr) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {(cuuint32_t)UM_K, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -633,28 +640,29 @@ static cudaError_t launch_umma_wide(const MatArgs& m, uint32_t* status, int num_
   for (int i = 0; i < a.nseg; ++i) a.tile_off[i + 1] = a.tile_off[i] + (a.seg[i].rows + UW_R - 1) / UW_R;
   g.wtiles = a.tile_off[a.nseg];
   const bool has_lo = a.seg[0].a_lo != nullptr;
+  const int UW_K = has_lo ? 32 : 64;                  // K per stage, see the kernel
   // activation tiles of <= 256 rows, as even as the count allows (multiple of 16)
   const int nct = (a.M + 255) / 256;
   g.nbox = ((a.M + nct - 1) / nct + 15) / 16 * 16;
   g.acc_stride = g.nbox > 128 ? 256 : 128;            // two accumulators of nbox columns
   g.tmem_cols = 2 * g.acc_stride;
-  const uint32_t stage = UW_W_BYTES + (uint32_t)g.nbox * 128 * (has_lo ? 2 : 1);
+  const uint32_t stage = (uint32_t)(UW_R + g.nbox * (has_lo ? 2 : 1)) * UW_K * 2;
   int stages = (int)((220u * 1024u) / stage);
-  g.stages = stages > 6 ? 6 : stages;
+  g.stages = stages > 8 ? 8 : stages;
   if (g.stages < 2) return cudaErrorInvalidValue;
   g.status = status;
-  const int nk = (a.k + UM_K - 1) / UM_K;
+  const int nk = (a.k + UW_K - 1) / UW_K;
   g.ksplit = choose_ksplit(a, (long)nct * g.wtiles, nk, num_sms, 1);
   g.kpart = a.kpart;
   for (int i = 0; i < a.nseg; ++i)
-    if (!make_map(&g.tw[i], a.seg[i].w, a.k, a.seg[i].rows, a.k, UW_R)) return cudaErrorInvalidValue;
-  if (!make_map(&g.ta, a.seg[0].a_hi, a.k, a.M, a.seg[0].ldx, g.nbox)) return cudaErrorInvalidValue;
-  if (has_lo && !make_map(&g.tl, a.seg[0].a_lo, a.k, a.M, a.seg[0].ldx, g.nbox)) return cudaErrorInvalidValue;
+    if (!make_map(&g.tw[i], a.seg[i].w, a.k, a.seg[i].rows, a.k, UW_R, UW_K)) return cudaErrorInvalidValue;
+  if (!make_map(&g.ta, a.seg[0].a_hi, a.k, a.M, a.seg[0].ldx, g.nbox, UW_K)) return cudaErrorInvalidValue;
+  if (has_lo && !make_map(&g.tl, a.seg[0].a_lo, a.k, a.M, a.seg[0].ldx, g.nbox, UW_K)) return cudaErrorInvalidValue;
   // at least 116 KB of shared memory keeps one CTA per SM, so the 512-column TMEM
   // allocations of co-resident CTAs never wait on each other
   size_t smem = (size_t)g.stages * stage + 1024;
   if (smem < 116u * 1024u) smem = 116u * 1024u;
-  auto kern = has_lo ? umma_wide_kernel<true> : umma_wide_kernel<false>;
+  auto kern = has_lo ? umma_wide_kernel<true, 32> : umma_wide_kernel<false, 64>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = launch_kernel(kern, dim3(nct, g.wtiles, g.ksplit), dim3(128), smem, st, 1, g);

@@ -148,11 +148,12 @@ struct AttnArgs {
 };
 cudaError_t launch_tree_attention(const AttnArgs& a, int dtype, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnArgs& a, cudaStream_t st);
-// Tensor-core tree attention (bf16, dh 64/128, G | 128, page size 8..64 dividing 64):
-// rows_per_block must be 128 or 256 (two query tiles sharing the K/V tiles) and chunk a
-// multiple of 64.  q_bf16: [B*n1][Hq][dh].
-bool tree_attention_tc_supported(int dtype, int dh, int G, int page_size);
-cudaError_t launch_tree_attention_tc(const AttnArgs& a, const void* q_bf16, cudaStream_t st);
+// Persistent tensor-core tree attention (bf16, dh 64/128, G | 128, page size 8..128
+// dividing 128): rows_per_block 128 or 256, chunk a multiple of 128; one CTA per SM at
+// most (num_sms), each walking a fixed stride of the (split, KV head, sequence, row block)
+// units.  q_bf16: [B*n1][Hq][dh].
+bool tree_attention_pp_supported(int dtype, int dh, int G, int page_size);
+cudaError_t launch_tree_attention_pp(const AttnArgs& a, const void* q_bf16, int num_sms, cudaStream_t st);
 // fp32 -> bf16 (round to nearest) of n elements.
 cudaError_t launch_to_bf16(const float* x, __nv_bfloat16* y, long n, cudaStream_t st);
 

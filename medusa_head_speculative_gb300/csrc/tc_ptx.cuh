@@ -173,6 +173,16 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   d |= (uint64_t)2 << 61;                             // 128-byte swizzle
   return d;
 }
+// The same for a K-major tile with the 64-byte swizzle: rows of 64 bytes, 8-row groups
+// 512 bytes apart (tile base 1024-byte aligned).
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;                             // 64-byte swizzle
+  return d;
+}
 // Instruction descriptor, kind::f16: fp32 D, bf16 A and B, both K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
