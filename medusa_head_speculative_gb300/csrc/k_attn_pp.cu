@@ -8,12 +8,13 @@
 // Here one CTA per SM walks a fixed stride of the units, so the K/V stream of the SM never
 // stops for a CTA launch, and keys go in chunks of 128:
 //
-//   warp 8 (one lane)  TMA: per unit the query tile(s), then the K and V chunks through two
-//                      rings of 2 to 4 stages that run on across units: a K stage is freed
-//                      as soon as its S products are done, a V stage after its P V
-//                      products (paged caches: one box per page; the warp reads 32 page
-//                      ids at once)
-//   warp 9 (one lane)  MMAs for two "slots", each with S (128 columns) and O (dh columns)
+//   warps 8-10         producers: per unit the query tile(s) (warp 8, TMA), then the K and
+//                      V chunks through two rings of 2 to 4 stages that run on across
+//                      units: a K stage is freed as soon as its S products are done, a V
+//                      stage after its P V products.  Contiguous caches and the tree keys
+//                      come by TMA (warp 8); a paged cache is copied by all three warps
+//                      with cp.async (each reads 32 page ids at once)
+//   warp 11 (one lane) MMAs for two "slots", each with S (128 columns) and O (dh columns)
 //                      in tensor memory: S = Q K^T, then O += P V with P read from tensor
 //                      memory (the A operand), V from shared memory (MN-major)
 //   warps 0-3, 4-7     two softmax warpgroups, one per slot, one query row per thread:
@@ -47,7 +48,9 @@ namespace medusa {
 constexpr int PP_ROWS = 128;     // query rows per tile (MMA M, TMEM lanes)
 constexpr int PP_KEYS = 128;     // keys per chunk
 constexpr int PP_MAXST = 4;      // K/V ring depth at most
-constexpr int PP_THREADS = 320;  // 8 softmax warps, TMA warp, MMA warp
+constexpr int PP_PROD = 3;       // producer warps (all three copy a paged cache)
+constexpr int PP_MMA_WARP = 8 + PP_PROD;
+constexpr int PP_THREADS = (PP_MMA_WARP + 1) * 32;   // 8 softmax warps, producers, MMA warp
 constexpr float PP_LAZY = 8.f;   // log2 headroom before O is rescaled
 constexpr uint32_t PP_SLOT_COLS = 256;   // per slot: S [0, 128), O [128, 128 + dh)
 
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(PP_THREADS, 1) tree_attn_pp_kernel(const __gri
     mbar_init(bar(PB_QE), 1);
     // paged caches: every lane of the producer warp arrives on a full stage (its own
     // copies, or a plain arrive next to lane 0's expected bytes for a TMA stage)
-    const uint32_t fcount = a.page_table ? 32 : 1;
+    const uint32_t fcount = a.page_table ? 32 * PP_PROD : 1;
     for (int i = 0; i < SK; ++i) {
       mbar_init(bar(PB_KF + i), fcount);
       mbar_init(bar(PB_KE + i), 1);
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(PP_THREADS, 1) tree_attn_pp_kernel(const __gri
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 9) tmem_alloc(smem_u32(&tmem_slot), 2 * PP_SLOT_COLS);
+  if (warp == PP_MMA_WARP) tmem_alloc(smem_u32(&tmem_slot), 2 * PP_SLOT_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -188,8 +191,11 @@ __global__ void __launch_bounds__(PP_THREADS, 1) tree_attn_pp_kernel(const __gri
   bool timed_out = false;
   auto aborted = [&]() { return *(volatile int*)&s_abort != 0; };
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp >= 8 && warp < PP_MMA_WARP && (warp == 8 || a.page_table)) {
+    // ------------------------------------------------------------ producers
+    // Warp 8 loads the query tiles and issues every copy-engine load; with a paged cache
+    // all producer warps copy prefix chunks (and arrive on each stage).
+    const int pw = warp - 8;
     const uint64_t pol_kv = policy_evict_first(), pol_q = policy_evict_last();
     int gc = 0, qn = 0;                   // chunks and query tiles issued so far
     bool first = true;
@@ -200,7 +206,7 @@ __global__ void __launch_bounds__(PP_THREADS, 1) tree_attn_pp_kernel(const __gri
       const int nta = nt == 2 ? (row0 + PP_ROWS < R ? 2 : 1) : 1;
       // The cached prefix is written by no kernel of this call: the first unit's first
       // K/V chunks go out before the wait for earlier kernels, its query tile after.
-      const int pre = first ? (w.tree ? 0 : min(w.nch, min(SK, SV))) : 0;
+      const int pre = first && pw == 0 ? (w.tree ? 0 : min(w.nch, min(SK, SV))) : 0;
       const bool paged = !w.tree && a.page_table;
       // Page ids of a 32-page window starting at p0 (lane l holds page l), refreshed when a
       // chunk leaves it.  All lanes.
@@ -219,6 +225,7 @@ __global__ void __launch_bounds__(PP_THREADS, 1) tree_attn_pp_kernel(const __gri
         }
       };
       auto load_q = [&]() -> bool {
+        if (pw != 0) return true;
         if (first) pdl_wait();
         first = false;
         bool ok = true;
@@ -255,13 +262,13 @@ __global__ void __launch_bounds__(PP_THREADS, 1) tree_attn_pp_kernel(const __gri
           const uint32_t dst = (part == 0 ? k0s : v0s) + st * KV_CHUNK;
           if (paged) {
             // Paged prefix: a page holds only 16 rows of a head, so copy-engine boxes would
-            // be small and many; the warp copies the chunk itself, 16 bytes per cp.async,
-            // lane l taking rows l, l + 32, ..., into the 128-byte-swizzled layout, and
-            // each lane's arrive fires once its own copies have landed.
+            // be small and many; the producer warps copy the chunk themselves, 16 bytes per
+            // cp.async into the 128-byte-swizzled layout (warp pw takes the 32-row groups
+            // pw, pw + 3, ...; lane l row l of a group), and each thread's arrive fires once
+            // its own copies have landed.
             const char* src = static_cast<const char*>(part == 0 ? a.kc : a.vc);
-#pragma unroll
-            for (int rr = 0; rr < PP_KEYS / 32; ++rr) {
-              const int r = lane + 32 * rr, t = t0 + r;
+            for (int grp = pw; grp < PP_KEYS / 32; grp += PP_PROD) {
+              const int r = lane + 32 * grp, t = t0 + r;
               const int pg = __shfl_sync(0xffffffffu, my_page, min((t - pref0) / a.page_size, 31));
               const bool in = t < a.capacity;
               const char* row = src + (((long)pg * a.page_size + t % a.page_size) * a.Hkv + w.g) * (long)(DH * 2);
@@ -272,13 +279,13 @@ __global__ void __launch_bounds__(PP_THREADS, 1) tree_attn_pp_kernel(const __gri
               }
             }
             asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar(full)) : "memory");
-            if (lane == 0) {
+            if (pw == 0 && lane == 0) {
               if (part == 0) s_kiss = c + 1;
               else s_viss = c + 1;
             }
             continue;
           }
-          if (lane != 0) {
+          if (pw != 0 || lane != 0) {
             if (a.page_table) mbar_arrive(bar(full));    // the tree keys of a paged launch
             continue;
           }
@@ -304,8 +311,8 @@ __global__ void __launch_bounds__(PP_THREADS, 1) tree_attn_pp_kernel(const __gri
       gc += w.nch;
       if (aborted()) break;
     }
-    if (first) pdl_wait();
-  } else if (warp == 9) {
+    if (first && pw == 0) pdl_wait();
+  } else if (warp == PP_MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16(PP_ROWS, PP_KEYS);
@@ -422,7 +429,7 @@ __global__ void __launch_bounds__(PP_THREADS, 1) tree_attn_pp_kernel(const __gri
       timed_out = dead;
       umma_commit(bar(PB_END));           // arrives once every MMA issued above is done
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax warpgroups
     const int slot = warp >> 2, wl = warp & 3;
     const int r = wl * 32 + lane;                    // row within the tile = TMEM lane
@@ -628,7 +635,7 @@ __global__ void __launch_bounds__(PP_THREADS, 1) tree_attn_pp_kernel(const __gri
     for (int c = s_vwait; c < s_viss; ++c) mbar_wait(bar(PB_VF + c % SV), (c / SV) & 1, TC_TIMEOUT_NS / 16);
   }
   __syncthreads();
-  if (warp == 9) tmem_dealloc(tmem, 2 * PP_SLOT_COLS);
+  if (warp == PP_MMA_WARP) tmem_dealloc(tmem, 2 * PP_SLOT_COLS);
 }
 
 // ------------------------------------------------------------------ host side
