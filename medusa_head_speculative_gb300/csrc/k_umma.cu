@@ -52,7 +52,7 @@ __device__ __forceinline__ void epilogue4(const MatArgs& a, const MatSeg& s, int
   float y[4] = {v.x, v.y, v.z, v.w};
   const int n = min(4, s.rows - r);
   if (kpart_row) {                                      // raw partial sum of a K range
-    float* kp = kpart_row + s.out_off + r;
+    float* kp = kpart_row + s.out_off + r - a.kp_c0;
     if (n == 4 && aligned16(kp)) *reinterpret_cast<float4*>(kp) = v;
     else for (int e = 0; e < n; ++e) kp[e] = y[e];
     return;
@@ -220,7 +220,7 @@ __device__ void staged_epilogue(const MatArgs& a, const MatSeg& s, int rbase, in
         const int m = m0 + c0 + ml, r = rbase + 4 * q;
         if (m < a.M && r < s.rows) {
           const float4 v = *reinterpret_cast<const float4*>(stage + ml * rt + 4 * q);
-          epilogue4(a, s, m, r, v, kpart ? kpart + ((long)blockIdx.z * a.M + m) * a.ldo : nullptr);
+          epilogue4(a, s, m, r, v, kpart ? kpart + ((long)blockIdx.z * a.M + m) * a.kp_ld : nullptr);
         }
       }
     }
@@ -370,7 +370,8 @@ struct UmmaWideArgs {
   CUtensorMap tw[kMaxSeg];   // weights of each segment: dims {k, rows}, box {64, 256}
   CUtensorMap ta, tl;        // activations (hi, lo), shared by all segments: box {64, nbox}
   MatArgs m;                 // tile_off counts 256-row tiles
-  int wtiles;                // weight tiles (grid.y)
+  int wtiles;                // weight tiles of the launch (grid.y), from tile wt0 on
+  int wt0;
   int nbox, stages, ksplit;
   float* kpart;
   uint32_t tmem_cols, acc_stride;
@@ -386,10 +387,11 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
   constexpr uint32_t UW_W_BYTES = UW_R * UW_K * 2;    // one stage of weights
   const MatArgs& a = g.m;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wtile = (int)blockIdx.y + g.wt0;
   int si = 0;
-  while (si + 1 < a.nseg && (int)blockIdx.y >= a.tile_off[si + 1]) ++si;
+  while (si + 1 < a.nseg && wtile >= a.tile_off[si + 1]) ++si;
   const MatSeg& s = a.seg[si];
-  const int rbase = ((int)blockIdx.y - a.tile_off[si]) * UW_R;
+  const int rbase = (wtile - a.tile_off[si]) * UW_R;
   const int rows_here = min(UW_R, s.rows - rbase);
   const int nacc = rows_here > 128 ? 2 : 1;
   const int m0 = (int)blockIdx.x * g.nbox;
@@ -523,18 +525,19 @@ __global__ void splitk_reduce_kernel(const MatArgs a, const float* __restrict__ 
   constexpr int ZMAX = 8;
   pdl_trigger();
   pdl_wait();
+  const long kld = a.kp_ld;
   if (a.epi == EPI_ROPE) {
     // one item = 4 columns of the first half of a head and their partners dh/2 further on
     const int dh = a.rope_dh, half = dh / 2, gh = half / 4;
-    const int per_row = (int)(a.ldo / dh) * gh;
+    const int per_row = (cols / dh) * gh;
     const long n = (long)a.M * per_row;
     for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
       const int m = (int)(i / per_row), rem = (int)(i - (long)m * per_row), hg = rem / gh;
-      const int c0 = hg * dh + 4 * (rem - hg * gh);
+      const int c0 = hg * dh + 4 * (rem - hg * gh);           // column within the partials
       float4 v0[ZMAX], v1[ZMAX];
 #pragma unroll
       for (int z = 0; z < ZMAX; ++z) {
-        const float* row = kpart + ((long)z * a.M + m) * a.ldo;
+        const float* row = kpart + ((long)z * a.M + m) * kld;
         v0[z] = z < ksplit ? __ldcg(reinterpret_cast<const float4*>(row + c0)) : make_float4(0.f, 0.f, 0.f, 0.f);
         v1[z] = z < ksplit ? __ldcg(reinterpret_cast<const float4*>(row + c0 + half)) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
@@ -544,7 +547,7 @@ __global__ void splitk_reduce_kernel(const MatArgs a, const float* __restrict__ 
         s0.x += v0[z].x; s0.y += v0[z].y; s0.z += v0[z].z; s0.w += v0[z].w;
         s1.x += v1[z].x; s1.y += v1[z].y; s1.z += v1[z].z; s1.w += v1[z].w;
       }
-      rope4(a, m, c0, s0, s1);
+      rope4(a, m, a.kp_c0 + c0, s0, s1);
     }
     return;
   }
@@ -555,7 +558,7 @@ __global__ void splitk_reduce_kernel(const MatArgs a, const float* __restrict__ 
     float4 v[ZMAX];
 #pragma unroll
     for (int z = 0; z < ZMAX; ++z)
-      v[z] = z < ksplit ? __ldcg(reinterpret_cast<const float4*>(kpart + ((long)z * a.M + m) * a.ldo + c))
+      v[z] = z < ksplit ? __ldcg(reinterpret_cast<const float4*>(kpart + ((long)z * a.M + m) * kld + c))
                         : make_float4(0.f, 0.f, 0.f, 0.f);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -567,9 +570,9 @@ __global__ void splitk_reduce_kernel(const MatArgs a, const float* __restrict__ 
     }
     const float4 y = make_float4(acc[0], acc[1], acc[2], acc[3]);
     if (a.nseg == 1) {
-      epilogue4(a, a.seg[0], m, c, y, nullptr);
+      epilogue4(a, a.seg[0], m, a.kp_c0 + c, y, nullptr);
     } else {
-      float* op = a.out + (long)m * a.ldo + c;
+      float* op = a.out + (long)m * a.ldo + a.kp_c0 + c;
       if (aligned16(op)) *reinterpret_cast<float4*>(op) = y;
       else for (int e = 0; e < 4; ++e) op[e] = acc[e];
     }
@@ -608,8 +611,9 @@ static bool make_map(CUtensorMap* map, const void* ptr, long cols, long rows, lo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static cudaError_t launch_splitk_reduce(const MatArgs& a, int ksplit, cudaStream_t st) {
-  const int ncols = a.nseg == 1 ? a.seg[0].rows : (int)a.ldo;
+// Sums the partials of output columns kp_c0 .. kp_c0 + ncols - 1 and applies the epilogue.
+static cudaError_t launch_splitk_reduce(const MatArgs& a, int ksplit, cudaStream_t st, int ncols = -1) {
+  if (ncols < 0) ncols = a.nseg == 1 ? a.seg[0].rows : (int)a.ldo;
   const long n4 = (long)a.M * (ncols / 4);
   const long blocks = (n4 + 255) / 256;
   return launch_kernel(splitk_reduce_kernel, dim3((unsigned)(blocks < 8192 ? blocks : 8192)), dim3(256), 0, st,
@@ -636,6 +640,8 @@ static cudaError_t launch_umma_wide(const MatArgs& m, uint32_t* status, int num_
   std::memset(&g, 0, sizeof(g));
   g.m = m;
   MatArgs& a = g.m;
+  a.kp_ld = a.ldo;                                    // a split of the whole output
+  a.kp_c0 = 0;
   a.tile_off[0] = 0;
   for (int i = 0; i < a.nseg; ++i) a.tile_off[i + 1] = a.tile_off[i] + (a.seg[i].rows + UW_R - 1) / UW_R;
   g.wtiles = a.tile_off[a.nseg];
@@ -665,6 +671,39 @@ static cudaError_t launch_umma_wide(const MatArgs& m, uint32_t* status, int num_
   auto kern = has_lo ? umma_wide_kernel<true, 32> : umma_wide_kernel<false, 64>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  // A grid of more than one but not a whole number of waves (one CTA per SM) leaves the
+  // last wave partly empty.  Then the weight tiles of the whole waves run as they are, and
+  // the remaining ones split K so that their CTAs fill one more wave: their partials (for
+  // their own output columns only) are summed by the reduce, which applies the epilogue.
+  const long tiles = (long)nct * g.wtiles;
+  const bool splittable = a.nseg == 1 || (a.epi == EPI_STORE && !a.out_hi) || a.epi == EPI_ROPE;
+  if (g.ksplit == 1 && splittable && a.kpart && tiles > num_sms && tiles % num_sms != 0) {
+    const int w1 = (int)((tiles / num_sms) * num_sms / nct);     // weight tiles of the whole waves
+    const int tail = g.wtiles - w1;
+    int si = 0;
+    while (si + 1 < a.nseg && w1 >= a.tile_off[si + 1]) ++si;
+    const int c0 = a.seg[si].out_off + (w1 - a.tile_off[si]) * UW_R;   // first output column of the tail
+    const int c1 = a.nseg == 1 ? a.seg[0].rows : (int)a.ldo;
+    int ks = (int)(num_sms / ((long)tail * nct));
+    ks = ks > 8 ? 8 : ks;
+    ks = ks > nk / 4 ? nk / 4 : ks;
+    while (ks > 1 && (size_t)ks * a.M * (c1 - c0) * sizeof(float) > a.kpart_bytes) --ks;
+    if (w1 > 0 && tail > 0 && ks >= 2 && (c1 - c0) % 4 == 0) {
+      UmmaWideArgs gm = g;
+      gm.wtiles = w1;
+      gm.wt0 = 0;
+      e = launch_kernel(kern, dim3(nct, w1, 1), dim3(128), smem, st, 1, gm);
+      if (e != cudaSuccess) return e;
+      g.wtiles = tail;
+      g.wt0 = w1;
+      g.ksplit = ks;
+      a.kp_c0 = c0;
+      a.kp_ld = c1 - c0;
+      e = launch_kernel(kern, dim3(nct, tail, ks), dim3(128), smem, st, 1, g);
+      if (e != cudaSuccess) return e;
+      return launch_splitk_reduce(a, ks, st, c1 - c0);
+    }
+  }
   e = launch_kernel(kern, dim3(nct, g.wtiles, g.ksplit), dim3(128), smem, st, 1, g);
   if (e != cudaSuccess || g.ksplit == 1) return e;
   return launch_splitk_reduce(a, g.ksplit, st);
@@ -699,6 +738,8 @@ cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st
   std::memset(&g, 0, sizeof(g));
   g.m = m;
   MatArgs& a = g.m;
+  a.kp_ld = a.ldo;                                    // a split of the whole output
+  a.kp_c0 = 0;
   a.tile_off[0] = 0;
   for (int i = 0; i < a.nseg; ++i) a.tile_off[i + 1] = a.tile_off[i] + (a.seg[i].rows + UM_R - 1) / UM_R;
   const bool has_lo = a.seg[0].a_lo != nullptr;

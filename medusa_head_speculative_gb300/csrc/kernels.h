@@ -43,6 +43,11 @@ struct MatArgs {
   __nv_bfloat16* out_lo;
   float* kpart;                  // tensor-core path: scratch for split-K partials, or null
   size_t kpart_bytes;
+  // layout of the split-K partials: kpart[z][m][kp_ld], holding output columns
+  // kp_c0 .. kp_c0 + kp_ld - 1 (set by the launcher; a split of the whole output has
+  // kp_c0 = 0 and kp_ld = ldo)
+  long kp_ld;
+  int kp_c0;
   // EPI_ROPE (tensor-core path, segments q | k | v of one head size): rotary embedding of
   // the q and k outputs at position rope_pos[m] (cos | sin rows of rope_table), then q to
   // rq (fp32, optional) and rqb (bf16, optional), k to rk and v to rv in the cache dtype
