@@ -80,12 +80,14 @@ struct medusa_plan {
   bool tc_attn = false;                      // tensor-core tree attention
   int M;                                     // node rows B * n1
   int topk_splits, topk_chunk;
+  int cand_ld = 1;                           // fused top-k: slots per (sequence, head)
   int nsplit, chunk, rpw, rows_per_block, nrb;
   // workspace layout (byte offsets)
   size_t o_logits, o_u, o_uhi, o_ulo, o_hhi, o_hlo, o_cv, o_ci, o_ttok, o_tval, o_root;
   size_t o_tok, o_pos, o_mask, o_retr, o_x, o_qkv, o_q, o_tk, o_tv, o_po, o_pml;
   size_t o_o, o_ohi, o_olo, o_hp, o_hphi, o_hplo, o_vlog, o_am, o_stats, o_path, o_nacc;
   size_t o_otok, o_hnext, o_rnext, o_qb;
+  size_t o_fcv, o_fci, o_finv, o_fini;       // fused top-k: slot lists, per-head final lists
   size_t ws_bytes;
 
   const int32_t* dparent() const { return d_spec; }
@@ -175,6 +177,10 @@ void layout(medusa_plan* p) {
   p->o_hlo = take(p->tc_heads ? B * D * 2 : 0);
   p->o_cv = take(B * (K + 1) * p->topk_splits * kTops * 4);
   p->o_ci = take(B * (K + 1) * p->topk_splits * kTops * 4);
+  p->o_fcv = take(B * (K + 1) * p->cand_ld * kTops * 4);
+  p->o_fci = take(B * (K + 1) * p->cand_ld * kTops * 4);
+  p->o_finv = take(B * (K + 1) * kTops * 4);
+  p->o_fini = take(B * (K + 1) * kTops * 4);
   p->o_ttok = take(B * K * kTops * 4);
   p->o_tval = take(B * K * kTops * 4);
   p->o_root = take(B * 4);
@@ -223,9 +229,49 @@ medusa_status check_ws(const medusa_plan* p, void* ws, size_t bytes) {
 inline cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 // ------------------------------------------------------------------ stage bodies
+// Slots that the heads launch `a` writes for fused top-k segment si (the selection merges
+// that many lists): the 128-row tiles on the tensor-core path, the row-dot CTAs covering
+// the block otherwise (grid: rowdot_grid of the same launch).
+long cand_slots(const medusa_plan* p, const MatArgs& a, int si, long grid) {
+  if (p->tc_heads) return (a.seg[si].rows + kCandTileRows - 1) / kCandTileRows;
+  long total = 0, s0 = 0;
+  for (int i = 0; i < a.nseg; ++i) {
+    if (i < si) s0 += a.seg[i].rows;
+    total += a.seg[i].rows;
+  }
+  if (grid < 1) return -1;
+  return rowdot_cta_of(s0 + a.seg[si].rows - 1, total, grid) - rowdot_cta_of(s0, total, grid) + 1;
+}
+
+// Upper bound of cand_slots over the heads launches a step makes: with the row-dot the LM
+// head (when computed) joins the first launch after the K blocks of d rows and the second
+// launch has the K heads' blocks of V rows.
+int plan_cand_ld(const medusa_plan* p) {
+  const medusa_dims& d = p->d;
+  if (p->tc_heads) return (d.V + kCandTileRows - 1) / kCandTileRows;
+  long most = 1;
+  for (int first = 0; first < 2; ++first) {
+    MatArgs a{};
+    a.M = d.B;
+    a.k = d.d;
+    a.nseg = first ? p->K + 1 : p->K;
+    for (int i = 0; i < a.nseg; ++i) {
+      a.seg[i].rows = first && i < p->K ? d.d : d.V;
+      a.seg[i].cand = !first || i == p->K;           // flagged as heads_impl flags them
+    }
+    const long grid = rowdot_grid(a, d.dtype);
+    for (int i = first ? p->K : 0; i < a.nseg; ++i) most = std::max(most, cand_slots(p, a, i, grid));
+  }
+  return (int)most;
+}
+
+// The heads' projections.  cand_count null: the logits of the computed heads go to
+// `logits` ([B][K+1][V]).  Otherwise the vocab projections keep the fused top-k instead
+// (slot lists in the workspace, per head the need[k] best) and cand_count[k] receives the
+// slots of head k.
 medusa_status heads_impl(const medusa_plan* p, const float* h, const int32_t* root_in,
                          const medusa_weights* w, float* logits, int32_t* ttok, float* tval,
-                         int32_t* root, void* ws, cudaStream_t st) {
+                         int32_t* root, void* ws, cudaStream_t st, int* cand_count = nullptr) {
   const medusa_dims& d = p->d;
   const int B = d.B, K = p->K, D = d.d, V = d.V;
   const size_t es = p->esize();
@@ -269,6 +315,34 @@ medusa_status heads_impl(const medusa_plan* p, const float* h, const int32_t* ro
     a.out_alt = logits;
     a.ldo_alt = (long)(K + 1) * V;
   }
+  // fused top-k: flag the candidate segments of a launch (head of segment i: head0 + i),
+  // then take their slot counts from that launch's own geometry
+  auto want_cand = [&](MatArgs& x, int i0, int head0) -> bool {
+    x.cand_val = at<float>(ws, p->o_fcv);
+    x.cand_idx = at<int32_t>(ws, p->o_fci);
+    x.cand_nh = K + 1;
+    x.cand_ld = p->cand_ld;
+    for (int i = i0; i < x.nseg; ++i) {
+      x.seg[i].cand = 1;
+      x.seg[i].head = head0 + i;
+      x.seg[i].rounds = p->need[head0 + i];
+    }
+    const long grid = p->tc_heads ? 0 : rowdot_grid(x, d.dtype);
+    long total = 0;
+    for (int i = 0; i < x.nseg; ++i) total += x.seg[i].rows;
+    long s0 = 0;
+    for (int i = 0; i < x.nseg; ++i) {
+      if (i >= i0) {
+        const long n = cand_slots(p, x, i, grid);
+        if (n < 1 || n > p->cand_ld) return false;
+        cand_count[head0 + i] = (int)n;
+        if (!p->tc_heads) x.seg[i].slot0 = (int)rowdot_cta_of(s0, total, grid);
+      }
+      s0 += x.seg[i].rows;
+    }
+    return true;
+  };
+  if (cand_count && lm_first && !want_cand(a, K, -K)) return MEDUSA_ERR_CUDA;
   LAUNCH(p, KN_H_W1, st, p->tc_heads ? launch_umma_gemm(a, p->d_status, st) : launch_rowdot(a, d.dtype, st));
   // z_k = W2_k u_k (and z_0 here when it did not join the first launch)
   const int k0 = root_in || lm_first ? 1 : 0;
@@ -295,6 +369,7 @@ medusa_status heads_impl(const medusa_plan* p, const float* h, const int32_t* ro
     s.rows = V;
     s.out_off = k * V;
   }
+  if (cand_count && !want_cand(b, 0, k0)) return MEDUSA_ERR_CUDA;
   LAUNCH(p, KN_H_VOCAB, st, p->tc_heads ? launch_umma_gemm(b, p->d_status, st) : launch_rowdot(b, d.dtype, st));
   (void)root_in; (void)ttok; (void)tval; (void)root;
   return MEDUSA_OK;
@@ -759,6 +834,7 @@ medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec
   }
   p->chunk = ((dims->capacity + p->nsplit - 1) / p->nsplit + gran - 1) / gran * gran;
   p->nsplit = (dims->capacity + p->chunk - 1) / p->chunk;
+  p->cand_ld = plan_cand_ld(p);
   layout(p);
 
   for (int k = 0; k <= MEDUSA_MAX_HEADS; ++k) p->need[k] = 1;
@@ -1005,15 +1081,24 @@ medusa_status step_core(const medusa_plan* p, const float* h, const int32_t* roo
   int32_t* cnt = at<int32_t>(ws, p->o_cnt);
   const int B = p->d.B;
   MEDUSA_TRY(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * (3 * B + p->M), st));
-  if ((s = heads_impl(p, h, root_in, w, logits, ttok, at<float>(ws, p->o_tval), root, ws, st)) != MEDUSA_OK)
+  int ccount[MEDUSA_MAX_HEADS + 1] = {0};
+  if ((s = heads_impl(p, h, root_in, w, logits, ttok, at<float>(ws, p->o_tval), root, ws, st, ccount)) !=
+      MEDUSA_OK)
     return s;
-  {   // fused: slice top-k, head merge and node tokens / positions
-    TopkArgs t = topk_args(p, logits, root_in, ws);
+  {   // fused top-k lists -> per-head top lists, head merge and node tokens / positions
+    CandArgs c{at<float>(ws, p->o_fcv), at<int32_t>(ws, p->o_fci), B, p->K + 1, p->cand_ld,
+               root_in ? 1 : 0};
+    for (int k = 0; k <= p->K; ++k) { c.count[k] = ccount[k]; c.rounds[k] = p->need[k]; }
+    c.fin_val = at<float>(ws, p->o_finv);
+    c.fin_idx = at<int32_t>(ws, p->o_fini);
     MergeArgs mg = merge_args(p, root_in, ttok, at<float>(ws, p->o_tval), root, ws);
-    for (int k = 0; k <= p->K; ++k) t.rounds[k] = mg.rounds[k] = p->need[k];
+    mg.cand_val = c.fin_val;
+    mg.cand_idx = c.fin_idx;
+    mg.splits = 1;
+    for (int k = 0; k <= p->K; ++k) mg.rounds[k] = p->need[k];
     TreeArgs tr{ttok, root, kv->len, p->d.B, p->K, p->d.V, p->n1, p->dparent(), p->ddepth(), p->drank(),
                 tok, pos, nullptr, nullptr, p->d_status};
-    LAUNCH(p, KN_SELECT, st, launch_heads_select(t, mg, tr, cnt, st));
+    LAUNCH(p, KN_SELECT, st, launch_cand_select(c, mg, tr, cnt, st));
   }
   if ((s = gather_impl(p, w, tok, ws, st)) != MEDUSA_OK) return s;
   auto tk_of = [&](int l) -> void* {

@@ -7,9 +7,12 @@
 // This file holds the CUDA-core streaming row-dot for few activation rows (decode at
 // small batch is a pure HBM stream of the weights); the tensor-core path for tens to
 // thousands of rows is in k_umma.cu.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
+#include "topk.cuh"
 
 namespace medusa {
 
@@ -43,9 +46,17 @@ __device__ __forceinline__ void epilogue_store(const MatArgs& a, const MatSeg& s
 // that segment's activations (MT rows x k fp32) in shared memory; each warp then streams
 // whole weight rows with 16-byte loads, U loads in flight per lane, and reduces across the
 // warp.  A single round avoids the tail of a partly filled last wave.
-template <typename W, int MT>
-__global__ void __launch_bounds__(256) rowdot_kernel(MatArgs a, long total_rows) {
+// Segments with fused top-k (MatSeg::cand) store nothing per row: each warp offers its row
+// sums to its running list of the best rows (per activation row, in shared memory), and at
+// the end of the CTA's range the 8 warps' lists are merged into the CTA's candidate slot.
+// CM: 0 = no segment has fused top-k, 1 = every segment has, 2 = some have (the kernel is
+// instantiated per case so the plain and the candidate paths do not share registers; the
+// mixed single-row case is held to 64 registers, 4 CTAs per SM, as the others reach alone).
+template <typename W, int MT, int CM>
+__global__ void __launch_bounds__(256, MT == 1 ? 4 : 3) rowdot_kernel(MatArgs a, long total_rows) {
   extern __shared__ float xs[];                       // [MT][k]
+  __shared__ float s_cv[MT][8][kTops];                // per-warp running candidate lists
+  __shared__ int s_ci[MT][8][kTops];
   constexpr int VEC = 16 / sizeof(W);
   constexpr int U = 8;
   const long g0 = total_rows * blockIdx.x / gridDim.x;
@@ -56,6 +67,7 @@ __global__ void __launch_bounds__(256) rowdot_kernel(MatArgs a, long total_rows)
   long seg_start = 0;
   for (int si = 0; si < a.nseg; ++si) {
     const MatSeg& s = a.seg[si];
+    const bool cand = CM == 1 || (CM == 2 && s.cand);
     const long lo = g0 > seg_start ? g0 : seg_start;
     const long hi = g1 < seg_start + s.rows ? g1 : seg_start + s.rows;
     if (lo < hi) {
@@ -92,47 +104,75 @@ __global__ void __launch_bounds__(256) rowdot_kernel(MatArgs a, long total_rows)
           }
         }
         __syncthreads();
-        bool have = rf < r1;                           // buf holds the loads of (rf, lane*VEC)
-        for (int r = rf; r < r1; r += 8) {
-          const W* wr = w + (long)r * k;
-          float acc[MT];
+        if (cand && lane < kTops) {
 #pragma unroll
-          for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-          for (int kb = lane * VEC; kb < k; kb += 32 * VEC * U) {
-            if (!have) {
+          for (int m = 0; m < MT; ++m) { s_cv[m][warp][lane] = NEG_INF; s_ci[m][warp][lane] = NO_IDX; }
+        }
+        // Rolling stream over the warp's rows rf, rf + 8, ... in groups of U 16-byte chunks
+        // per lane: as each chunk of the current group is unpacked, the same chunk of the next
+        // group (the next row's first group after a row's last) is requested, so U loads stay
+        // in flight through the FMAs, the row's reduction and its epilogue.
+        constexpr int GK = 32 * VEC * U;               // K covered by one group
+        const int G = (k + GK - 1) / GK;               // groups per row (the last may be partial)
+        const int nrow = rf < r1 ? (r1 - rf + 7) / 8 : 0;
+        const W* wc = w + (long)rf * k + lane * VEC;   // group in buf (loaded above)
+        const long to_next_row = 8L * k - (long)(G - 1) * GK;   // last group -> next row's first
+        float acc[MT];
 #pragma unroll
-              for (int u = 0; u < U; ++u) {
-                const int kk = kb + u * 32 * VEC;
-                if (kk < k) buf[u] = ld_stream16(wr + kk);
-              }
-            }
-            have = false;
+        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+        int g = 0, r = rf;
+        for (int left = nrow * G; left > 0; --left) {
+          const W* wnx = wc + (g + 1 < G ? (long)GK : to_next_row);
+          const int kb = lane * VEC + g * GK;
+          const int kbn = g + 1 < G ? kb + GK : lane * VEC;
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-              const int kk = kb + u * 32 * VEC;
-              if (kk < k) {
-                float f[VEC];
-                unpack16(buf[u], f);
+          for (int u = 0; u < U; ++u) {
+            const int kk = kb + u * 32 * VEC;
+            const bool cur = kk < k;                   // a row's last group may be partial
+            float f[VEC];
+            if (cur) unpack16(buf[u], f);
+            if (left > 1 && kbn + u * 32 * VEC < k) buf[u] = ld_stream16(wnx + u * 32 * VEC);
+            if (!cur) continue;
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                  const float4* xv = reinterpret_cast<const float4*>(xs + m * k + kk);
+            for (int m = 0; m < MT; ++m) {
+              const float4* xv = reinterpret_cast<const float4*>(xs + m * k + kk);
 #pragma unroll
-                  for (int e4 = 0; e4 < VEC / 4; ++e4) {
-                    const float4 x4 = xv[e4];
-                    acc[m] = fmaf(f[4 * e4 + 0], x4.x, acc[m]);
-                    acc[m] = fmaf(f[4 * e4 + 1], x4.y, acc[m]);
-                    acc[m] = fmaf(f[4 * e4 + 2], x4.z, acc[m]);
-                    acc[m] = fmaf(f[4 * e4 + 3], x4.w, acc[m]);
-                  }
-                }
+              for (int e4 = 0; e4 < VEC / 4; ++e4) {
+                const float4 x4 = xv[e4];
+                acc[m] = fmaf(f[4 * e4 + 0], x4.x, acc[m]);
+                acc[m] = fmaf(f[4 * e4 + 1], x4.y, acc[m]);
+                acc[m] = fmaf(f[4 * e4 + 2], x4.z, acc[m]);
+                acc[m] = fmaf(f[4 * e4 + 3], x4.w, acc[m]);
               }
             }
           }
+          wc = wnx;
+          if (++g == G) {                              // row r complete
+            g = 0;
 #pragma unroll
-          for (int m = 0; m < MT; ++m) acc[m] = warp_sum(acc[m]);
+            for (int m = 0; m < MT; ++m) acc[m] = warp_sum(acc[m]);
+            if (cand) {
 #pragma unroll
-          for (int m = 0; m < MT; ++m)
-            if (lane == m && m < mt) epilogue_store(a, s, si, m0 + m, r, acc[m]);
+              for (int m = 0; m < MT; ++m)
+                if (m < mt) warp_list_offer(s_cv[m][warp], s_ci[m][warp], acc[m], r, s.rounds);
+            } else {
+#pragma unroll
+              for (int m = 0; m < MT; ++m)
+                if (lane == m && m < mt) epilogue_store(a, s, si, m0 + m, r, acc[m]);
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+            r += 8;
+          }
+        }
+        if (cand) {                                    // CTA-uniform
+          __syncthreads();
+          const int slot = (int)blockIdx.x - s.slot0;
+          for (int m = 0; m < mt; ++m) {
+            const long o = (((long)(m0 + m) * a.cand_nh + s.head) * a.cand_ld + slot) * kTops;
+            rank_merge(s_cv[m], s_ci[m], 8, s.rounds, a.cand_val + o, a.cand_idx + o, threadIdx.x, blockDim.x);
+          }
+          __syncthreads();                             // the lists are refilled next
         }
       }
     }
@@ -140,8 +180,10 @@ __global__ void __launch_bounds__(256) rowdot_kernel(MatArgs a, long total_rows)
   }
 }
 
-template <typename W, int MT>
-static cudaError_t rowdot_go(const MatArgs& a, cudaStream_t st) {
+// Grid of one launch (or -1): one round of resident CTAs, at least one row per warp.  The
+// fused top-k's slot counts come from the same number.
+template <typename W, int MT, int CM>
+static long rowdot_grid_t(const MatArgs& a, size_t smem) {
   static int num_sms = 0;
   if (!num_sms) {
     int dev = 0;
@@ -151,38 +193,71 @@ static cudaError_t rowdot_go(const MatArgs& a, cudaStream_t st) {
   }
   long total = 0;
   for (int i = 0; i < a.nseg; ++i) total += a.seg[i].rows;
-  const size_t smem = (size_t)MT * a.k * sizeof(float);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(rowdot_kernel<W, MT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(rowdot_kernel<W, MT, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
+    return -1;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rowdot_kernel<W, MT>, 256, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rowdot_kernel<W, MT, CM>, 256, smem) !=
           cudaSuccess || per_sm < 1)
     per_sm = 1;
   long grid = (long)per_sm * num_sms;
-  const long by_rows = (total + 7) / 8;               // at least one row per warp
+  const long by_rows = (total + 7) / 8;
   grid = grid < by_rows ? grid : by_rows;
-  return launch_kernel(rowdot_kernel<W, MT>, dim3((unsigned)grid), dim3(256), smem, st, 1, a, total);
+  return grid < 1 ? 1 : grid;
 }
 
-cudaError_t launch_rowdot(const MatArgs& a, int dtype, cudaStream_t st) {
+template <typename W, int MT, int CM>
+static cudaError_t rowdot_go(const MatArgs& a, cudaStream_t st) {
+  long total = 0;
+  for (int i = 0; i < a.nseg; ++i) total += a.seg[i].rows;
+  const size_t smem = (size_t)MT * a.k * sizeof(float);
+  const long grid = rowdot_grid_t<W, MT, CM>(a, smem);
+  if (grid < 0) return cudaErrorInvalidValue;
+  return launch_kernel(rowdot_kernel<W, MT, CM>, dim3((unsigned)grid), dim3(256), smem, st, 1, a, total);
+}
+
+// Dispatch on the weight type, the activation rows per pass (MT = min(M, 4)) and which
+// segments keep fused top-k (CM).
+template <int CM, typename F>
+static auto rowdot_dispatch_cm(const MatArgs& a, int dtype, F&& f) {
   const int mt = a.M >= 4 ? 4 : a.M;
+  using C = std::integral_constant<int, CM>;
   if (dtype == 0) {
     switch (mt) {
-      case 1: return rowdot_go<float, 1>(a, st);
-      case 2: return rowdot_go<float, 2>(a, st);
-      case 3: return rowdot_go<float, 3>(a, st);
-      default: return rowdot_go<float, 4>(a, st);
+      case 1: return f(std::integral_constant<int, 1>{}, float{}, C{});
+      case 2: return f(std::integral_constant<int, 2>{}, float{}, C{});
+      case 3: return f(std::integral_constant<int, 3>{}, float{}, C{});
+      default: return f(std::integral_constant<int, 4>{}, float{}, C{});
     }
   }
   switch (mt) {
-    case 1: return rowdot_go<bf16, 1>(a, st);
-    case 2: return rowdot_go<bf16, 2>(a, st);
-    case 3: return rowdot_go<bf16, 3>(a, st);
-    default: return rowdot_go<bf16, 4>(a, st);
+    case 1: return f(std::integral_constant<int, 1>{}, bf16{}, C{});
+    case 2: return f(std::integral_constant<int, 2>{}, bf16{}, C{});
+    case 3: return f(std::integral_constant<int, 3>{}, bf16{}, C{});
+    default: return f(std::integral_constant<int, 4>{}, bf16{}, C{});
   }
+}
+template <typename F>
+static auto rowdot_dispatch(const MatArgs& a, int dtype, F&& f) {
+  int nc = 0;
+  for (int i = 0; i < a.nseg; ++i) nc += a.seg[i].cand ? 1 : 0;
+  if (nc == 0) return rowdot_dispatch_cm<0>(a, dtype, f);
+  if (nc == a.nseg) return rowdot_dispatch_cm<1>(a, dtype, f);
+  return rowdot_dispatch_cm<2>(a, dtype, f);
+}
+
+cudaError_t launch_rowdot(const MatArgs& a, int dtype, cudaStream_t st) {
+  return rowdot_dispatch(a, dtype, [&](auto mt, auto w, auto cm) {
+    return rowdot_go<decltype(w), decltype(mt)::value, decltype(cm)::value>(a, st);
+  });
+}
+
+int rowdot_grid(const MatArgs& a, int dtype) {
+  return (int)rowdot_dispatch(a, dtype, [&](auto mt, auto w, auto cm) {
+    return rowdot_grid_t<decltype(w), decltype(mt)::value, decltype(cm)::value>(
+        a, (size_t)decltype(mt)::value * a.k * sizeof(float));
+  });
 }
 
 // =========================================================== small helpers

@@ -13,99 +13,9 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
+#include "topk.cuh"
 
 namespace medusa {
-
-#define NEG_INF (-INFINITY)
-constexpr int NO_IDX = 0x7fffffff;
-
-// Sorted (descending) per-thread candidate list of depth N kept in registers.
-template <int N>
-struct TopListN {
-  float v[N];
-  int i[N];
-  __device__ __forceinline__ void init() {
-#pragma unroll
-    for (int t = 0; t < N; ++t) { v[t] = NEG_INF; i[t] = NO_IDX; }
-  }
-  __device__ __forceinline__ void insert(float x, int idx) {
-    if (!better(x, idx, v[N - 1], i[N - 1])) return;
-    v[N - 1] = x;
-    i[N - 1] = idx;
-#pragma unroll
-    for (int t = N - 1; t > 0; --t) {
-      if (better(v[t], i[t], v[t - 1], i[t - 1])) {
-        float tv = v[t]; v[t] = v[t - 1]; v[t - 1] = tv;
-        int ti = i[t]; i[t] = i[t - 1]; i[t - 1] = ti;
-      }
-    }
-  }
-  __device__ __forceinline__ void pop() {
-#pragma unroll
-    for (int t = 0; t < N - 1; ++t) { v[t] = v[t + 1]; i[t] = i[t + 1]; }
-    v[N - 1] = NEG_INF;
-    i[N - 1] = NO_IDX;
-  }
-};
-using TopList = TopListN<kTops>;
-
-// Order-preserving 32-bit key of a float (larger float -> larger key; -0 as +0; NaN lowest).
-__device__ __forceinline__ uint32_t float_key(float v) {
-  uint32_t u = __float_as_uint(v);
-  if (u == 0x80000000u) u = 0u;
-  if (v != v) return 0u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_float(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-// Merge the 32 lanes' sorted lists into the first `rounds` ranks of ov/oi (kTops entries;
-// ranks past `rounds` are written as sentinels): each round is a warp reduction over the
-// list heads (max of the value keys, then min of the token ids among the lanes holding
-// that value) and the winning lane pops.  Token ids are distinct across lanes (sentinels
-// aside).
-template <int N>
-__device__ __forceinline__ void warp_merge(TopListN<N>& L, float* ov, int* oi, int rounds = kTops) {
-  const int lane = threadIdx.x & 31;
-  rounds = rounds < 1 || rounds > kTops ? kTops : rounds;
-  if (lane == 0)                                   // ranks past `rounds` are not needed
-    for (int t = rounds; t < kTops; ++t) { ov[t] = NEG_INF; oi[t] = NO_IDX; }
-#pragma unroll 1
-  for (int t = 0; t < rounds; ++t) {
-    const uint32_t key = float_key(L.v[0]);
-    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
-    const uint32_t imin = __reduce_min_sync(0xffffffffu, key == kmax ? (uint32_t)L.i[0] : 0x7fffffffu);
-    if (key == kmax && (uint32_t)L.i[0] == imin) L.pop();
-    if (lane == 0) {
-      ov[t] = kmax != 0u ? key_float(kmax) : NEG_INF;
-      oi[t] = (int)imin;
-    }
-  }
-}
-
-// Sorts N (value, token) pairs into descending `better` order with a bitonic sorting
-// network (N a power of two); every comparator index is a compile-time constant, so the
-// pairs stay in registers.
-template <int N>
-__device__ __forceinline__ void bitonic_sort_desc(float (&v)[N], int (&ix)[N]) {
-#pragma unroll
-  for (int k = 2; k <= N; k <<= 1)
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1)
-#pragma unroll
-      for (int x = 0; x < N; ++x) {
-        const int y = x ^ j;
-        if (y <= x) continue;
-        // blocks of k with bit k clear end descending, the others ascending: each pair of
-        // neighbouring blocks is then a bitonic sequence for the next merge
-        const bool sw = (x & k) == 0 ? better(v[y], ix[y], v[x], ix[x]) : better(v[x], ix[x], v[y], ix[y]);
-        if (sw) {
-          const float tv = v[x]; v[x] = v[y]; v[y] = tv;
-          const int ti = ix[x]; ix[x] = ix[y]; ix[y] = ti;
-        }
-      }
-}
 
 // The 16 best (logit, token) pairs of one vocab slice of one head, by a 256-thread CTA.
 // When the slice starts on a 16-byte boundary each thread loads F float4 of it (4F <= 16
@@ -215,6 +125,15 @@ __device__ void merge_heads(const MergeArgs& a, int b, float (*tv)[kTops], int (
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
   const int nh = a.K + 1;
   for (int k = warp + a.k0; k < nh; k += nw) {
+    if (a.splits == 1) {           // one list per head: it is the head's final list
+      const long o = ((long)b * nh + k) * kTops;
+      const int r = a.rounds[k] < 1 || a.rounds[k] > kTops ? kTops : a.rounds[k];
+      if (lane < kTops) {
+        tv[k][lane] = lane < r ? __ldcg(a.cand_val + o + lane) : NEG_INF;
+        ti[k][lane] = lane < r ? __ldcg(a.cand_idx + o + lane) : NO_IDX;
+      }
+      continue;
+    }
     TopList L;
     L.init();
     if (lane < a.splits) {
@@ -300,6 +219,71 @@ cudaError_t launch_heads_select(const TopkArgs& t, const MergeArgs& m, const Tre
                                 int32_t* counter, cudaStream_t st) {
   dim3 grid(t.splits, t.nh - t.k0, t.B);
   return launch_kernel(heads_select_kernel, grid, dim3(256), 0, st, 1, t, m, tr, counter);
+}
+
+// Selection from the fused top-k candidates: CTA (head k, sequence b) reads the head's
+// slot lists (each sorted, written by the projection's CTAs), thread t merging slots t,
+// t + 256, ... by insertion until an entry no longer enters; the warps' lists and then the
+// 8 warp lists are merged into the head's final list.  The last CTA of a sequence takes the
+// heads' final lists, picks the root and writes the node tokens as heads_select does.
+__global__ void __launch_bounds__(256) cand_select_kernel(CandArgs c, MergeArgs m, TreeArgs tr,
+                                                          int32_t* counter) {
+  __shared__ float sv[8][kTops];
+  __shared__ int si[8][kTops];
+  __shared__ float tv[MEDUSA_MAX_HEADS + 1][kTops];
+  __shared__ int ti[MEDUSA_MAX_HEADS + 1][kTops];
+  __shared__ int s_root, s_last;
+  pdl_trigger();
+  pdl_wait();
+  const int k = blockIdx.x + c.k0, b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, n = c.count[k];
+  const long base = ((long)b * c.nh + k) * c.ld;
+  TopList L;
+  L.init();
+  auto load = [&](int slot, float (&v)[kTops], int (&ix)[kTops]) {
+    const float4* pv = reinterpret_cast<const float4*>(c.cand_val + (base + slot) * kTops);
+    const int4* pi = reinterpret_cast<const int4*>(c.cand_idx + (base + slot) * kTops);
+#pragma unroll
+    for (int q = 0; q < kTops / 4; ++q) {
+      const float4 x = __ldcg(pv + q);
+      const int4 y = __ldcg(pi + q);
+      v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+      ix[4 * q] = y.x; ix[4 * q + 1] = y.y; ix[4 * q + 2] = y.z; ix[4 * q + 3] = y.w;
+    }
+  };
+  if ((int)threadIdx.x < n) load(threadIdx.x, L.v, L.i);     // a sorted list as it stands
+  for (int slot = threadIdx.x + blockDim.x; slot < n; slot += blockDim.x) {
+    float v[kTops];
+    int ix[kTops];
+    load(slot, v, ix);
+#pragma unroll
+    for (int t = 0; t < kTops; ++t) {
+      if (!better(v[t], ix[t], L.v[kTops - 1], L.i[kTops - 1])) break;
+      L.insert(v[t], ix[t]);
+    }
+  }
+  warp_merge(L, sv[warp], si[warp], c.rounds[k]);
+  __syncthreads();
+  {
+    const long o = ((long)b * c.nh + k) * kTops;
+    rank_merge(sv, si, 8, c.rounds[k], c.fin_val + o, c.fin_idx + o, threadIdx.x, blockDim.x);
+  }
+  __threadfence();                 // the head's final list, before the count below
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(counter + b, 1) == c.nh - c.k0 - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  merge_heads(m, b, tv, ti, &s_root);
+  node_tokens(tr, b, ti, s_root);
+  if (threadIdx.x == 0) counter[b] = 0;
+}
+
+cudaError_t launch_cand_select(const CandArgs& c, const MergeArgs& m, const TreeArgs& tr,
+                               int32_t* counter, cudaStream_t st) {
+  if (m.splits != 1 || m.cand_val != c.fin_val || m.cand_idx != c.fin_idx) return cudaErrorInvalidValue;
+  dim3 grid(c.nh - c.k0, c.B);
+  return launch_kernel(cand_select_kernel, grid, dim3(256), 0, st, 1, c, m, tr, counter);
 }
 
 // One CTA per sequence: node tokens and position ids.  Block 0 also writes the per-tree

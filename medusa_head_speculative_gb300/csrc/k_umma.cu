@@ -22,12 +22,14 @@
 #include "kernels.h"
 #include "launch.cuh"
 #include "tc_ptx.cuh"
+#include "topk.cuh"
 
 namespace medusa {
 
 constexpr int UM_R = 128;           // weight rows per CTA (MMA M)
 constexpr int UM_K = 64;            // K per stage (one 128-byte swizzle row)
 constexpr uint32_t UM_W_BYTES = UM_R * 128;
+static_assert(UM_R == kCandTileRows, "fused top-k slots are the 128-row tiles");
 
 struct UmmaArgs {
   CUtensorMap tw[kMaxSeg];   // weights of each segment: dims {k, rows}, box {64, 128}
@@ -201,7 +203,19 @@ __device__ void staged_epilogue(const MatArgs& a, const MatSeg& s, int rbase, in
       }
     }
     __syncthreads();
-    if (a.epi == EPI_ROPE && !kpart) {
+    if (s.cand && !kpart) {
+      // fused top-k: per activation row, the best of each 128 weight rows -> its slot
+      for (int ml = warp; ml < cm; ml += 4) {
+        const int m = m0 + c0 + ml;
+        if (m >= a.M) break;
+        for (int t = 0; t < nacc; ++t) {
+          const float4 v = *reinterpret_cast<const float4*>(stage + ml * rt + t * 128 + 4 * lane);
+          const int r0 = rbase + t * 128;
+          const long o = (((long)m * a.cand_nh + s.head) * a.cand_ld + r0 / kCandTileRows) * kTops;
+          warp_top_of_128(v, r0, s.rows, s.rounds, a.cand_val + o, a.cand_idx + o);
+        }
+      }
+    } else if (a.epi == EPI_ROPE && !kpart) {
       // weight tiles start on head boundaries: both halves of every head are in the stage
       const int dh = a.rope_dh, half = dh / 2, gh = half / 4, heads = rt / dh;
       for (int i = tid; i < cm * heads * gh; i += 128) {
@@ -709,6 +723,12 @@ static cudaError_t launch_umma_wide(const MatArgs& m, uint32_t* status, int num_
   return launch_splitk_reduce(a, g.ksplit, st);
 }
 
+static bool any_cand(const MatArgs& a) {
+  for (int i = 0; i < a.nseg; ++i)
+    if (a.seg[i].cand) return true;
+  return false;
+}
+
 // The wide variant needs every segment to read the same activations (one shared tile).
 static bool shared_activations(const MatArgs& a) {
   for (int i = 1; i < a.nseg; ++i)
@@ -733,7 +753,7 @@ cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st
     for (int i = 1; i < m.nseg; ++i)
       if ((m.seg[i].a_lo != nullptr) != (m.seg[0].a_lo != nullptr)) lo_ok = false;
     if (!lo_ok) return cudaErrorInvalidValue;
-    if (m.M > 128 && shared_activations(m)) return launch_umma_wide(m, status, num_sms, st);
+    if (m.M > 128 && shared_activations(m) && !any_cand(m)) return launch_umma_wide(m, status, num_sms, st);
   }
   std::memset(&g, 0, sizeof(g));
   g.m = m;
@@ -760,7 +780,8 @@ cudaError_t launch_umma_gemm(const MatArgs& m, uint32_t* status, cudaStream_t st
   // split K when the tiles alone cannot cover the SMs
   const int nk = (a.k + UM_K - 1) / UM_K;
   const int mchunks = (a.M + nbox - 1) / nbox;
-  const int ksplit = choose_ksplit(a, (long)mchunks * a.tile_off[a.nseg], nk, num_sms, 2);
+  // (the fused top-k needs whole sums in the epilogue: no K split)
+  const int ksplit = any_cand(a) ? 1 : choose_ksplit(a, (long)mchunks * a.tile_off[a.nseg], nk, num_sms, 2);
   g.ksplit = ksplit;
   g.kpart = a.kpart;
   for (int i = 0; i < a.nseg; ++i) {

@@ -26,6 +26,13 @@ struct MatSeg {
   long ldx;                      // activation row stride (elements)
   int rows;
   int out_off;
+  // Fused top-k (vocab projections of the heads): when `cand` is set the block's outputs
+  // are not stored; instead each CTA writes, per activation row m, the best `rounds`
+  // (logit, token) pairs of the rows it computed (sorted, then sentinels up to kTops) to
+  // MatArgs::cand_val / cand_idx at [m][head][slot][kTops], token = row index r.  The slot
+  // is the CTA's index among those covering the block: the 128-row tile for the
+  // tensor-core path; for the row-dot blockIdx.x - slot0, slot0 = rowdot_cta_of(first row).
+  int cand, head, rounds, slot0;
 };
 
 struct MatArgs {
@@ -71,10 +78,23 @@ struct MatArgs {
   // on a barrier that nothing arrives on, for at most this many nanoseconds, and then
   // takes the expired-wait path.
   unsigned long long test_wait_ns;
+  // fused top-k output of the segments with `cand` set: [M][cand_nh][cand_ld][kTops]
+  float* cand_val;
+  int32_t* cand_idx;
+  int cand_nh, cand_ld;
 };
 
 // CUDA-core row-dot projection: dtype 0 = f32 weights, 1 = bf16.
 cudaError_t launch_rowdot(const MatArgs& a, int dtype, cudaStream_t st);
+// CTAs of that launch (one round: as many as are resident at once, >= 8 rows each).
+int rowdot_grid(const MatArgs& a, int dtype);
+// Row-dot CTA c computes the stacked rows [total*c/grid, total*(c+1)/grid); the CTA that
+// computes row x is the largest c with floor(total*c/grid) <= x.
+__host__ __device__ inline long rowdot_cta_of(long x, long total, long grid) {
+  return ((x + 1) * grid + total - 1) / total - 1;
+}
+// Tensor-core path with fused top-k: 128-row tiles of a block (its slots).
+constexpr int kCandTileRows = 128;
 // Tensor-core (tcgen05 + TMA + TMEM) projection; bf16 weights only.  Sets
 // MEDUSA_FLAG_TIMEOUT in *status if a pipeline wait expires.
 cudaError_t launch_umma_gemm(const MatArgs& a, uint32_t* status, cudaStream_t st);
@@ -125,6 +145,20 @@ cudaError_t launch_heads_select(const TopkArgs& t, const MergeArgs& m, const Tre
                                 int32_t* counter, cudaStream_t st);
 // Resident 256-thread selection CTAs per SM (0 when the query fails).
 int heads_select_ctas_per_sm();
+
+// Selection from the fused top-k candidates (MatSeg::cand): CTA (head, sequence) merges
+// the head's `count[head]` slot lists into its final top list (fin_val / fin_idx,
+// [B][nh][kTops]); the last CTA of a sequence (atomic counter, reset on exit) merges the
+// heads, picks the root and writes the node tokens and positions, as heads_select does.
+struct CandArgs {
+  const float* cand_val; const int32_t* cand_idx;     // [B][nh][ld][kTops]
+  int B, nh, ld, k0;
+  int count[MEDUSA_MAX_HEADS + 1];
+  int rounds[MEDUSA_MAX_HEADS + 1];
+  float* fin_val; int32_t* fin_idx;                  // [B][nh][kTops]
+};
+cudaError_t launch_cand_select(const CandArgs& c, const MergeArgs& m, const TreeArgs& tr,
+                               int32_t* counter, cudaStream_t st);
 
 // qkv [M][(Hq+2Hkv)*dh] fp32 -> q [M][Hq][dh] fp32 (RoPE; also as bf16 into qb when
 // non-null), tree k (RoPE) / v in dtype.
