@@ -510,7 +510,8 @@ medusa_status attn_impl(const medusa_plan* p, const float* q, const medusa_kv* k
   a.rpw = p->rpw;
   a.part_o = at<float>(ws, p->o_po);
   a.part_ml = at<float>(ws, p->o_pml);
-  a.o = o;
+  // the step's tensor-core out projection reads only the bf16 halves: no fp32 copy then
+  a.o = split_out && p->tc_nodes ? nullptr : o;
   a.o_hi = split_out && p->tc_nodes ? at<bf16>(ws, p->o_ohi) : nullptr;
   a.o_lo = split_out && p->tc_nodes ? at<bf16>(ws, p->o_olo) : nullptr;
   a.status = p->d_status;

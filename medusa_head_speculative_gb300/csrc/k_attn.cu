@@ -217,11 +217,28 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
   const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
   const int n = r / a.G, hq = g * a.G + r % a.G;
   const long o0 = (((long)b * a.n1 + n) * a.Hq + hq) * a.dh + lane * VPL;
+  float y[VPL];
 #pragma unroll
-  for (int c = 0; c < VPL; ++c) {
-    const float y = Lsum > 0.f ? acc[c] * inv : 0.f;
-    a.o[o0 + c] = y;
-    if (a.o_hi) split_hi_lo(y, a.o_hi[o0 + c], a.o_lo[o0 + c]);
+  for (int c = 0; c < VPL; ++c) y[c] = Lsum > 0.f ? acc[c] * inv : 0.f;
+  if (a.o) {
+    if (VPL == 4) {
+      *reinterpret_cast<float4*>(a.o + o0) = make_float4(y[0], y[VPL > 1 ? 1 : 0], y[VPL > 2 ? 2 : 0], y[VPL > 3 ? 3 : 0]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) a.o[o0 + c] = y[c];
+    }
+  }
+  if (a.o_hi) {
+    bf16 hi[VPL], lo[VPL];
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) split_hi_lo(y[c], hi[c], lo[c]);
+    if (VPL == 4) {                                  // 8-byte stores of four halves
+      *reinterpret_cast<uint2*>(a.o_hi + o0) = *reinterpret_cast<const uint2*>(hi);
+      *reinterpret_cast<uint2*>(a.o_lo + o0) = *reinterpret_cast<const uint2*>(lo);
+    } else {
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) { a.o_hi[o0 + c] = hi[c]; a.o_lo[o0 + c] = lo[c]; }
+    }
   }
 }
 
