@@ -47,45 +47,40 @@ struct UmmaArgs {
 __device__ __forceinline__ bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 __device__ __forceinline__ bool aligned8(const void* p) { return ((uintptr_t)p & 7) == 0; }
 
-// Outputs r..r+3 (weight rows of segment s) of activation row m: the epilogue with 16-byte
-// loads and stores where all four exist and the addresses allow it, else per element.
-__device__ __forceinline__ void epilogue4(const MatArgs& a, const MatSeg& s, int m, int r, float4 v,
-                                          float* kpart_row) {
-  float y[4] = {v.x, v.y, v.z, v.w};
-  const int n = min(4, s.rows - r);
-  if (kpart_row) {                                      // raw partial sum of a K range
-    float* kp = kpart_row + s.out_off + r - a.kp_c0;
-    if (n == 4 && aligned16(kp)) *reinterpret_cast<float4*>(kp) = v;
-    else for (int e = 0; e < n; ++e) kp[e] = y[e];
-    return;
-  }
-  const long o = (long)m * a.ldo + s.out_off + r;
-  if (a.epi != EPI_STORE) {
-    const long ro = (long)m * a.ldr + r;
-    float res[4] = {0.f, 0.f, 0.f, 0.f};
-    if (a.res_f32) {
-      const float* rp = a.res_f32 + ro;
-      if (n == 4 && aligned16(rp)) {
-        const float4 q = *reinterpret_cast<const float4*>(rp);
-        res[0] = q.x; res[1] = q.y; res[2] = q.z; res[3] = q.w;
-      } else {
-        for (int e = 0; e < n; ++e) res[e] = rp[e];
-      }
-    } else {
-      const bf16* rw = reinterpret_cast<const bf16*>(a.res_w) + ro;
-      if (n == 4 && aligned8(rw)) {
-        const uint2 q = *reinterpret_cast<const uint2*>(rw);
-        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&q.x);
-        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&q.y);
-        res[0] = __low2float(p0); res[1] = __high2float(p0);
-        res[2] = __low2float(p1); res[3] = __high2float(p1);
-      } else {
-        for (int e = 0; e < n; ++e) res[e] = to_f32(rw[e]);
-      }
+// Residual of outputs r..r+3 of activation row m for EPI_SILU_RES / EPI_RES_ADD (n of them
+// exist): 16-byte (fp32) or 8-byte (bf16) loads where all four exist and the address allows.
+__device__ __forceinline__ float4 load_res4(const MatArgs& a, int m, int r, int n) {
+  const long ro = (long)m * a.ldr + r;
+  float res[4] = {0.f, 0.f, 0.f, 0.f};
+  if (a.res_f32) {
+    const float* rp = a.res_f32 + ro;
+    if (n == 4 && aligned16(rp)) return *reinterpret_cast<const float4*>(rp);
+    for (int e = 0; e < n; ++e) res[e] = rp[e];
+  } else {
+    const bf16* rw = reinterpret_cast<const bf16*>(a.res_w) + ro;
+    if (n == 4 && aligned8(rw)) {
+      const uint2 q = *reinterpret_cast<const uint2*>(rw);
+      const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&q.x);
+      const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&q.y);
+      return make_float4(__low2float(p0), __high2float(p0), __low2float(p1), __high2float(p1));
     }
+    for (int e = 0; e < n; ++e) res[e] = to_f32(rw[e]);
+  }
+  return make_float4(res[0], res[1], res[2], res[3]);
+}
+
+// Outputs r..r+3 (weight rows of segment s) of activation row m from the sums v and the
+// residual (ignored for EPI_STORE): the activation, the fp32 store and the optional bf16
+// hi/lo copies, vectorised where all four exist and the addresses allow it.
+__device__ __forceinline__ void finish4(const MatArgs& a, const MatSeg& s, int m, int r, float4 v,
+                                        float4 rv, int n) {
+  float y[4] = {v.x, v.y, v.z, v.w};
+  if (a.epi != EPI_STORE) {
+    const float res[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) y[e] = (a.epi == EPI_SILU_RES ? silu(y[e]) : y[e]) + res[e];
   }
+  const long o = (long)m * a.ldo + s.out_off + r;
   float* op = a.out + o;
   if (n == 4 && aligned16(op)) *reinterpret_cast<float4*>(op) = make_float4(y[0], y[1], y[2], y[3]);
   else for (int e = 0; e < n; ++e) op[e] = y[e];
@@ -107,6 +102,22 @@ __device__ __forceinline__ void epilogue4(const MatArgs& a, const MatSeg& s, int
       }
     }
   }
+}
+
+// Outputs r..r+3 (weight rows of segment s) of activation row m: the epilogue, or the raw
+// partial sum of a K range into kpart_row.
+__device__ __forceinline__ void epilogue4(const MatArgs& a, const MatSeg& s, int m, int r, float4 v,
+                                          float* kpart_row) {
+  const int n = min(4, s.rows - r);
+  if (kpart_row) {                                      // raw partial sum of a K range
+    float* kp = kpart_row + s.out_off + r - a.kp_c0;
+    const float y[4] = {v.x, v.y, v.z, v.w};
+    if (n == 4 && aligned16(kp)) *reinterpret_cast<float4*>(kp) = v;
+    else for (int e = 0; e < n; ++e) kp[e] = y[e];
+    return;
+  }
+  const float4 rv = a.epi != EPI_STORE ? load_res4(a, m, r, n) : make_float4(0.f, 0.f, 0.f, 0.f);
+  finish4(a, s, m, r, v, rv, n);
 }
 
 __device__ __forceinline__ void store4(float* p, const float (&y)[4]) {
@@ -532,32 +543,40 @@ __global__ void __launch_bounds__(128, 1) umma_wide_kernel(const __grid_constant
   if (warp == 1) tmem_dealloc(tmem, g.tmem_cols);
 }
 
-// Sum of the K-range partials for 4 consecutive output columns per thread (all loads issued
-// before the epilogue's stores), then the epilogue (single-segment launches) or a plain
-// store (multi-segment EPI_STORE launches).  cols % 4 == 0.
-__global__ void splitk_reduce_kernel(const MatArgs a, const float* __restrict__ kpart, int ksplit, int cols) {
-  constexpr int ZMAX = 8;
+// Sum of the K-range partials (in K order) for 4 consecutive output columns per item, then
+// the epilogue (single-segment launches) or a plain store (multi-segment EPI_STORE
+// launches).  A thread takes IPT items a grid stride apart and issues all their loads (the
+// partials and the residual) before the first sum, so each pass is one round trip.
+// cols % 4 == 0.
+template <int KS>
+constexpr int reduce_ipt() { return KS <= 2 ? 4 : (KS <= 4 ? 2 : 1); }
+
+template <int KS>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const MatArgs a, const float* __restrict__ kpart,
+                                                            int cols) {
+  constexpr int IPT = reduce_ipt<KS>();
   pdl_trigger();
   pdl_wait();
   const long kld = a.kp_ld;
+  const long stride = (long)gridDim.x * blockDim.x;
   if (a.epi == EPI_ROPE) {
     // one item = 4 columns of the first half of a head and their partners dh/2 further on
     const int dh = a.rope_dh, half = dh / 2, gh = half / 4;
     const int per_row = (cols / dh) * gh;
     const long n = (long)a.M * per_row;
-    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += stride) {
       const int m = (int)(i / per_row), rem = (int)(i - (long)m * per_row), hg = rem / gh;
       const int c0 = hg * dh + 4 * (rem - hg * gh);           // column within the partials
-      float4 v0[ZMAX], v1[ZMAX];
+      float4 v0[KS], v1[KS];
 #pragma unroll
-      for (int z = 0; z < ZMAX; ++z) {
+      for (int z = 0; z < KS; ++z) {
         const float* row = kpart + ((long)z * a.M + m) * kld;
-        v0[z] = z < ksplit ? __ldcg(reinterpret_cast<const float4*>(row + c0)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v1[z] = z < ksplit ? __ldcg(reinterpret_cast<const float4*>(row + c0 + half)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v0[z] = __ldcg(reinterpret_cast<const float4*>(row + c0));
+        v1[z] = __ldcg(reinterpret_cast<const float4*>(row + c0 + half));
       }
       float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
 #pragma unroll
-      for (int z = 0; z < ZMAX; ++z) {
+      for (int z = 0; z < KS; ++z) {
         s0.x += v0[z].x; s0.y += v0[z].y; s0.z += v0[z].z; s0.w += v0[z].w;
         s1.x += v1[z].x; s1.y += v1[z].y; s1.z += v1[z].z; s1.w += v1[z].w;
       }
@@ -567,28 +586,38 @@ __global__ void splitk_reduce_kernel(const MatArgs a, const float* __restrict__ 
   }
   const int c4 = cols / 4;
   const long n = (long)a.M * c4;
-  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
-    const int m = (int)(i / c4), c = (int)(i - (long)m * c4) * 4;
-    float4 v[ZMAX];
+  const bool res = a.nseg == 1 && a.epi != EPI_STORE;
+  for (long i0 = blockIdx.x * (long)blockDim.x + threadIdx.x; i0 < n; i0 += stride * IPT) {
+    float4 v[IPT][KS], rv[IPT];
 #pragma unroll
-    for (int z = 0; z < ZMAX; ++z)
-      v[z] = z < ksplit ? __ldcg(reinterpret_cast<const float4*>(kpart + ((long)z * a.M + m) * kld + c))
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int t = 0; t < IPT; ++t) {
+      const long i = i0 + t * stride;
+      rv[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < n) {
+        const int m = (int)(i / c4), c = (int)(i - (long)m * c4) * 4;
 #pragma unroll
-    for (int z = 0; z < ZMAX; ++z) {
-      acc[0] += v[z].x;
-      acc[1] += v[z].y;
-      acc[2] += v[z].z;
-      acc[3] += v[z].w;
+        for (int z = 0; z < KS; ++z)
+          v[t][z] = __ldcg(reinterpret_cast<const float4*>(kpart + ((long)z * a.M + m) * kld + c));
+        if (res) rv[t] = load_res4(a, m, a.kp_c0 + c, 4);
+      }
     }
-    const float4 y = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    if (a.nseg == 1) {
-      epilogue4(a, a.seg[0], m, a.kp_c0 + c, y, nullptr);
-    } else {
-      float* op = a.out + (long)m * a.ldo + a.kp_c0 + c;
-      if (aligned16(op)) *reinterpret_cast<float4*>(op) = y;
-      else for (int e = 0; e < 4; ++e) op[e] = acc[e];
+#pragma unroll
+    for (int t = 0; t < IPT; ++t) {
+      const long i = i0 + t * stride;
+      if (i >= n) break;
+      const int m = (int)(i / c4), c = (int)(i - (long)m * c4) * 4;
+      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int z = 0; z < KS; ++z) {
+        y.x += v[t][z].x; y.y += v[t][z].y; y.z += v[t][z].z; y.w += v[t][z].w;
+      }
+      if (a.nseg == 1) {
+        finish4(a, a.seg[0], m, a.kp_c0 + c, y, rv[t], 4);
+      } else {
+        float* op = a.out + (long)m * a.ldo + a.kp_c0 + c;
+        if (aligned16(op)) *reinterpret_cast<float4*>(op) = y;
+        else { op[0] = y.x; op[1] = y.y; op[2] = y.z; op[3] = y.w; }
+      }
     }
   }
 }
@@ -626,12 +655,38 @@ static bool make_map(CUtensorMap* map, const void* ptr, long cols, long rows, lo
 }
 
 // Sums the partials of output columns kp_c0 .. kp_c0 + ncols - 1 and applies the epilogue.
+template <int KS>
+static cudaError_t reduce_go(const MatArgs& a, cudaStream_t st, int ncols) {
+  static long wave = 0;                               // resident CTAs of this kernel
+  if (!wave) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 148;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, splitk_reduce_kernel<KS>, 256, 0) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    wave = (long)sms * per_sm;
+  }
+  const long n4 = (long)a.M * (ncols / 4);
+  long blocks = (n4 + 256L * reduce_ipt<KS>() - 1) / (256L * reduce_ipt<KS>());
+  if (blocks > wave) blocks = wave;
+  if (blocks < 1) blocks = 1;
+  return launch_kernel(splitk_reduce_kernel<KS>, dim3((unsigned)blocks), dim3(256), 0, st, 1, a, a.kpart, ncols);
+}
+
 static cudaError_t launch_splitk_reduce(const MatArgs& a, int ksplit, cudaStream_t st, int ncols = -1) {
   if (ncols < 0) ncols = a.nseg == 1 ? a.seg[0].rows : (int)a.ldo;
-  const long n4 = (long)a.M * (ncols / 4);
-  const long blocks = (n4 + 255) / 256;
-  return launch_kernel(splitk_reduce_kernel, dim3((unsigned)(blocks < 8192 ? blocks : 8192)), dim3(256), 0, st,
-                       1, a, a.kpart, ksplit, ncols);
+  switch (ksplit) {
+    case 2: return reduce_go<2>(a, st, ncols);
+    case 3: return reduce_go<3>(a, st, ncols);
+    case 4: return reduce_go<4>(a, st, ncols);
+    case 5: return reduce_go<5>(a, st, ncols);
+    case 6: return reduce_go<6>(a, st, ncols);
+    case 7: return reduce_go<7>(a, st, ncols);
+    case 8: return reduce_go<8>(a, st, ncols);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // K ranges for a launch of `ctas` CTAs that leaves SMs idle (single-segment launches, or
