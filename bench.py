@@ -807,6 +807,7 @@ def run_sweep(args):
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     hbm, _ = peaks()
+    tflops, _ = tensor_peak()
     Bs = [int(x) for x in args.sweep_b.split(",")]
     Ls = [int(x) for x in args.sweep_l.split(",")]
     Ns = [int(x) for x in args.sweep_n.split(",")]
@@ -863,6 +864,8 @@ def run_sweep(args):
                 heads_ms = t.get("heads_w1", 0) + t.get("heads_vocab", 0) + t.get("split_h", 0)
                 attn_ms = t.get("tree_attention", 0) + t.get("attn_combine", 0) + t.get("cast_q", 0)
                 sb = step_bytes(w, n1)
+                kf = kernel_flops(w, n1, plan_tc_heads(w))
+                ideal_us = sum(max(kb[k] / (hbm * 1e9), kf.get(k, 0) / (tflops * 1e12)) * 1e6 for k in kb)
                 row = {"sweep": "vicuna33b", "B": B, "prefix": L, "tree_nodes": n1,
                        "steps_per_s": round(1e3 / ms, 2), "ms_per_step": round(ms, 4),
                        "tree_nodes_per_s": round(1e3 / ms * B * n1, 1),
@@ -871,6 +874,7 @@ def run_sweep(args):
                        "medusa_heads_gbs": round((kb["heads_w1"] + kb["heads_vocab"])
                                                  / (heads_ms * 1e-3) / 1e9, 1),
                        "tree_attention_gbs": round(kb["tree_attention"] / (attn_ms * 1e-3) / 1e9, 1),
+                       "step_roofline_frac": round(ideal_us / (ms * 1e3), 4),
                        "kernels_us": {k: round(v * 1e3, 1) for k, v in t.items()},
                        "status": status}
                 print(json.dumps(row), flush=True)
