@@ -41,9 +41,15 @@ CASES = {
                             mode="typical", temperature=1.3, s=(4, 3, 2, 2), tree="cartesian",
                             N=4 + 12 + 24 + 48), None),
     "mid_fp32_gqa": (_mid(dtype="f32", d=96, V=700, lengths=(5, 70, 33)), None),
+    # fp32 batch of 6: the row-dot takes the activation rows in passes of 4, and every pass
+    # keeps candidate lists of its own for the fused top-k
+    "mid_fp32_b6": (_mid(dtype="f32", B=6, d=96, V=700, lengths=(3, 17, 40, 64, 90, 128)), None),
     # a vocabulary that is not a multiple of 4: scalar loads in the selection and the
     # verification statistics, ragged slices
     "mid_odd_vocab": (_mid(V=997, lengths=(12, 64, 129)), None),
+    # the same at batch 1: the row-dot path, whose candidate slots are its CTAs' row ranges
+    # (ragged against the heads' 997-row blocks)
+    "mid_b1_odd_vocab": (_mid(B=1, V=997, lengths=(77,)), None),
     # 151 nodes of one query head per KV head: two 128-row attention tiles, three tree-key
     # chunks, ancestors across the tile boundary
     "mid_n150_mha": (_mid(B=2, Hq=4, Hkv=4, N=150, lengths=(70, 200)), None),
