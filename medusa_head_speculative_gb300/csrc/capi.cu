@@ -787,7 +787,7 @@ medusa_status medusa_plan_create(const medusa_dims* dims, const medusa_tree_spec
   // boundaries when V allows (the selection then loads float4)
   {
     const long pairs = (long)dims->B * (p->K + 1);
-    const long wave = (long)std::max(1, heads_select_ctas_per_sm()) * p->num_sms;
+    const long wave = (long)std::max(1, topk_partial_ctas_per_sm()) * p->num_sms;
     const long lo = (dims->V + 4095) / 4096, hi = std::max(1, std::min(32, (dims->V + 1023) / 1024));
     const long sp = std::min<long>(32, std::max(lo, std::min(hi, wave / pairs)));
     p->topk_splits = (int)std::max(1L, sp);

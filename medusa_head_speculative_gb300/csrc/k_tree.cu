@@ -1,7 +1,10 @@
 // Candidate selection and tree construction of the Medusa step.
-//   topk_partial  per (sequence, head, vocab slice): the 16 best (logit, token) pairs
-//   tree_build    merge of the slices -> per-head top-s_k and the root; node tokens and
-//                 depth position ids; ancestor bitmask and root->leaf paths
+//   cand_select   the step's selection: per head the merge of the candidate lists that the
+//                 vocab projections wrote (fused top-k), then per sequence the root, the
+//                 heads' top-s_k and the node tokens and depth position ids
+//   topk_partial  (per-stage entry point, from stored logits) per (sequence, head, vocab
+//   topk_merge    slice) the 16 best (logit, token) pairs, then their merge
+//   tree_build    node tokens and depth position ids; ancestor bitmask and root->leaf paths
 //   rope_split    q/k/v of the tree nodes with rotary embedding at the node positions
 // Sources: "Medusa: Simple LLM Inference Acceleration Framework with Multiple Decoding
 // Heads" §3.4 Tree Attention, Steps 1-4; "MEDUSA 精读" section 6 (tree mask, tree position
@@ -184,48 +187,17 @@ cudaError_t launch_topk_merge(const MergeArgs& a, cudaStream_t st) {
   return launch_kernel(topk_merge_kernel, dim3(a.B), dim3(256), 0, st, 1, a);
 }
 
-// Fused selection for the whole step: every CTA takes the top-16 of one vocab slice of one
-// head; the last CTA to finish for a sequence (atomic counter, nothing waits) merges that
-// sequence's heads, picks the root and writes the node tokens and positions, then resets
-// the counter for the next launch.
-__global__ void __launch_bounds__(256) heads_select_kernel(TopkArgs t, MergeArgs m, TreeArgs tr,
-                                                           int32_t* counter) {
-  __shared__ float tv[MEDUSA_MAX_HEADS + 1][kTops];
-  __shared__ int ti[MEDUSA_MAX_HEADS + 1][kTops];
-  __shared__ int s_root, s_last;
-  pdl_trigger();
-  pdl_wait();
-  const int b = blockIdx.z;
-  slice_topk(t, blockIdx.x, blockIdx.y + t.k0, b);
-  if (threadIdx.x == 0) {          // thread 0 wrote this slice's candidates
-    __threadfence();
-    s_last = atomicAdd(counter + b, 1) == t.splits * (t.nh - t.k0) - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  merge_heads(m, b, tv, ti, &s_root);
-  node_tokens(tr, b, ti, s_root);
-  if (threadIdx.x == 0) counter[b] = 0;
-}
-
-int heads_select_ctas_per_sm() {
+int topk_partial_ctas_per_sm() {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, heads_select_kernel, 256, 0) != cudaSuccess) n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, topk_partial_kernel, 256, 0) != cudaSuccess) n = 0;
   return n;
-}
-
-cudaError_t launch_heads_select(const TopkArgs& t, const MergeArgs& m, const TreeArgs& tr,
-                                int32_t* counter, cudaStream_t st) {
-  dim3 grid(t.splits, t.nh - t.k0, t.B);
-  return launch_kernel(heads_select_kernel, grid, dim3(256), 0, st, 1, t, m, tr, counter);
 }
 
 // Selection from the fused top-k candidates: CTA (head k, sequence b) reads the head's
 // slot lists (each sorted, written by the projection's CTAs), thread t merging slots t,
 // t + 256, ... by insertion until an entry no longer enters; the warps' lists and then the
 // 8 warp lists are merged into the head's final list.  The last CTA of a sequence takes the
-// heads' final lists, picks the root and writes the node tokens as heads_select does.
+// heads' final lists, picks the root and writes the node tokens and positions.
 __global__ void __launch_bounds__(256) cand_select_kernel(CandArgs c, MergeArgs m, TreeArgs tr,
                                                           int32_t* counter) {
   __shared__ float sv[8][kTops];

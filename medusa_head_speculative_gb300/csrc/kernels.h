@@ -139,17 +139,13 @@ struct TreeArgs {
   uint32_t* status;
 };
 cudaError_t launch_tree_build(const TreeArgs& a, cudaStream_t st);
-// Fused slice top-k + head merge + node tokens/positions (tr.mask/retrieve unused).
-// counter: [B] zeros on entry; left at zero on exit.
-cudaError_t launch_heads_select(const TopkArgs& t, const MergeArgs& m, const TreeArgs& tr,
-                                int32_t* counter, cudaStream_t st);
-// Resident 256-thread selection CTAs per SM (0 when the query fails).
-int heads_select_ctas_per_sm();
+// Resident 256-thread slice top-k CTAs per SM (0 when the query fails).
+int topk_partial_ctas_per_sm();
 
 // Selection from the fused top-k candidates (MatSeg::cand): CTA (head, sequence) merges
 // the head's `count[head]` slot lists into its final top list (fin_val / fin_idx,
 // [B][nh][kTops]); the last CTA of a sequence (atomic counter, reset on exit) merges the
-// heads, picks the root and writes the node tokens and positions, as heads_select does.
+// heads, picks the root and writes the node tokens and positions.
 struct CandArgs {
   const float* cand_val; const int32_t* cand_idx;     // [B][nh][ld][kTops]
   int B, nh, ld, k0;
