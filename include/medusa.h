@@ -248,8 +248,11 @@ medusa_status medusa_heads(const medusa_plan* plan, const float* h, const int32_
  * returned).  Its scratch lives in one library-owned device array of
  * MEDUSA_NOALLOC_SCRATCH_BYTES, present on every GPU that loads the library until the
  * process exits; no cudaMalloc, cudaFree or other allocating call is made.
- *   - Plans whose heads scratch exceeds the array (about B*(K+1)*V*4 bytes of logits plus
- *     small extras) get MEDUSA_ERR_UNSUPPORTED and nothing is launched.
+ *   - Like the step, it keeps no logits: the vocab projections keep each CTA's best
+ *     candidates and a selection merges them.  Plans whose heads scratch exceeds the array
+ *     (about B*(K+1)*slots*128 bytes of candidate lists, slots = V/128 from batch 2 and a
+ *     few hundred at batch 1, plus B*K*d*8 bytes of head activations) get
+ *     MEDUSA_ERR_UNSUPPORTED and nothing is launched.
  *   - The first call on a device looks up the array's address with that device current;
  *     make that first call before any stream capture begins.  The address is kept per
  *     device and context; the first call after a cudaDeviceReset looks it up again and

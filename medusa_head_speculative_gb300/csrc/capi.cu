@@ -229,27 +229,13 @@ medusa_status check_ws(const medusa_plan* p, void* ws, size_t bytes) {
 inline cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 // ------------------------------------------------------------------ stage bodies
-// Slots that the heads launch `a` writes for fused top-k segment si (the selection merges
-// that many lists): the 128-row tiles on the tensor-core path, the row-dot CTAs covering
-// the block otherwise (grid: rowdot_grid of the same launch).
-long cand_slots(const medusa_plan* p, const MatArgs& a, int si, long grid) {
-  if (p->tc_heads) return (a.seg[si].rows + kCandTileRows - 1) / kCandTileRows;
-  long total = 0, s0 = 0;
-  for (int i = 0; i < a.nseg; ++i) {
-    if (i < si) s0 += a.seg[i].rows;
-    total += a.seg[i].rows;
-  }
-  if (grid < 1) return -1;
-  return rowdot_cta_of(s0 + a.seg[si].rows - 1, total, grid) - rowdot_cta_of(s0, total, grid) + 1;
-}
-
-// Upper bound of cand_slots over the heads launches a step makes: with the row-dot the LM
-// head (when computed) joins the first launch after the K blocks of d rows and the second
-// launch has the K heads' blocks of V rows.
+// Upper bound of the fused top-k's slots over the heads launches a step makes: with the
+// row-dot the LM head (when computed) joins the first launch after the K blocks of d rows
+// and the second launch has the K heads' blocks of V rows.
 int plan_cand_ld(const medusa_plan* p) {
   const medusa_dims& d = p->d;
   if (p->tc_heads) return (d.V + kCandTileRows - 1) / kCandTileRows;
-  long most = 1;
+  int most = 1;
   for (int first = 0; first < 2; ++first) {
     MatArgs a{};
     a.M = d.B;
@@ -259,10 +245,12 @@ int plan_cand_ld(const medusa_plan* p) {
       a.seg[i].rows = first && i < p->K ? d.d : d.V;
       a.seg[i].cand = !first || i == p->K;           // flagged as heads_impl flags them
     }
-    const long grid = rowdot_grid(a, d.dtype);
-    for (int i = first ? p->K : 0; i < a.nseg; ++i) most = std::max(most, cand_slots(p, a, i, grid));
+    for (int i = first ? p->K : 0; i < a.nseg; ++i) {
+      int n = 0, c0 = 0;
+      if (cand_geometry(a, i, false, d.dtype, &n, &c0)) most = std::max(most, n);
+    }
   }
-  return (int)most;
+  return most;
 }
 
 // The heads' projections.  cand_count null: the logits of the computed heads go to
@@ -327,18 +315,11 @@ medusa_status heads_impl(const medusa_plan* p, const float* h, const int32_t* ro
       x.seg[i].head = head0 + i;
       x.seg[i].rounds = p->need[head0 + i];
     }
-    const long grid = p->tc_heads ? 0 : rowdot_grid(x, d.dtype);
-    long total = 0;
-    for (int i = 0; i < x.nseg; ++i) total += x.seg[i].rows;
-    long s0 = 0;
-    for (int i = 0; i < x.nseg; ++i) {
-      if (i >= i0) {
-        const long n = cand_slots(p, x, i, grid);
-        if (n < 1 || n > p->cand_ld) return false;
-        cand_count[head0 + i] = (int)n;
-        if (!p->tc_heads) x.seg[i].slot0 = (int)rowdot_cta_of(s0, total, grid);
-      }
-      s0 += x.seg[i].rows;
+    for (int i = i0; i < x.nseg; ++i) {
+      int n = 0, c0 = 0;
+      if (!cand_geometry(x, i, p->tc_heads, d.dtype, &n, &c0) || n < 1 || n > p->cand_ld) return false;
+      cand_count[head0 + i] = n;
+      x.seg[i].slot0 = c0;
     }
     return true;
   };

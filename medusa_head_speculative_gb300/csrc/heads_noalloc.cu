@@ -5,21 +5,23 @@
 // plug-in that lives inside another framework's memory pool and may not call cudaMalloc
 // behind its back, or code that must not allocate because the stream may be in the
 // middle of being captured into a CUDA graph.  This entry point needs no workspace from
-// them: its scratch (the logits, the head activations and the top-k candidates) lives in
+// them: its scratch (the head activations and the fused top-k's candidate lists) lives in
 // one fixed array in device global memory that belongs to this library.
 //
 // Limits and behaviour:
 //   * The array holds MEDUSA_NOALLOC_SCRATCH_BYTES (4 MiB) on every GPU that loads the
 //     library, for as long as the process lives.  Plans whose heads scratch needs more
-//     (roughly B * (K+1) * V * 4 bytes of logits plus small extras) are rejected with
-//     MEDUSA_ERR_UNSUPPORTED before anything is launched.
+//     (the candidate lists, B * (K+1) * slots * 128 bytes with slots = V/128 at batch >= 2
+//     and up to a few hundred at batch 1, plus B * K * d * 8 bytes of head activations) are
+//     rejected with MEDUSA_ERR_UNSUPPORTED before anything is launched.
 //   * The first call on a device looks up the array's device address (a CUDA runtime
 //     symbol lookup, no allocation) with that device current; make that first call
 //     before starting any stream capture.  The address is kept per device and CUDA
 //     context: after cudaDeviceReset the next call looks it up again, so that call too
 //     should come before any capture.
 //   * Every call shares the one array and leaves its last contents there; nothing in it
-//     has to start at zero, since each call overwrites everything it reads.  Calls whose
+//     has to start at zero (each call clears its completion counts with a memset and
+//     overwrites everything else it reads).  Calls whose
 //     GPU work overlaps (different streams, or different plans at the same time) race on
 //     the array: order them on one stream.
 #include <cuda.h>
@@ -89,23 +91,25 @@ medusa_status scratch_address(void** out) {
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct Layout {
-  size_t logits, u, uhi, ulo, hhi, hlo, cv, ci, total;
+  size_t u, uhi, ulo, hhi, hlo, cv, ci, fv, fi, cnt, total;
 };
 
-Layout layout_of(const HeadsPlanView& v) {
-  const size_t B = v.dims.B, K = v.K, V = v.dims.V, D = v.dims.d;
+Layout layout_of(const HeadsPlanView& v, int ld) {
+  const size_t B = v.dims.B, K = v.K, D = v.dims.d;
   const size_t tc = v.tc_heads ? 1 : 0;
   Layout l{};
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = up256(off + bytes); return o; };
-  l.logits = take(B * (K + 1) * V * 4);
   l.u = take(B * K * D * 4);
   l.uhi = take(tc * B * K * D * 2);
   l.ulo = take(tc * B * K * D * 2);
   l.hhi = take(tc * B * D * 2);
   l.hlo = take(tc * B * D * 2);
-  l.cv = take(B * (K + 1) * v.topk_splits * kTops * 4);
-  l.ci = take(B * (K + 1) * v.topk_splits * kTops * 4);
+  l.cv = take(B * (K + 1) * (size_t)ld * kTops * 4);
+  l.ci = take(B * (K + 1) * (size_t)ld * kTops * 4);
+  l.fv = take(B * (K + 1) * kTops * 4);
+  l.fi = take(B * (K + 1) * kTops * 4);
+  l.cnt = take(B * 4);
   l.total = off;
   return l;
 }
@@ -114,6 +118,9 @@ bool ok16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+// The heads' projections with the fused top-k (each CTA keeps its rows' best candidates;
+// no logits) and the candidate selection, as the step runs them, but with all 16 ranks of
+// every head kept, as medusa_heads() returns them.
 extern "C" medusa_status medusa_heads_noalloc(const medusa_plan* plan, const float* h,
                                               const int32_t* root_in, const medusa_weights* w,
                                               int32_t* topk_tok, float* topk_val, int32_t* root,
@@ -121,75 +128,127 @@ extern "C" medusa_status medusa_heads_noalloc(const medusa_plan* plan, const flo
   EntryScope scope("medusa_heads_noalloc");
   HeadsPlanView v;
   if (!heads_plan_view(plan, &v)) return MEDUSA_ERR_INVALID;
-  const Layout l = layout_of(v);
+  const int B = v.dims.B, K = v.K, D = v.dims.d, V = v.dims.V;
+  const size_t es = v.dims.dtype == MEDUSA_F32 ? 4 : 2;
+  const bool tc = v.tc_heads;
+
+  // u_k = SiLU(W1_k h) + h; on the row-dot path z_0 = LM h joins this launch when the root
+  // is not given
+  MatArgs a{};
+  a.nseg = K;
+  a.M = B;
+  a.k = D;
+  a.ldo = (long)K * D;
+  a.epi = EPI_SILU_RES;
+  a.res_f32 = h;
+  a.ldr = D;
+  for (int k = 0; k < K; ++k) {
+    a.seg[k].rows = D;
+    a.seg[k].out_off = k * D;
+  }
+  const bool lm_first = !tc && !root_in;
+  if (lm_first) {
+    a.seg[K].rows = V;
+    a.seg[K].cand = 1;
+    a.seg[K].head = 0;
+    a.seg[K].rounds = kTops;
+    a.nseg = K + 1;
+  }
+  // z_k = W2_k u_k (and z_0 here when it did not join the first launch)
+  const int k0 = root_in || lm_first ? 1 : 0;
+  MatArgs b{};
+  b.nseg = K + 1 - k0;
+  b.M = B;
+  b.k = D;
+  b.epi = EPI_STORE;
+  for (int i = 0; i < b.nseg; ++i) {
+    b.seg[i].rows = V;
+    b.seg[i].cand = 1;
+    b.seg[i].head = i + k0;
+    b.seg[i].rounds = kTops;
+  }
+  // candidate slots of both launches, then the scratch they need
+  int count[MEDUSA_MAX_HEADS + 1] = {0};
+  int ld = 1;
+  auto geometry = [&](MatArgs& x, int i0) -> bool {
+    for (int i = i0; i < x.nseg; ++i) {
+      int n = 0, c0 = 0;
+      if (!cand_geometry(x, i, tc, v.dims.dtype, &n, &c0) || n < 1) return false;
+      x.seg[i].slot0 = c0;
+      count[x.seg[i].head] = n;
+      ld = n > ld ? n : ld;
+    }
+    return true;
+  };
+  if ((lm_first && !geometry(a, K)) || !geometry(b, 0)) return MEDUSA_ERR_CUDA;
+  const Layout l = layout_of(v, ld);
   if (l.total > (size_t)MEDUSA_NOALLOC_SCRATCH_BYTES) return MEDUSA_ERR_UNSUPPORTED;
   if (!h || !w || !topk_tok || !topk_val || !root) return MEDUSA_ERR_INVALID;
-  if (!ok16(w->w1) || !ok16(w->w2) || !ok16(w->lm)) return MEDUSA_ERR_INVALID;
+  if (!ok16(w->w1) || !ok16(w->w2) || (!root_in && !ok16(w->lm))) return MEDUSA_ERR_INVALID;
   void* base = nullptr;
   medusa_status s = scratch_address(&base);
   if (s != MEDUSA_OK) return s;
   char* sc = static_cast<char*>(base);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int B = v.dims.B, K = v.K, D = v.dims.d, V = v.dims.V;
-  const size_t es = v.dims.dtype == MEDUSA_F32 ? 4 : 2;
-  float* logits = reinterpret_cast<float*>(sc + l.logits);
   float* u = reinterpret_cast<float*>(sc + l.u);
-  bf16* uhi = v.tc_heads ? reinterpret_cast<bf16*>(sc + l.uhi) : nullptr;
-  bf16* ulo = v.tc_heads ? reinterpret_cast<bf16*>(sc + l.ulo) : nullptr;
-  bf16* hhi = v.tc_heads ? reinterpret_cast<bf16*>(sc + l.hhi) : nullptr;
-  bf16* hlo = v.tc_heads ? reinterpret_cast<bf16*>(sc + l.hlo) : nullptr;
+  bf16* uhi = tc ? reinterpret_cast<bf16*>(sc + l.uhi) : nullptr;
+  bf16* ulo = tc ? reinterpret_cast<bf16*>(sc + l.ulo) : nullptr;
+  bf16* hhi = tc ? reinterpret_cast<bf16*>(sc + l.hhi) : nullptr;
+  bf16* hlo = tc ? reinterpret_cast<bf16*>(sc + l.hlo) : nullptr;
+  float* cv = reinterpret_cast<float*>(sc + l.cv);
+  int32_t* ci = reinterpret_cast<int32_t*>(sc + l.ci);
+  float* fv = reinterpret_cast<float*>(sc + l.fv);
+  int32_t* fi = reinterpret_cast<int32_t*>(sc + l.fi);
+  int32_t* cnt = reinterpret_cast<int32_t*>(sc + l.cnt);
+  // the selection's completion counts start at zero (a memset, not an allocation)
+  if (cudaMemsetAsync(cnt, 0, sizeof(int32_t) * B, st) != cudaSuccess) return MEDUSA_ERR_CUDA;
 
-  // u_k = SiLU(W1_k h) + h
-  MatArgs a{};
-  a.nseg = K;
-  a.M = B;
-  a.k = D;
   a.out = u;
-  a.ldo = (long)K * D;
-  a.epi = EPI_SILU_RES;
-  a.res_f32 = h;
-  a.ldr = D;
   a.out_hi = uhi;
   a.out_lo = ulo;
-  if (v.tc_heads && launch_split(h, hhi, hlo, (long)B * D, st) != cudaSuccess) return MEDUSA_ERR_CUDA;
   for (int k = 0; k < K; ++k) {
     MatSeg& g = a.seg[k];
     g.w = static_cast<const char*>(w->w1) + (size_t)k * D * D * es;
     g.x = h; g.a_hi = hhi; g.a_lo = hlo; g.ldx = D;
-    g.rows = D;
-    g.out_off = k * D;
   }
-  if ((v.tc_heads ? launch_umma_gemm(a, v.status, st) : launch_rowdot(a, v.dims.dtype, st)) != cudaSuccess)
-    return MEDUSA_ERR_CUDA;
-  // z_0 = LM h, z_k = W2_k u_k
-  MatArgs b{};
-  b.nseg = K + 1;
-  b.M = B;
-  b.k = D;
-  b.out = logits;
-  b.ldo = (long)(K + 1) * V;
-  b.epi = EPI_STORE;
-  b.seg[0].w = w->lm;
-  b.seg[0].x = h; b.seg[0].a_hi = hhi; b.seg[0].a_lo = hlo; b.seg[0].ldx = D;
-  b.seg[0].rows = V;
-  b.seg[0].out_off = 0;
-  for (int k = 1; k <= K; ++k) {
-    MatSeg& g = b.seg[k];
-    g.w = static_cast<const char*>(w->w2) + (size_t)(k - 1) * V * D * es;
-    g.x = u + (size_t)(k - 1) * D;
-    g.a_hi = uhi ? uhi + (size_t)(k - 1) * D : nullptr;
-    g.a_lo = ulo ? ulo + (size_t)(k - 1) * D : nullptr;
-    g.ldx = (long)K * D;
-    g.rows = V;
-    g.out_off = k * V;
+  if (lm_first) {
+    a.seg[K].w = w->lm;
+    a.seg[K].x = h;
+    a.seg[K].ldx = D;
   }
-  if ((v.tc_heads ? launch_umma_gemm(b, v.status, st) : launch_rowdot(b, v.dims.dtype, st)) != cudaSuccess)
+  for (MatArgs* x : {&a, &b}) {
+    x->cand_val = cv;
+    x->cand_idx = ci;
+    x->cand_nh = K + 1;
+    x->cand_ld = ld;
+  }
+  if (tc && launch_split(h, hhi, hlo, (long)B * D, st) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  if ((tc ? launch_umma_gemm(a, v.status, st) : launch_rowdot(a, v.dims.dtype, st)) != cudaSuccess)
     return MEDUSA_ERR_CUDA;
-  float* cv = reinterpret_cast<float*>(sc + l.cv);
-  int32_t* ci = reinterpret_cast<int32_t*>(sc + l.ci);
-  TopkArgs t{logits, B, K + 1, V, v.topk_splits, v.topk_chunk, cv, ci};
-  if (launch_topk_partial(t, st) != cudaSuccess) return MEDUSA_ERR_CUDA;
-  MergeArgs mg{cv, ci, B, K, V, v.topk_splits, root_in, topk_tok, topk_val, root, v.status};
-  if (launch_topk_merge(mg, st) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  for (int i = 0; i < b.nseg; ++i) {
+    MatSeg& g = b.seg[i];
+    const int k = i + k0;                                  // 0: the LM head
+    if (k == 0) {
+      g.w = w->lm;
+      g.x = h; g.a_hi = hhi; g.a_lo = hlo; g.ldx = D;
+    } else {
+      g.w = static_cast<const char*>(w->w2) + (size_t)(k - 1) * V * D * es;
+      g.x = u + (size_t)(k - 1) * D;
+      g.a_hi = uhi ? uhi + (size_t)(k - 1) * D : nullptr;
+      g.a_lo = ulo ? ulo + (size_t)(k - 1) * D : nullptr;
+      g.ldx = (long)K * D;
+    }
+  }
+  if ((tc ? launch_umma_gemm(b, v.status, st) : launch_rowdot(b, v.dims.dtype, st)) != cudaSuccess)
+    return MEDUSA_ERR_CUDA;
+  CandArgs c{cv, ci, B, K + 1, ld, root_in ? 1 : 0};
+  for (int k = 0; k <= K; ++k) { c.count[k] = count[k]; c.rounds[k] = kTops; }
+  c.fin_val = fv;
+  c.fin_idx = fi;
+  MergeArgs mg{fv, fi, B, K, V, 1, root_in, topk_tok, topk_val, root, v.status};
+  mg.k0 = c.k0;
+  TreeArgs tr{};                                           // no tree: selection only
+  tr.n1 = 0;
+  if (launch_cand_select(c, mg, tr, cnt, st) != cudaSuccess) return MEDUSA_ERR_CUDA;
   return MEDUSA_OK;
 }

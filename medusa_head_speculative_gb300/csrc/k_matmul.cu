@@ -253,6 +253,25 @@ cudaError_t launch_rowdot(const MatArgs& a, int dtype, cudaStream_t st) {
   });
 }
 
+bool cand_geometry(const MatArgs& a, int si, bool tensor_cores, int dtype, int* count, int* first) {
+  if (tensor_cores) {
+    *count = (a.seg[si].rows + kCandTileRows - 1) / kCandTileRows;
+    *first = 0;
+    return true;
+  }
+  const long grid = rowdot_grid(a, dtype);
+  if (grid < 1) return false;
+  long total = 0, s0 = 0;
+  for (int i = 0; i < a.nseg; ++i) {
+    if (i < si) s0 += a.seg[i].rows;
+    total += a.seg[i].rows;
+  }
+  const long c0 = rowdot_cta_of(s0, total, grid), c1 = rowdot_cta_of(s0 + a.seg[si].rows - 1, total, grid);
+  *count = (int)(c1 - c0 + 1);
+  *first = (int)c0;
+  return true;
+}
+
 int rowdot_grid(const MatArgs& a, int dtype) {
   return (int)rowdot_dispatch(a, dtype, [&](auto mt, auto w, auto cm) {
     return rowdot_grid_t<decltype(w), decltype(mt)::value, decltype(cm)::value>(

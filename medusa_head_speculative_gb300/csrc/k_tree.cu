@@ -163,6 +163,7 @@ __device__ void merge_heads(const MergeArgs& a, int b, float (*tv)[kTops], int (
 
 // Node tokens and position ids of sequence b, from the merged lists in shared memory.
 __device__ void node_tokens(const TreeArgs& a, int b, const int (*ti)[kTops], int root) {
+  if (a.n1 <= 0) return;                     // selection only (no tree)
   int L = a.len[b];
   if (L < 0) L = 0;
   for (int n = threadIdx.x; n < a.n1; n += blockDim.x) {

@@ -95,6 +95,11 @@ __host__ __device__ inline long rowdot_cta_of(long x, long total, long grid) {
 }
 // Tensor-core path with fused top-k: 128-row tiles of a block (its slots).
 constexpr int kCandTileRows = 128;
+// Fused top-k geometry of segment si of a heads launch `a` (its `cand` flags set as
+// launched): the candidate slots it writes per (activation row, head), and on the row-dot
+// path the first CTA covering it (MatSeg::slot0; 0 on the tensor-core path, whose slots are
+// its 128-row tiles).  False when the row-dot's launch geometry cannot be had.
+bool cand_geometry(const MatArgs& a, int si, bool tensor_cores, int dtype, int* count, int* first);
 // Tensor-core (tcgen05 + TMA + TMEM) projection; bf16 weights only.  Sets
 // MEDUSA_FLAG_TIMEOUT in *status if a pipeline wait expires.
 cudaError_t launch_umma_gemm(const MatArgs& a, uint32_t* status, cudaStream_t st);

@@ -44,10 +44,9 @@ def test_noalloc_heads_matches_workspace_heads(w):
         root = torch.full((B,), -7, **i32)
         Bnd.heads_noalloc(p, dev.h, None, dev.wstruct, tok, val, root)
         torch.cuda.synchronize()
-        for k in range(K):
-            s = w.s[k]
-            np.testing.assert_array_equal(tok[:, k, :s].cpu().numpy(), ref_tok[:, k, :s].cpu().numpy())
-            assert close(val[:, k, :s].cpu().numpy(), ref_val[:, k, :s].cpu().numpy(), ATOL, RTOL) <= 0
+        for k in range(K):                                   # all 16 ranks, as medusa_heads
+            np.testing.assert_array_equal(tok[:, k].cpu().numpy(), ref_tok[:, k].cpu().numpy())
+            assert close(val[:, k].cpu().numpy(), ref_val[:, k].cpu().numpy(), ATOL, RTOL) <= 0
         np.testing.assert_array_equal(root.cpu().numpy(), ref_root.cpu().numpy())
     assert p.status() == 0
 
@@ -64,9 +63,17 @@ def test_noalloc_heads_carries_root_in():
     assert root.tolist() == [5, 6, 7]
 
 
+def test_noalloc_heads_batch8_full_vocab():
+    # batch 8 of a 32000-token vocabulary: 8*5*32000*4 bytes of logits would not fit the
+    # 4 MiB array, the fused top-k's candidate lists (8*5*250*128 bytes) do
+    w = S.Workload("noalloc_b8", B=8, d=256, V=32000, Hq=4, Hkv=4, dh=64, K=4, dtype="bf16",
+                   lengths=(5, 9, 17, 33, 65, 100, 120, 127), tree="greedy", s=(10, 10, 10, 10), N=30)
+    test_noalloc_heads_matches_workspace_heads(w)
+
+
 def test_noalloc_heads_rejects_plans_past_the_scratch_limit():
-    # batch 8 of a 32000-token vocabulary needs 8*5*32000*4 bytes of logits > 4 MiB
-    p = Bnd.Plan(8, 256, 32000, 4, 4, 4, 64, Bnd.BF16, 64, (2, 2, 2, 2),
+    # batch 64 of a 32000-token vocabulary: 64*5*250*128 bytes of candidate lists > 4 MiB
+    p = Bnd.Plan(64, 256, 32000, 4, 4, 4, 64, Bnd.BF16, 64, (2, 2, 2, 2),
                  *Bnd.tree_cartesian((2, 2, 2, 2)))
     dummy = torch.zeros(64, dtype=torch.int32, device="cuda")
     with pytest.raises(Bnd.MedusaError) as e:
